@@ -1,0 +1,190 @@
+/*
+ * motion.h -- C ABI of the GB300 integer motion / PSNR-SSE library
+ * (libmotion_gb300.so, built for sm_103a).
+ *
+ * What it computes (the integer motion feature of a video-quality pipeline):
+ *   For each frame F (h rows x w columns, bpc bits per sample):
+ *     V[y][x] = (sum_k t_k F[mirror(y+k-2, h)][x] + 2^(bpc-1)) >> bpc
+ *     B[y][x] = (sum_k t_k V[y][mirror(x+k-2, w)] + 2^15) >> 16
+ *   with t = {3571, 16004, 26386, 16004, 3571} (sum 65536) and
+ *   mirror(i, n) = i < 0 ? -i : (i >= n ? 2n - i - 2 : i);
+ *     SAD_i     = sum_{y,x} |B_i[y][x] - B_{i-1}[y][x]|   (uint64, exact)
+ *     score_i   = ((double)SAD_i / 256.0) / (double)(w * h)
+ *     motion2_i = min(score_i, score_{i+1})
+ *   and, per plane of a reference/distorted pair,
+ *     SSE = sum (ref - dist)^2                             (uint64, exact).
+ *
+ * Sources, by page title and section:
+ *   "ADR-1392: CUDA motion, PSNR and moment kernels add one atomic per block,
+ *   the motion SAD filters separably, and PSNR selects its plane with constant
+ *   indices" -- Context (one integer per pixel summed into one 64-bit value,
+ *   equal to the CPU bit for bit; order-independent, so any reduction order is
+ *   exact), Decision 1 (one atomic per block), Decision 3 (planes selected with
+ *   constant indices), Decision 4 (vertical pass first, rounded >> bpc, then
+ *   the horizontal taps, rounded >> 16).
+ *   "ADR-1380: The CUDA SpEED twins are device-resident ..." -- Decision
+ *   (submit enqueues on the caller's stream; one small readback per frame).
+ *   "Making it fast: three rounds on one pipeline" -- Round 1 (batched launches,
+ *   one kernel over all frames), Round 2 (no allocation on the hot path).
+ *
+ * Conventions for every entry point:
+ *   - Return 0 (MOTION_OK) on success or a MOTION_ERR_* code; nothing is written
+ *     to an output on error.  motion_strerror() names a code.
+ *   - "d_" pointers are device memory (cudaMalloc / PyTorch CUDA tensors) owned
+ *     by the caller; "h_" pointers are host memory owned by the caller (pinned
+ *     memory gives full copy speed; pageable memory works).
+ *   - stream is a cudaStream_t passed as void* (NULL = the legacy default
+ *     stream).  Device-result calls only enqueue work on it.
+ *   - Samples are uint8 when bpc == 8 and little-endian uint16 when
+ *     9 <= bpc <= 16.  Values >= 2^bpc violate a precondition and give
+ *     unspecified (but memory-safe) results.  uint16 planes must be 2-byte
+ *     aligned (pointer, pitch and frame stride).
+ *   - pitch / stride arguments are in BYTES.
+ *   - Frames must be at least 3 x 3 (the mirror rule needs n >= 3) and at most
+ *     MOTION_MAX_DIM on each side.
+ *   - Calls on one context must not overlap (one stream per context, or
+ *     ordered by the caller); distinct contexts are independent.
+ */
+#ifndef MOTION_GB300_H
+#define MOTION_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MOTION_MAX_DIM 32768
+
+#if defined(__GNUC__)
+#define MOTION_API __attribute__((visibility("default")))
+#else
+#define MOTION_API
+#endif
+
+enum motion_status {
+    MOTION_OK = 0,
+    MOTION_ERR_INVALID_ARGUMENT = 1,   /* NULL pointer, n < 0, bad plane index */
+    MOTION_ERR_FRAME_TOO_SMALL = 2,     /* w < 3 or h < 3 */
+    MOTION_ERR_UNSUPPORTED_BITDEPTH = 3,/* bpc outside [8, 16] */
+    MOTION_ERR_BAD_PITCH = 4,           /* pitch < w * sample size, or misaligned uint16 layout */
+    MOTION_ERR_TOO_LARGE = 5,           /* w or h > MOTION_MAX_DIM */
+    MOTION_ERR_CUDA = 6,                /* a CUDA runtime call failed (motion_last_cuda_error) */
+    MOTION_ERR_OUT_OF_MEMORY = 7,       /* device or pinned allocation failed */
+    MOTION_ERR_NO_DEVICE = 8,           /* no CUDA device visible */
+    MOTION_ERR_WRONG_DEVICE = 9         /* called with a device other than the context's */
+};
+
+typedef struct motion_ctx motion_ctx;  /* opaque, library-owned */
+
+/* Create a motion context for frames of w x h samples at bpc bits on the
+ * current CUDA device.  All device scratch (the previous frame's blurred plane,
+ * w*h uint16) is allocated here, never on a submit.  *out receives the handle. */
+MOTION_API int motion_init(int w, int h, int bpc, motion_ctx** out);
+
+/* Free the context and its device memory.  NULL is accepted. */
+MOTION_API int motion_destroy(motion_ctx* ctx);
+
+/* Start a new sequence: the next frame submitted has SAD 0 / score 0. */
+MOTION_API int motion_reset(motion_ctx* ctx);
+
+/* Submit ONE frame (device memory, pitch_bytes between rows).  Enqueues the
+ * blur + SAD on `stream`, waits for it, and returns the frame's SAD against
+ * the previously submitted frame (0 for the first frame of a sequence) and its
+ * score.  Either output pointer may be NULL.  Follows the submit / collect
+ * pattern with one 8-byte readback per frame (ADR-1380, Decision). */
+MOTION_API int motion_submit(motion_ctx* ctx, const void* d_frame, size_t pitch_bytes,
+                  void* stream, uint64_t* sad_out, double* score_out);
+
+/* Submit n frames in ONE launch (ADR-1392 Decision 1; "Making it fast",
+ * Round 1, batched launches).  Frame i starts at d_frames + i*frame_stride
+ * bytes.  d_sad_out (device, n uint64) receives SAD_i against frame i-1; SAD_0
+ * is against the last frame of the previous submit on this context, or 0 at
+ * the start of a sequence.  Asynchronous: only enqueues on `stream`.  n == 0
+ * is a no-op. */
+MOTION_API int motion_submit_batch(motion_ctx* ctx, const void* d_frames, int n,
+                        size_t frame_stride_bytes, size_t pitch_bytes,
+                        void* stream, uint64_t* d_sad_out);
+
+/* Fused pass over n 4:2:0 reference/distorted picture pairs in ONE launch:
+ * motion SAD on the reference luma (continuing the context's sequence, as
+ * motion_submit_batch) and SSE of each plane Y, U, V of every pair.
+ * Luma planes are ctx w x h; chroma planes ceil(w/2) x ceil(h/2).  Reference
+ * and distorted pictures share one layout: pitch_y / pitch_uv between rows,
+ * stride_y / stride_uv between pairs.  d_sad_out: device uint64[n];
+ * d_sse_out: device uint64[n][3] (Y, U, V).  Asynchronous. */
+MOTION_API int motion_psnr_yuv420_batch(motion_ctx* ctx, int n,
+                             const void* d_ref_y, const void* d_ref_u,
+                             const void* d_ref_v, const void* d_dist_y,
+                             const void* d_dist_u, const void* d_dist_v,
+                             size_t pitch_y, size_t pitch_uv,
+                             size_t stride_y, size_t stride_uv, void* stream,
+                             uint64_t* d_sad_out, uint64_t* d_sse_out);
+
+/* The same fused pass with HOST pictures and HOST results: the library copies
+ * chunks of pairs host->device into its own staging buffers (allocated on the
+ * first call and kept; size them with motion_reserve_host_staging to keep the
+ * first call allocation-free) on two streams so that copies overlap the
+ * kernels, and copies the results back.  Blocks until h_sad_out (uint64[n])
+ * and h_sse_out (uint64[n][3]) are written.  Host planes are tightly packed
+ * with the given pitches and strides.  Pinned host memory recommended. */
+MOTION_API int motion_psnr_yuv420_batch_host(motion_ctx* ctx, int n,
+                                  const void* h_ref_y, const void* h_ref_u,
+                                  const void* h_ref_v, const void* h_dist_y,
+                                  const void* h_dist_u, const void* h_dist_v,
+                                  size_t pitch_y, size_t pitch_uv,
+                                  size_t stride_y, size_t stride_uv,
+                                  uint64_t* h_sad_out, uint64_t* h_sse_out);
+
+/* Allocate the two device staging sets, result buffers and streams used by
+ * motion_psnr_yuv420_batch_host, for chunks of `pairs_per_chunk` pairs whose
+ * planes are stride_y / stride_uv bytes apart (0 picks about 64 MB of pictures
+ * per chunk; a stride of 0 means tightly packed rows).  Kept until destroy;
+ * a later call with a larger need reallocates. */
+MOTION_API int motion_reserve_host_staging(motion_ctx* ctx, int pairs_per_chunk,
+                                size_t stride_y, size_t stride_uv);
+
+/* SSE of one plane pair (ADR-1392 Context / Decision 2): d_sse_out (device,
+ * one uint64) receives sum (ref - dist)^2.  Stateless; asynchronous. */
+MOTION_API int psnr_sse(const void* d_ref, const void* d_dist, size_t ref_pitch,
+             size_t dist_pitch, int w, int h, int bpc, void* stream,
+             uint64_t* d_sse_out);
+
+/* SSE of all three planes of n 4:2:0 pairs in ONE launch, planes selected
+ * with constant indices (ADR-1392 Decision 3).  Layout as in
+ * motion_psnr_yuv420_batch; d_sse_out: device uint64[n][3].  Stateless. */
+MOTION_API int psnr_sse_yuv420_batch(int w, int h, int bpc, int n,
+                          const void* d_ref_y, const void* d_ref_u,
+                          const void* d_ref_v, const void* d_dist_y,
+                          const void* d_dist_u, const void* d_dist_v,
+                          size_t pitch_y, size_t pitch_uv, size_t stride_y,
+                          size_t stride_uv, void* stream, uint64_t* d_sse_out);
+
+/* Host helper: score_i = (SAD_i / 256) / (w h) and motion2_i =
+ * min(score_i, score_{i+1}); motion2_{n-1} = score_{n-1} unless next_score
+ * (the score of the frame after the last, e.g. from the next shard) is
+ * non-NULL.  All pointers are host memory. */
+MOTION_API int motion_scores_from_sad(const uint64_t* sad, int n, int w, int h,
+                           const double* next_score, double* score,
+                           double* motion2);
+
+/* Host helper: mse = SSE / n_samples and psnr_db = 10 log10((2^bpc-1)^2 /
+ * mse), +inf when SSE == 0 (no cap). */
+MOTION_API int psnr_from_sse(uint64_t sse, uint64_t n_samples, int bpc, double* mse,
+                  double* psnr_db);
+
+/* Number of this library's kernels launched by the calls above since load. */
+MOTION_API uint64_t motion_kernel_launch_count(void);
+
+/* Human-readable name of a status code (static string). */
+MOTION_API const char* motion_strerror(int code);
+
+/* The last CUDA error seen by a MOTION_ERR_CUDA return (cudaError_t value). */
+MOTION_API int motion_last_cuda_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOTION_GB300_H */

@@ -1,0 +1,338 @@
+"""Python binding of libmotion_gb300 (the GB300 integer motion / PSNR-SSE
+library).  Argument marshalling only: every step of the computation runs in
+the library's CUDA kernels; there is no CPU fallback.  If the shared library
+has not been built this module raises on first use.
+
+The functions carry the names of the C ABI in ``include/motion.h``.  Device
+arguments may be PyTorch CUDA tensors (uint8, or int16/uint16 holding uint16
+samples) or raw device addresses (int); streams may be ``torch.cuda.Stream``
+objects, raw ``cudaStream_t`` values (int) or None (the current PyTorch stream
+when torch is loaded, else the legacy default stream).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import numpy as np
+
+from . import _build
+
+__all__ = [
+    "MotionError", "load_library", "motion_init", "motion_destroy", "motion_reset",
+    "motion_submit", "motion_submit_batch", "motion_psnr_yuv420_batch",
+    "motion_psnr_yuv420_batch_host", "motion_reserve_host_staging", "psnr_sse",
+    "psnr_sse_yuv420_batch", "motion_scores_from_sad", "psnr_from_sse",
+    "motion_kernel_launch_count", "motion_strerror", "MotionContext", "EXPORTED_SYMBOLS",
+]
+
+EXPORTED_SYMBOLS = (
+    "motion_init", "motion_destroy", "motion_reset", "motion_submit", "motion_submit_batch",
+    "motion_psnr_yuv420_batch", "motion_psnr_yuv420_batch_host", "motion_reserve_host_staging",
+    "psnr_sse", "psnr_sse_yuv420_batch", "motion_scores_from_sad", "psnr_from_sse",
+    "motion_kernel_launch_count", "motion_strerror", "motion_last_cuda_error",
+)
+
+_LIB: ctypes.CDLL | None = None
+
+
+class MotionError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = code
+        msg = _LIB.motion_strerror(code).decode() if _LIB is not None else str(code)
+        extra = ""
+        if _LIB is not None and code == 6:
+            extra = f" (cudaError {_LIB.motion_last_cuda_error()})"
+        super().__init__(f"{what}: {msg}{extra} [status {code}]")
+
+
+def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
+    P, I, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+    U64P = ctypes.POINTER(ctypes.c_uint64)
+    DP = ctypes.POINTER(ctypes.c_double)
+    sig = {
+        "motion_init": ([I, I, I, ctypes.POINTER(P)], I),
+        "motion_destroy": ([P], I),
+        "motion_reset": ([P], I),
+        "motion_submit": ([P, P, Z, P, U64P, DP], I),
+        "motion_submit_batch": ([P, P, I, Z, Z, P, P], I),
+        "motion_psnr_yuv420_batch": ([P, I, P, P, P, P, P, P, Z, Z, Z, Z, P, P, P], I),
+        "motion_psnr_yuv420_batch_host": ([P, I, P, P, P, P, P, P, Z, Z, Z, Z, P, P], I),
+        "motion_reserve_host_staging": ([P, I, Z, Z], I),
+        "psnr_sse": ([P, P, Z, Z, I, I, I, P, P], I),
+        "psnr_sse_yuv420_batch": ([I, I, I, I, P, P, P, P, P, P, Z, Z, Z, Z, P, P], I),
+        "motion_scores_from_sad": ([P, I, I, I, P, P, P], I),
+        "psnr_from_sse": ([ctypes.c_uint64, ctypes.c_uint64, I, DP, DP], I),
+        "motion_kernel_launch_count": ([], ctypes.c_uint64),
+        "motion_strerror": ([I], ctypes.c_char_p),
+        "motion_last_cuda_error": ([], I),
+    }
+    for name, (args, res) in sig.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = res
+    return lib
+
+
+def load_library(path: str | None = None) -> ctypes.CDLL:
+    """Load libmotion_gb300.so (built in-tree by ``__graft_entry__.build()``)."""
+    global _LIB
+    if _LIB is None:
+        p = path or _build.lib_path()
+        if not os.path.exists(p):
+            raise RuntimeError(
+                f"{p} is missing: build the CUDA library first (python -c 'import "
+                "__graft_entry__ as g; g.build()'); there is no CPU fallback")
+        _LIB = _declare(ctypes.CDLL(p))
+    return _LIB
+
+
+def _check(code: int, what: str) -> None:
+    if code != 0:
+        raise MotionError(code, what)
+
+
+# ----------------------------------------------------------------- marshalling
+def _addr(x) -> int:
+    if x is None:
+        return 0
+    if isinstance(x, int):
+        return x
+    if hasattr(x, "data_ptr"):
+        if hasattr(x, "is_cuda") and not x.is_cuda:
+            raise ValueError("expected a CUDA tensor")
+        return int(x.data_ptr())
+    raise TypeError(f"cannot take the device address of {type(x).__name__}")
+
+
+def _host_addr(x) -> int:
+    if isinstance(x, int):
+        return x
+    if isinstance(x, np.ndarray):
+        return int(x.ctypes.data)
+    if hasattr(x, "data_ptr"):
+        if getattr(x, "is_cuda", False):
+            raise ValueError("expected a host tensor")
+        return int(x.data_ptr())
+    raise TypeError(f"cannot take the host address of {type(x).__name__}")
+
+
+def _stream(s) -> int:
+    if s is None:
+        try:
+            import torch
+            if torch.cuda.is_available() and torch.cuda.is_initialized():
+                return int(torch.cuda.current_stream().cuda_stream)
+        except Exception:
+            pass
+        return 0
+    if isinstance(s, int):
+        return s
+    if hasattr(s, "cuda_stream"):
+        return int(s.cuda_stream)
+    raise TypeError("stream must be a torch.cuda.Stream, an int handle or None")
+
+
+def _itemsize(t) -> int:
+    return int(t.element_size()) if hasattr(t, "element_size") else int(t.itemsize)
+
+
+def _layout(t):
+    """(pitch_bytes, frame_stride_bytes) of a (h, w) or (n, h, w) array/tensor
+    whose last dimension is contiguous."""
+    st = t.stride() if callable(getattr(t, "stride", None)) else tuple(s // t.itemsize for s in t.strides)
+    if st[-1] != 1:
+        raise ValueError("samples within a row must be contiguous")
+    isz = _itemsize(t)
+    pitch = st[-2] * isz
+    stride = st[0] * isz if len(st) == 3 else 0
+    return pitch, stride
+
+
+# ----------------------------------------------------------------- C-ABI names
+def motion_init(w: int, h: int, bpc: int) -> int:
+    lib = load_library()
+    h_ = ctypes.c_void_p()
+    _check(lib.motion_init(w, h, bpc, ctypes.byref(h_)), "motion_init")
+    return int(h_.value)
+
+
+def motion_destroy(ctx: int) -> None:
+    _check(load_library().motion_destroy(ctx), "motion_destroy")
+
+
+def motion_reset(ctx: int) -> None:
+    _check(load_library().motion_reset(ctx), "motion_reset")
+
+
+def motion_submit(ctx: int, frame, pitch_bytes: int | None = None, stream=None):
+    """One frame; returns (SAD, score) after the stream has been synchronised."""
+    if pitch_bytes is None:
+        pitch_bytes, _ = _layout(frame)
+    sad = ctypes.c_uint64()
+    score = ctypes.c_double()
+    _check(load_library().motion_submit(ctx, _addr(frame), pitch_bytes, _stream(stream),
+                                        ctypes.byref(sad), ctypes.byref(score)), "motion_submit")
+    return int(sad.value), float(score.value)
+
+
+def motion_submit_batch(ctx: int, frames, sad_out, n: int | None = None,
+                        frame_stride: int | None = None, pitch_bytes: int | None = None,
+                        stream=None) -> None:
+    if n is None:
+        n = int(frames.shape[0])
+    if pitch_bytes is None or frame_stride is None:
+        p, s = _layout(frames)
+        pitch_bytes = p if pitch_bytes is None else pitch_bytes
+        frame_stride = s if frame_stride is None else frame_stride
+    _check(load_library().motion_submit_batch(ctx, _addr(frames), n, frame_stride, pitch_bytes,
+                                              _stream(stream), _addr(sad_out)),
+           "motion_submit_batch")
+
+
+@dataclass
+class Yuv420Layout:
+    pitch_y: int
+    pitch_uv: int
+    stride_y: int
+    stride_uv: int
+
+
+def _yuv_layout(ref_y, ref_u) -> Yuv420Layout:
+    py, sy = _layout(ref_y)
+    pu, su = _layout(ref_u)
+    return Yuv420Layout(py, pu, sy, su)
+
+
+def motion_psnr_yuv420_batch(ctx: int, ref_y, ref_u, ref_v, dist_y, dist_u, dist_v,
+                             sad_out, sse_out, n: int | None = None,
+                             layout: Yuv420Layout | None = None, stream=None) -> None:
+    if n is None:
+        n = int(ref_y.shape[0])
+    lay = layout or _yuv_layout(ref_y, ref_u)
+    _check(load_library().motion_psnr_yuv420_batch(
+        ctx, n, _addr(ref_y), _addr(ref_u), _addr(ref_v), _addr(dist_y), _addr(dist_u),
+        _addr(dist_v), lay.pitch_y, lay.pitch_uv, lay.stride_y, lay.stride_uv, _stream(stream),
+        _addr(sad_out), _addr(sse_out)), "motion_psnr_yuv420_batch")
+
+
+def motion_psnr_yuv420_batch_host(ctx: int, ref_y, ref_u, ref_v, dist_y, dist_u, dist_v,
+                                  sad_out: np.ndarray | None = None,
+                                  sse_out: np.ndarray | None = None,
+                                  n: int | None = None, layout: Yuv420Layout | None = None):
+    """Host pictures in, host results out (uint64[n], uint64[n][3])."""
+    if n is None:
+        n = int(ref_y.shape[0])
+    lay = layout or _yuv_layout(ref_y, ref_u)
+    if sad_out is None:
+        sad_out = np.zeros(n, np.uint64)
+    if sse_out is None:
+        sse_out = np.zeros((n, 3), np.uint64)
+    _check(load_library().motion_psnr_yuv420_batch_host(
+        ctx, n, _host_addr(ref_y), _host_addr(ref_u), _host_addr(ref_v), _host_addr(dist_y),
+        _host_addr(dist_u), _host_addr(dist_v), lay.pitch_y, lay.pitch_uv, lay.stride_y,
+        lay.stride_uv, _host_addr(sad_out), _host_addr(sse_out)), "motion_psnr_yuv420_batch_host")
+    return sad_out, sse_out
+
+
+def motion_reserve_host_staging(ctx: int, pairs_per_chunk: int = 0, stride_y: int = 0,
+                                stride_uv: int = 0) -> None:
+    _check(load_library().motion_reserve_host_staging(ctx, pairs_per_chunk, stride_y, stride_uv),
+           "motion_reserve_host_staging")
+
+
+def psnr_sse(ref, dist, bpc: int, sse_out, w: int | None = None, h: int | None = None,
+             ref_pitch: int | None = None, dist_pitch: int | None = None, stream=None) -> None:
+    if h is None or w is None:
+        h, w = int(ref.shape[-2]), int(ref.shape[-1])
+    if ref_pitch is None:
+        ref_pitch, _ = _layout(ref)
+    if dist_pitch is None:
+        dist_pitch, _ = _layout(dist)
+    _check(load_library().psnr_sse(_addr(ref), _addr(dist), ref_pitch, dist_pitch, w, h, bpc,
+                                   _stream(stream), _addr(sse_out)), "psnr_sse")
+
+
+def psnr_sse_yuv420_batch(w: int, h: int, bpc: int, ref_y, ref_u, ref_v, dist_y, dist_u, dist_v,
+                          sse_out, n: int | None = None, layout: Yuv420Layout | None = None,
+                          stream=None) -> None:
+    if n is None:
+        n = int(ref_y.shape[0])
+    lay = layout or _yuv_layout(ref_y, ref_u)
+    _check(load_library().psnr_sse_yuv420_batch(
+        w, h, bpc, n, _addr(ref_y), _addr(ref_u), _addr(ref_v), _addr(dist_y), _addr(dist_u),
+        _addr(dist_v), lay.pitch_y, lay.pitch_uv, lay.stride_y, lay.stride_uv, _stream(stream),
+        _addr(sse_out)), "psnr_sse_yuv420_batch")
+
+
+def motion_scores_from_sad(sad, w: int, h: int, next_score: float | None = None):
+    s = np.ascontiguousarray(np.asarray(sad, dtype=np.uint64))
+    n = s.size
+    score = np.zeros(n, np.float64)
+    motion2 = np.zeros(n, np.float64)
+    nxt = ctypes.c_double(next_score) if next_score is not None else None
+    _check(load_library().motion_scores_from_sad(
+        s.ctypes.data, n, w, h, ctypes.addressof(nxt) if nxt is not None else None,
+        score.ctypes.data, motion2.ctypes.data), "motion_scores_from_sad")
+    return score, motion2
+
+
+def psnr_from_sse(sse: int, n_samples: int, bpc: int):
+    mse = ctypes.c_double()
+    db = ctypes.c_double()
+    _check(load_library().psnr_from_sse(sse, n_samples, bpc, ctypes.byref(mse), ctypes.byref(db)),
+           "psnr_from_sse")
+    return float(mse.value), float(db.value)
+
+
+def motion_kernel_launch_count() -> int:
+    return int(load_library().motion_kernel_launch_count())
+
+
+def motion_strerror(code: int) -> str:
+    return load_library().motion_strerror(code).decode()
+
+
+class MotionContext:
+    """Owning wrapper over a motion_ctx handle."""
+
+    def __init__(self, w: int, h: int, bpc: int = 8):
+        self.w, self.h, self.bpc = w, h, bpc
+        self.handle = motion_init(w, h, bpc)
+
+    def close(self) -> None:
+        if self.handle:
+            motion_destroy(self.handle)
+            self.handle = 0
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def reset(self) -> None:
+        motion_reset(self.handle)
+
+    def submit(self, frame, stream=None):
+        return motion_submit(self.handle, frame, stream=stream)
+
+    def submit_batch(self, frames, sad_out, stream=None) -> None:
+        motion_submit_batch(self.handle, frames, sad_out, stream=stream)
+
+    def yuv420_batch(self, ref_y, ref_u, ref_v, dist_y, dist_u, dist_v, sad_out, sse_out,
+                     stream=None) -> None:
+        motion_psnr_yuv420_batch(self.handle, ref_y, ref_u, ref_v, dist_y, dist_u, dist_v,
+                                 sad_out, sse_out, stream=stream)
+
+    def yuv420_batch_host(self, ref_y, ref_u, ref_v, dist_y, dist_u, dist_v, sad_out=None,
+                          sse_out=None):
+        return motion_psnr_yuv420_batch_host(self.handle, ref_y, ref_u, ref_v, dist_y, dist_u,
+                                             dist_v, sad_out, sse_out)

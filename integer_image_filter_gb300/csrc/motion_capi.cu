@@ -1,0 +1,496 @@
+// motion_capi.cu -- the C ABI of libmotion_gb300: argument validation, the
+// motion context (resident previous blurred plane, result slot, host staging),
+// launch planning, and the host-buffer pipeline.  See include/motion.h for
+// the contract of every entry point.
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <new>
+
+#include "motion.h"
+#include "motion_internal.h"
+
+namespace {
+
+std::atomic<uint64_t> g_launches{0};
+std::atomic<int> g_last_cuda_error{0};
+
+int cuda_fail(cudaError_t e) {
+    g_last_cuda_error.store((int)e);
+    return e == cudaErrorMemoryAllocation ? MOTION_ERR_OUT_OF_MEMORY : MOTION_ERR_CUDA;
+}
+#define MG_CUDA(call)                               \
+    do {                                            \
+        cudaError_t e_ = (call);                    \
+        if (e_ != cudaSuccess) return cuda_fail(e_); \
+    } while (0)
+
+int sample_bytes(int bpc) { return bpc == 8 ? 1 : 2; }
+
+int check_dims(int w, int h, int bpc) {
+    if (bpc < 8 || bpc > 16) return MOTION_ERR_UNSUPPORTED_BITDEPTH;
+    if (w < 3 || h < 3) return MOTION_ERR_FRAME_TOO_SMALL;
+    if (w > MOTION_MAX_DIM || h > MOTION_MAX_DIM) return MOTION_ERR_TOO_LARGE;
+    return MOTION_OK;
+}
+
+// A plane layout: rows of w samples, pitch bytes apart; n planes stride apart.
+int check_layout(const void* p, size_t pitch, size_t stride, int n, int w, int bpc) {
+    if (!p) return MOTION_ERR_INVALID_ARGUMENT;
+    const size_t s = (size_t)sample_bytes(bpc);
+    if (pitch < (size_t)w * s) return MOTION_ERR_BAD_PITCH;
+    if (s == 2 && (((uintptr_t)p & 1) || (pitch & 1) || (n > 1 && (stride & 1))))
+        return MOTION_ERR_BAD_PITCH;
+    if (pitch > (size_t)1 << 40 || stride > (size_t)1 << 46) return MOTION_ERR_INVALID_ARGUMENT;
+    return MOTION_OK;
+}
+
+bool aligned16(const void* p, size_t pitch, size_t stride, int n) {
+    return (((uintptr_t)p | pitch) % 16 == 0) && (n <= 1 || stride % 16 == 0);
+}
+
+int current_device(int* dev) {
+    cudaError_t e = cudaGetDevice(dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return MOTION_OK;
+}
+
+}  // namespace
+
+struct motion_ctx {
+    int device = -1;
+    int w = 0, h = 0, bpc = 8, cw = 0, ch = 0;
+    int sm_count = 0;
+    int bprev_pitch = 0;            // elements per row of the resident plane
+    uint16_t* d_bprev = nullptr;    // previous frame's blurred plane (B_{i-1})
+    int has_prev = 0;
+    unsigned long long* d_slot = nullptr;   // single-submit result
+    unsigned long long* h_slot = nullptr;   // pinned readback slot
+    // host-buffer pipeline
+    int stage_pairs = 0;
+    size_t stage_stride_y = 0, stage_stride_uv = 0;
+    uint8_t* d_stage[2] = {nullptr, nullptr};
+    unsigned long long* d_res[2] = {nullptr, nullptr};
+    cudaStream_t s_copy = nullptr, s_comp = nullptr;
+    cudaEvent_t ev_in[2] = {nullptr, nullptr}, ev_done[2] = {nullptr, nullptr};
+};
+
+namespace {
+
+int ctx_device_ok(const motion_ctx* c) {
+    int dev = -1;
+    int rc = current_device(&dev);
+    if (rc) return rc;
+    return dev == c->device ? MOTION_OK : MOTION_ERR_WRONG_DEVICE;
+}
+
+void free_staging(motion_ctx* c) {
+    for (int k = 0; k < 2; ++k) {
+        if (c->d_stage[k]) cudaFree(c->d_stage[k]);
+        if (c->d_res[k]) cudaFree(c->d_res[k]);
+        if (c->ev_in[k]) cudaEventDestroy(c->ev_in[k]);
+        if (c->ev_done[k]) cudaEventDestroy(c->ev_done[k]);
+        c->d_stage[k] = nullptr;
+        c->d_res[k] = nullptr;
+        c->ev_in[k] = c->ev_done[k] = nullptr;
+    }
+    if (c->s_copy) cudaStreamDestroy(c->s_copy);
+    if (c->s_comp) cudaStreamDestroy(c->s_comp);
+    c->s_copy = c->s_comp = nullptr;
+    c->stage_pairs = 0;
+}
+
+mg::TileArgs motion_args(motion_ctx* c, int n) {
+    mg::TileArgs a;
+    std::memset(&a, 0, sizeof(a));
+    a.w = c->w;
+    a.h = c->h;
+    a.cw = c->cw;
+    a.ch = c->ch;
+    a.bpc = c->bpc;
+    a.n = n;
+    a.has_prev = c->has_prev;
+    a.store_last = 1;
+    a.bprev = c->d_bprev;
+    a.bprev_pitch = c->bprev_pitch;
+    return a;
+}
+
+int validate_yuv(const motion_ctx* c, int n, const void* ry, const void* ru, const void* rv,
+                 const void* dy, const void* du, const void* dv, size_t pitch_y,
+                 size_t pitch_uv, size_t stride_y, size_t stride_uv) {
+    int rc;
+    if ((rc = check_layout(ry, pitch_y, stride_y, n, c->w, c->bpc))) return rc;
+    if ((rc = check_layout(dy, pitch_y, stride_y, n, c->w, c->bpc))) return rc;
+    if ((rc = check_layout(ru, pitch_uv, stride_uv, n, c->cw, c->bpc))) return rc;
+    if ((rc = check_layout(rv, pitch_uv, stride_uv, n, c->cw, c->bpc))) return rc;
+    if ((rc = check_layout(du, pitch_uv, stride_uv, n, c->cw, c->bpc))) return rc;
+    if ((rc = check_layout(dv, pitch_uv, stride_uv, n, c->cw, c->bpc))) return rc;
+    return MOTION_OK;
+}
+
+int launch_fused(motion_ctx* c, int n, const void* ry, const void* ru, const void* rv,
+                 const void* dy, const void* du, const void* dv, size_t pitch_y,
+                 size_t pitch_uv, size_t stride_y, size_t stride_uv, cudaStream_t s,
+                 uint64_t* d_sad, uint64_t* d_sse) {
+    MG_CUDA(cudaMemsetAsync(d_sad, 0, sizeof(uint64_t) * (size_t)n, s));
+    MG_CUDA(cudaMemsetAsync(d_sse, 0, sizeof(uint64_t) * 3 * (size_t)n, s));
+    mg::TileArgs a = motion_args(c, n);
+    a.ref_y = (const uint8_t*)ry;
+    a.ref_u = (const uint8_t*)ru;
+    a.ref_v = (const uint8_t*)rv;
+    a.dist_y = (const uint8_t*)dy;
+    a.dist_u = (const uint8_t*)du;
+    a.dist_v = (const uint8_t*)dv;
+    a.pitch_y = (long long)pitch_y;
+    a.pitch_uv = (long long)pitch_uv;
+    a.stride_y = (long long)stride_y;
+    a.stride_uv = (long long)stride_uv;
+    a.aligned16 = aligned16(ry, pitch_y, stride_y, n) && aligned16(dy, pitch_y, stride_y, n) &&
+                  aligned16(ru, pitch_uv, stride_uv, n) && aligned16(rv, pitch_uv, stride_uv, n) &&
+                  aligned16(du, pitch_uv, stride_uv, n) && aligned16(dv, pitch_uv, stride_uv, n);
+    a.sad_out = (unsigned long long*)d_sad;
+    a.sse_out = (unsigned long long*)d_sse;
+    int launched = 0;
+    cudaError_t e = mg::launch_motion_tile(a, true, s, &launched);
+    g_launches += (uint64_t)launched;
+    if (e != cudaSuccess) return cuda_fail(e);
+    c->has_prev = 1;
+    return MOTION_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int motion_init(int w, int h, int bpc, motion_ctx** out) {
+    if (!out) return MOTION_ERR_INVALID_ARGUMENT;
+    *out = nullptr;
+    int rc = check_dims(w, h, bpc);
+    if (rc) return rc;
+    int ndev = 0;
+    if (cudaGetDeviceCount(&ndev) != cudaSuccess || ndev == 0) {
+        cudaGetLastError();
+        return MOTION_ERR_NO_DEVICE;
+    }
+    motion_ctx* c = new (std::nothrow) motion_ctx();
+    if (!c) return MOTION_ERR_OUT_OF_MEMORY;
+    c->w = w;
+    c->h = h;
+    c->bpc = bpc;
+    c->cw = (w + 1) / 2;
+    c->ch = (h + 1) / 2;
+    c->bprev_pitch = (w + 7) & ~7;
+    cudaError_t e = cudaGetDevice(&c->device);
+    if (e == cudaSuccess)
+        e = cudaDeviceGetAttribute(&c->sm_count, cudaDevAttrMultiProcessorCount, c->device);
+    if (e == cudaSuccess)
+        e = cudaMalloc(&c->d_bprev, sizeof(uint16_t) * (size_t)c->bprev_pitch * (size_t)h);
+    if (e == cudaSuccess) e = cudaMalloc(&c->d_slot, sizeof(unsigned long long));
+    if (e == cudaSuccess) e = cudaMallocHost(&c->h_slot, sizeof(unsigned long long));
+    if (e != cudaSuccess) {
+        motion_destroy(c);
+        return cuda_fail(e);
+    }
+    *out = c;
+    return MOTION_OK;
+}
+
+int motion_destroy(motion_ctx* c) {
+    if (!c) return MOTION_OK;
+    int prev = -1;
+    cudaGetDevice(&prev);
+    if (c->device >= 0) cudaSetDevice(c->device);
+    free_staging(c);
+    if (c->d_bprev) cudaFree(c->d_bprev);
+    if (c->d_slot) cudaFree(c->d_slot);
+    if (c->h_slot) cudaFreeHost(c->h_slot);
+    if (prev >= 0) cudaSetDevice(prev);
+    delete c;
+    return MOTION_OK;
+}
+
+int motion_reset(motion_ctx* c) {
+    if (!c) return MOTION_ERR_INVALID_ARGUMENT;
+    c->has_prev = 0;
+    return MOTION_OK;
+}
+
+int motion_submit_batch(motion_ctx* c, const void* d_frames, int n, size_t frame_stride,
+                        size_t pitch, void* stream, uint64_t* d_sad_out) {
+    if (!c || n < 0) return MOTION_ERR_INVALID_ARGUMENT;
+    if (n == 0) return MOTION_OK;
+    if (!d_sad_out) return MOTION_ERR_INVALID_ARGUMENT;
+    int rc = check_layout(d_frames, pitch, frame_stride, n, c->w, c->bpc);
+    if (rc) return rc;
+    if ((rc = ctx_device_ok(c))) return rc;
+    cudaStream_t s = (cudaStream_t)stream;
+    MG_CUDA(cudaMemsetAsync(d_sad_out, 0, sizeof(uint64_t) * (size_t)n, s));
+    mg::TileArgs a = motion_args(c, n);
+    a.ref_y = (const uint8_t*)d_frames;
+    a.pitch_y = (long long)pitch;
+    a.stride_y = (long long)frame_stride;
+    a.aligned16 = aligned16(d_frames, pitch, frame_stride, n);
+    a.sad_out = (unsigned long long*)d_sad_out;
+    int launched = 0;
+    cudaError_t e = mg::launch_motion_tile(a, false, s, &launched);
+    g_launches += (uint64_t)launched;
+    if (e != cudaSuccess) return cuda_fail(e);
+    c->has_prev = 1;
+    return MOTION_OK;
+}
+
+int motion_submit(motion_ctx* c, const void* d_frame, size_t pitch, void* stream,
+                  uint64_t* sad_out, double* score_out) {
+    if (!c) return MOTION_ERR_INVALID_ARGUMENT;
+    cudaStream_t s = (cudaStream_t)stream;
+    int rc = motion_submit_batch(c, d_frame, 1, 0, pitch, stream, (uint64_t*)c->d_slot);
+    if (rc) return rc;
+    MG_CUDA(cudaMemcpyAsync(c->h_slot, c->d_slot, sizeof(unsigned long long),
+                            cudaMemcpyDeviceToHost, s));
+    MG_CUDA(cudaStreamSynchronize(s));
+    const uint64_t sad = (uint64_t)*c->h_slot;
+    if (sad_out) *sad_out = sad;
+    if (score_out) *score_out = ((double)sad / 256.0) / ((double)c->w * (double)c->h);
+    return MOTION_OK;
+}
+
+int motion_psnr_yuv420_batch(motion_ctx* c, int n, const void* ry, const void* ru,
+                             const void* rv, const void* dy, const void* du, const void* dv,
+                             size_t pitch_y, size_t pitch_uv, size_t stride_y,
+                             size_t stride_uv, void* stream, uint64_t* d_sad_out,
+                             uint64_t* d_sse_out) {
+    if (!c || n < 0) return MOTION_ERR_INVALID_ARGUMENT;
+    if (n == 0) return MOTION_OK;
+    if (!d_sad_out || !d_sse_out) return MOTION_ERR_INVALID_ARGUMENT;
+    int rc = validate_yuv(c, n, ry, ru, rv, dy, du, dv, pitch_y, pitch_uv, stride_y, stride_uv);
+    if (rc) return rc;
+    if ((rc = ctx_device_ok(c))) return rc;
+    return launch_fused(c, n, ry, ru, rv, dy, du, dv, pitch_y, pitch_uv, stride_y, stride_uv,
+                        (cudaStream_t)stream, d_sad_out, d_sse_out);
+}
+
+int motion_reserve_host_staging(motion_ctx* c, int pairs_per_chunk, size_t stride_y,
+                                size_t stride_uv) {
+    if (!c || pairs_per_chunk < 0) return MOTION_ERR_INVALID_ARGUMENT;
+    int rc = ctx_device_ok(c);
+    if (rc) return rc;
+    const size_t s = (size_t)sample_bytes(c->bpc);
+    if (stride_y == 0) stride_y = (size_t)c->w * s * (size_t)c->h;
+    if (stride_uv == 0) stride_uv = (size_t)c->cw * s * (size_t)c->ch;
+    if (pairs_per_chunk == 0) {
+        // about 64 MB of pictures per chunk, at least one pair
+        const size_t pair_bytes = 2 * (stride_y + 2 * stride_uv);
+        pairs_per_chunk = (int)((size_t)64 << 20) / (int)(pair_bytes ? pair_bytes : 1);
+        if (pairs_per_chunk < 1) pairs_per_chunk = 1;
+        if (pairs_per_chunk > 64) pairs_per_chunk = 64;
+    }
+    if (c->stage_pairs >= pairs_per_chunk && c->stage_stride_y >= stride_y &&
+        c->stage_stride_uv >= stride_uv)
+        return MOTION_OK;
+    free_staging(c);
+    const size_t bytes = 2 * (size_t)pairs_per_chunk * (stride_y + 2 * stride_uv);
+    for (int k = 0; k < 2; ++k) {
+        MG_CUDA(cudaMalloc(&c->d_stage[k], bytes));
+        MG_CUDA(cudaMalloc(&c->d_res[k], sizeof(unsigned long long) * 4 * (size_t)pairs_per_chunk));
+        MG_CUDA(cudaEventCreateWithFlags(&c->ev_in[k], cudaEventDisableTiming));
+        MG_CUDA(cudaEventCreateWithFlags(&c->ev_done[k], cudaEventDisableTiming));
+    }
+    MG_CUDA(cudaStreamCreateWithFlags(&c->s_copy, cudaStreamNonBlocking));
+    MG_CUDA(cudaStreamCreateWithFlags(&c->s_comp, cudaStreamNonBlocking));
+    c->stage_pairs = pairs_per_chunk;
+    c->stage_stride_y = stride_y;
+    c->stage_stride_uv = stride_uv;
+    return MOTION_OK;
+}
+
+int motion_psnr_yuv420_batch_host(motion_ctx* c, int n, const void* ry, const void* ru,
+                                  const void* rv, const void* dy, const void* du,
+                                  const void* dv, size_t pitch_y, size_t pitch_uv,
+                                  size_t stride_y, size_t stride_uv, uint64_t* h_sad_out,
+                                  uint64_t* h_sse_out) {
+    if (!c || n < 0) return MOTION_ERR_INVALID_ARGUMENT;
+    if (n == 0) return MOTION_OK;
+    if (!h_sad_out || !h_sse_out) return MOTION_ERR_INVALID_ARGUMENT;
+    int rc = validate_yuv(c, n, ry, ru, rv, dy, du, dv, pitch_y, pitch_uv, stride_y, stride_uv);
+    if (rc) return rc;
+    if ((rc = ctx_device_ok(c))) return rc;
+    const size_t s = (size_t)sample_bytes(c->bpc);
+    if (stride_y < pitch_y * (size_t)(c->h - 1) + (size_t)c->w * s ||
+        stride_uv < pitch_uv * (size_t)(c->ch - 1) + (size_t)c->cw * s)
+        return MOTION_ERR_BAD_PITCH;  // host pairs must not overlap
+    if ((rc = motion_reserve_host_staging(c, c->stage_pairs, stride_y, stride_uv))) return rc;
+    const int P = c->stage_pairs;
+    const size_t ybytes = (size_t)P * stride_y, cbytes = (size_t)P * stride_uv;
+    const void* src[6] = {ry, ru, rv, dy, du, dv};
+    const int nchunks = (n + P - 1) / P;
+    for (int ci = 0; ci < nchunks; ++ci) {
+        const int k = ci & 1;
+        const int first = ci * P;
+        const int m = (n - first) < P ? (n - first) : P;
+        uint8_t* dst[6];
+        dst[0] = c->d_stage[k];
+        dst[1] = dst[0] + ybytes;
+        dst[2] = dst[1] + cbytes;
+        dst[3] = dst[2] + cbytes;
+        dst[4] = dst[3] + ybytes;
+        dst[5] = dst[4] + cbytes;
+        // the staging set k is free once the kernel of chunk ci-2 has finished
+        MG_CUDA(cudaStreamWaitEvent(c->s_copy, c->ev_done[k], 0));
+        for (int p = 0; p < 6; ++p) {
+            const bool luma = (p == 0 || p == 3);
+            const size_t stride = luma ? stride_y : stride_uv;
+            const size_t last = luma ? pitch_y * (size_t)(c->h - 1) + (size_t)c->w * s
+                                     : pitch_uv * (size_t)(c->ch - 1) + (size_t)c->cw * s;
+            const size_t bytes = (size_t)(m - 1) * stride + last;
+            MG_CUDA(cudaMemcpyAsync(dst[p], (const uint8_t*)src[p] + (size_t)first * stride, bytes,
+                                    cudaMemcpyHostToDevice, c->s_copy));
+        }
+        MG_CUDA(cudaEventRecord(c->ev_in[k], c->s_copy));
+        MG_CUDA(cudaStreamWaitEvent(c->s_comp, c->ev_in[k], 0));
+        uint64_t* d_sad = (uint64_t*)c->d_res[k];
+        uint64_t* d_sse = d_sad + P;
+        rc = launch_fused(c, m, dst[0], dst[1], dst[2], dst[3], dst[4], dst[5], pitch_y, pitch_uv,
+                          stride_y, stride_uv, c->s_comp, d_sad, d_sse);
+        if (rc) return rc;
+        MG_CUDA(cudaMemcpyAsync(h_sad_out + first, d_sad, sizeof(uint64_t) * (size_t)m,
+                                cudaMemcpyDeviceToHost, c->s_comp));
+        MG_CUDA(cudaMemcpyAsync(h_sse_out + 3 * (size_t)first, d_sse, sizeof(uint64_t) * 3 * (size_t)m,
+                                cudaMemcpyDeviceToHost, c->s_comp));
+        MG_CUDA(cudaEventRecord(c->ev_done[k], c->s_comp));
+    }
+    MG_CUDA(cudaStreamSynchronize(c->s_comp));
+    return MOTION_OK;
+}
+
+int psnr_sse(const void* d_ref, const void* d_dist, size_t ref_pitch, size_t dist_pitch, int w,
+             int h, int bpc, void* stream, uint64_t* d_sse_out) {
+    if (bpc < 8 || bpc > 16) return MOTION_ERR_UNSUPPORTED_BITDEPTH;
+    if (w < 1 || h < 1) return MOTION_ERR_INVALID_ARGUMENT;
+    if (w > MOTION_MAX_DIM || h > MOTION_MAX_DIM) return MOTION_ERR_TOO_LARGE;
+    if (!d_sse_out) return MOTION_ERR_INVALID_ARGUMENT;
+    int rc;
+    if ((rc = check_layout(d_ref, ref_pitch, 0, 1, w, bpc))) return rc;
+    if ((rc = check_layout(d_dist, dist_pitch, 0, 1, w, bpc))) return rc;
+    cudaStream_t s = (cudaStream_t)stream;
+    MG_CUDA(cudaMemsetAsync(d_sse_out, 0, sizeof(uint64_t), s));
+    int dev = 0, sms = 0;
+    MG_CUDA(cudaGetDevice(&dev));
+    MG_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+    mg::SseArgs a;
+    std::memset(&a, 0, sizeof(a));
+    a.ref_y = (const uint8_t*)d_ref;
+    a.dist_y = (const uint8_t*)d_dist;
+    a.ref_pitch_y = (long long)ref_pitch;
+    a.dist_pitch_y = (long long)dist_pitch;
+    a.w = w;
+    a.h = h;
+    a.bpc = bpc;
+    a.n = 1;
+    a.planes = 1;
+    a.sse_out = (unsigned long long*)d_sse_out;
+    int launched = 0;
+    cudaError_t e = mg::launch_sse(a, s, sms, &launched);
+    g_launches += (uint64_t)launched;
+    if (e != cudaSuccess) return cuda_fail(e);
+    return MOTION_OK;
+}
+
+int psnr_sse_yuv420_batch(int w, int h, int bpc, int n, const void* ry, const void* ru,
+                          const void* rv, const void* dy, const void* du, const void* dv,
+                          size_t pitch_y, size_t pitch_uv, size_t stride_y, size_t stride_uv,
+                          void* stream, uint64_t* d_sse_out) {
+    if (bpc < 8 || bpc > 16) return MOTION_ERR_UNSUPPORTED_BITDEPTH;
+    if (w < 1 || h < 1 || n < 0) return MOTION_ERR_INVALID_ARGUMENT;
+    if (w > MOTION_MAX_DIM || h > MOTION_MAX_DIM) return MOTION_ERR_TOO_LARGE;
+    if (n == 0) return MOTION_OK;
+    if (!d_sse_out) return MOTION_ERR_INVALID_ARGUMENT;
+    const int cw = (w + 1) / 2, ch = (h + 1) / 2;
+    int rc;
+    if ((rc = check_layout(ry, pitch_y, stride_y, n, w, bpc))) return rc;
+    if ((rc = check_layout(dy, pitch_y, stride_y, n, w, bpc))) return rc;
+    if ((rc = check_layout(ru, pitch_uv, stride_uv, n, cw, bpc))) return rc;
+    if ((rc = check_layout(rv, pitch_uv, stride_uv, n, cw, bpc))) return rc;
+    if ((rc = check_layout(du, pitch_uv, stride_uv, n, cw, bpc))) return rc;
+    if ((rc = check_layout(dv, pitch_uv, stride_uv, n, cw, bpc))) return rc;
+    cudaStream_t s = (cudaStream_t)stream;
+    MG_CUDA(cudaMemsetAsync(d_sse_out, 0, sizeof(uint64_t) * 3 * (size_t)n, s));
+    int dev = 0, sms = 0;
+    MG_CUDA(cudaGetDevice(&dev));
+    MG_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+    mg::SseArgs a;
+    std::memset(&a, 0, sizeof(a));
+    a.ref_y = (const uint8_t*)ry;
+    a.dist_y = (const uint8_t*)dy;
+    a.ref_u = (const uint8_t*)ru;
+    a.dist_u = (const uint8_t*)du;
+    a.ref_v = (const uint8_t*)rv;
+    a.dist_v = (const uint8_t*)dv;
+    a.ref_pitch_y = (long long)pitch_y;
+    a.dist_pitch_y = (long long)pitch_y;
+    a.pitch_uv = (long long)pitch_uv;
+    a.stride_y = (long long)stride_y;
+    a.stride_uv = (long long)stride_uv;
+    a.w = w;
+    a.h = h;
+    a.cw = cw;
+    a.ch = ch;
+    a.bpc = bpc;
+    a.n = n;
+    a.planes = 3;
+    a.sse_out = (unsigned long long*)d_sse_out;
+    int launched = 0;
+    cudaError_t e = mg::launch_sse(a, s, sms, &launched);
+    g_launches += (uint64_t)launched;
+    if (e != cudaSuccess) return cuda_fail(e);
+    return MOTION_OK;
+}
+
+int motion_scores_from_sad(const uint64_t* sad, int n, int w, int h, const double* next_score,
+                           double* score, double* motion2) {
+    if (n < 0 || w <= 0 || h <= 0) return MOTION_ERR_INVALID_ARGUMENT;
+    if (n > 0 && (!sad || !score || !motion2)) return MOTION_ERR_INVALID_ARGUMENT;
+    const double area = (double)w * (double)h;
+    for (int i = 0; i < n; ++i) score[i] = ((double)sad[i] / 256.0) / area;
+    for (int i = 0; i < n; ++i) {
+        if (i + 1 < n)
+            motion2[i] = std::fmin(score[i], score[i + 1]);
+        else
+            motion2[i] = next_score ? std::fmin(score[i], *next_score) : score[i];
+    }
+    return MOTION_OK;
+}
+
+int psnr_from_sse(uint64_t sse, uint64_t n_samples, int bpc, double* mse, double* psnr_db) {
+    if (n_samples == 0 || bpc < 8 || bpc > 16) return MOTION_ERR_INVALID_ARGUMENT;
+    const double m = (double)sse / (double)n_samples;
+    if (mse) *mse = m;
+    if (psnr_db) {
+        const double peak = (double)((1u << bpc) - 1u);
+        *psnr_db = sse == 0 ? INFINITY : 10.0 * std::log10(peak * peak / m);
+    }
+    return MOTION_OK;
+}
+
+uint64_t motion_kernel_launch_count(void) { return g_launches.load(); }
+
+int motion_last_cuda_error(void) { return g_last_cuda_error.load(); }
+
+const char* motion_strerror(int code) {
+    switch (code) {
+        case MOTION_OK: return "ok";
+        case MOTION_ERR_INVALID_ARGUMENT: return "invalid argument";
+        case MOTION_ERR_FRAME_TOO_SMALL: return "frame smaller than 3x3";
+        case MOTION_ERR_UNSUPPORTED_BITDEPTH: return "bits per sample outside [8, 16]";
+        case MOTION_ERR_BAD_PITCH: return "pitch, stride or alignment does not fit the samples";
+        case MOTION_ERR_TOO_LARGE: return "frame larger than MOTION_MAX_DIM";
+        case MOTION_ERR_CUDA: return "CUDA runtime error";
+        case MOTION_ERR_OUT_OF_MEMORY: return "out of memory";
+        case MOTION_ERR_NO_DEVICE: return "no CUDA device";
+        case MOTION_ERR_WRONG_DEVICE: return "current device is not the context's device";
+        default: return "unknown status";
+    }
+}
+
+}  // extern "C"

@@ -1,0 +1,49 @@
+// motion_internal.h -- host-side launch interface between the C-ABI layer and
+// the kernels of libmotion_gb300.  Internal; not installed.
+#pragma once
+
+#include <cstdint>
+#include <cstddef>
+#include <cuda_runtime.h>
+
+namespace mg {
+
+// Arguments of one batched motion (+ optional fused 4:2:0 SSE) launch.  All
+// plane pointers are byte pointers; pitches and strides are in bytes.  Passed
+// by value and only ever read field by field (no runtime-indexed arrays).
+struct TileArgs {
+    const uint8_t* ref_y;
+    const uint8_t* dist_y;
+    const uint8_t* ref_u;
+    const uint8_t* dist_u;
+    const uint8_t* ref_v;
+    const uint8_t* dist_v;
+    long long pitch_y, pitch_uv, stride_y, stride_uv;
+    int w, h, cw, ch, bpc, n;
+    int has_prev;       // B of the previous frame is in bprev
+    int store_last;     // write B of the last frame to bprev
+    int aligned16;      // every plane base, pitch and stride is 16-byte aligned
+    uint16_t* bprev;    // resident blurred plane, bprev_pitch elements per row
+    int bprev_pitch;
+    unsigned long long* sad_out;  // [n], zeroed by the caller
+    unsigned long long* sse_out;  // [n][3], zeroed by the caller (fused only)
+};
+
+// Arguments of one batched SSE launch over n pairs x (1 or 3) planes.
+struct SseArgs {
+    const uint8_t* ref_y;
+    const uint8_t* dist_y;
+    const uint8_t* ref_u;
+    const uint8_t* dist_u;
+    const uint8_t* ref_v;
+    const uint8_t* dist_v;
+    long long ref_pitch_y, dist_pitch_y, pitch_uv, stride_y, stride_uv;
+    int w, h, cw, ch, bpc, n, planes;  // planes: 1 (luma only) or 3
+    unsigned long long* sse_out;       // [n][planes], zeroed by the caller
+};
+
+cudaError_t launch_motion_tile(const TileArgs& a, bool fused, cudaStream_t s,
+                               int* launches);
+cudaError_t launch_sse(const SseArgs& a, cudaStream_t s, int sm_count, int* launches);
+
+}  // namespace mg

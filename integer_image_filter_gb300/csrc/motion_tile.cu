@@ -1,0 +1,345 @@
+// motion_tile.cu -- batched integer motion kernel (blur + SAD against the
+// previous frame), optionally fused with the per-plane SSE of 4:2:0 pairs.
+//
+// Design (GB300 / sm_103a):
+//  * One CTA owns a TW x TH output tile and walks the whole batch of frames in
+//    time order, so the previous frame's blurred tile B_prev never leaves the
+//    SM (registers); each frame is read from HBM once ("Making it fast",
+//    Round 1: one kernel over all frames; Round 2: no scratch rebuilt per call).
+//  * The next frame's tile (luma with a 2-row / 16-byte halo, and in the fused
+//    form the distorted luma and the four chroma tiles) is staged into shared
+//    memory with 16-byte cp.async copies while the current frame is computed
+//    (double buffer).  Tiles touching the frame border load sample by sample
+//    with the mirror rule applied at load time.
+//  * The blur is separable: the vertical 5-tap pass runs once per sample
+//    (rounded >> bpc) into a shared V tile, the horizontal 5-tap pass reads it
+//    (rounded >> 16) -- "ADR-1392: CUDA motion, PSNR and moment kernels add one
+//    atomic per block, the motion SAD filters separably, ...", Decision 4.
+//  * |B - B_prev| and (ref - dist)^2 are reduced per block with warp shuffles
+//    and shared memory, then ONE 64-bit atomic per block per frame and per
+//    accumulator (same page, Decision 1).  Integer sums are order-independent,
+//    so the result is exact (same page, Context).
+#include "motion_common.cuh"
+#include "motion_internal.h"
+
+namespace mg {
+
+constexpr int TW = 128;            // output tile width, samples
+constexpr int TH = 32;             // output tile height, rows
+constexpr int NT = 256;            // threads per CTA
+constexpr int NW = NT / 32;
+constexpr int SVW = TW + 8;        // V tile row pitch (uint32); col j <-> x = x0 - 4 + j
+
+template <typename Pix>
+struct Geo {
+    static constexpr int S = sizeof(Pix);
+    static constexpr int HX = 16 / S;                 // halo columns staged on each side
+    static constexpr int RAW_W = TW + 2 * HX;         // staged luma row, samples
+    static constexpr int RAW_ROWS = TH + 4;
+    static constexpr int RAW_BYTES = RAW_ROWS * RAW_W * S;
+    static constexpr int DIST_BYTES = TH * TW * S;
+    static constexpr int CW = TW / 2, CH = TH / 2;    // 4:2:0 chroma tile
+    static constexpr int C_BYTES = CH * CW * S;
+    static constexpr int STAGE_MOTION = RAW_BYTES;
+    static constexpr int STAGE_FUSED = RAW_BYTES + DIST_BYTES + 4 * C_BYTES;
+    static constexpr int SV_BYTES = TH * SVW * 4;
+    static_assert(RAW_BYTES % 16 == 0 && DIST_BYTES % 16 == 0 && C_BYTES % 16 == 0, "16B");
+};
+
+template <typename Pix> struct SseAcc;
+template <> struct SseAcc<uint8_t> { using T = uint32_t; };            // 4096 * 255^2 < 2^32
+template <> struct SseAcc<uint16_t> { using T = unsigned long long; };
+
+__device__ __forceinline__ void unpack4(const uint8_t* p, uint32_t (&o)[4]) {
+    const uint32_t w = *reinterpret_cast<const uint32_t*>(p);
+    o[0] = w & 0xffu; o[1] = (w >> 8) & 0xffu; o[2] = (w >> 16) & 0xffu; o[3] = w >> 24;
+}
+__device__ __forceinline__ void unpack4(const uint16_t* p, uint32_t (&o)[4]) {
+    const uint2 w = *reinterpret_cast<const uint2*>(p);
+    o[0] = w.x & 0xffffu; o[1] = w.x >> 16; o[2] = w.y & 0xffffu; o[3] = w.y >> 16;
+}
+
+__device__ __forceinline__ uint32_t vtap(uint32_t a, uint32_t b, uint32_t c, uint32_t d,
+                                         uint32_t e, uint32_t rnd, int sh) {
+    return (kT0 * (a + e) + kT1 * (b + d) + kT2 * c + rnd) >> sh;
+}
+
+template <typename Pix, bool FUSED>
+__device__ __forceinline__ void load_stage(const TileArgs& a, int f, unsigned char* st,
+                                           int x0, int y0, bool fast) {
+    using G = Geo<Pix>;
+    constexpr int S = G::S;
+    const int tid = threadIdx.x;
+    const uint8_t* fy = a.ref_y + (long long)f * a.stride_y;
+    if (fast) {
+        constexpr int CHR = G::RAW_W * S / 16;
+        const uint8_t* g0 = fy + (long long)(y0 - 2) * a.pitch_y + (long long)(x0 - G::HX) * S;
+        for (int c = tid; c < G::RAW_ROWS * CHR; c += NT) {
+            const int r = c / CHR, k = c - r * CHR;
+            cp_async16(st + (r * G::RAW_W) * S + k * 16, g0 + (long long)r * a.pitch_y + k * 16);
+        }
+        if constexpr (FUSED) {
+            unsigned char* sd = st + G::RAW_BYTES;
+            constexpr int CHD = TW * S / 16;
+            const uint8_t* d0 = a.dist_y + (long long)f * a.stride_y + (long long)y0 * a.pitch_y +
+                                (long long)x0 * S;
+            for (int c = tid; c < TH * CHD; c += NT) {
+                const int r = c / CHD, k = c - r * CHD;
+                cp_async16(sd + r * TW * S + k * 16, d0 + (long long)r * a.pitch_y + k * 16);
+            }
+            constexpr int CHC = G::CW * S / 16;
+            const long long coff = (long long)f * a.stride_uv + (long long)(y0 / 2) * a.pitch_uv +
+                                   (long long)(x0 / 2) * S;
+            unsigned char* sc = sd + G::DIST_BYTES;
+            for (int c = tid; c < 4 * G::CH * CHC; c += NT) {
+                const int p = c / (G::CH * CHC);
+                const int rem = c - p * (G::CH * CHC);
+                const int r = rem / CHC, k = rem - r * CHC;
+                // constant-index plane selection (ADR-1392 Decision 3)
+                const uint8_t* base = p == 0 ? a.ref_u : p == 1 ? a.dist_u : p == 2 ? a.ref_v : a.dist_v;
+                cp_async16(sc + p * G::C_BYTES + r * G::CW * S + k * 16,
+                           base + coff + (long long)r * a.pitch_uv + k * 16);
+            }
+        }
+        return;
+    }
+    // border tile: sample loads with the mirror rule applied here
+    Pix* raw = reinterpret_cast<Pix*>(st);
+    for (int e = tid; e < G::RAW_ROWS * G::RAW_W; e += NT) {
+        const int r = e / G::RAW_W, c = e - r * G::RAW_W;
+        const int yy = mirror_clamp(y0 - 2 + r, a.h), xx = mirror_clamp(x0 - G::HX + c, a.w);
+        raw[e] = *reinterpret_cast<const Pix*>(fy + (long long)yy * a.pitch_y + (long long)xx * S);
+    }
+    if constexpr (FUSED) {
+        Pix* sd = reinterpret_cast<Pix*>(st + G::RAW_BYTES);
+        const uint8_t* fd = a.dist_y + (long long)f * a.stride_y;
+        for (int e = tid; e < TH * TW; e += NT) {
+            const int r = e / TW, c = e - r * TW;
+            const int y = y0 + r, x = x0 + c;
+            // outside the picture the distorted sample repeats the staged
+            // reference sample, so the squared error there is zero
+            const bool in = (y < a.h) && (x < a.w);
+            const uint8_t* src = in ? fd + (long long)y * a.pitch_y + (long long)x * S
+                                    : fy + (long long)mirror_clamp(y, a.h) * a.pitch_y +
+                                          (long long)mirror_clamp(x, a.w) * S;
+            sd[e] = *reinterpret_cast<const Pix*>(src);
+        }
+        Pix* sc = reinterpret_cast<Pix*>(st + G::RAW_BYTES + G::DIST_BYTES);
+        const long long foff = (long long)f * a.stride_uv;
+        for (int e = tid; e < 4 * G::CH * G::CW; e += NT) {
+            const int p = e / (G::CH * G::CW);
+            const int rem = e - p * (G::CH * G::CW);
+            const int r = rem / G::CW, c = rem - r * G::CW;
+            const int y = y0 / 2 + r, x = x0 / 2 + c;
+            const uint8_t* base = p == 0 ? a.ref_u : p == 1 ? a.dist_u : p == 2 ? a.ref_v : a.dist_v;
+            Pix v = 0;
+            if (y < a.ch && x < a.cw)
+                v = *reinterpret_cast<const Pix*>(base + foff + (long long)y * a.pitch_uv + (long long)x * S);
+            sc[e] = v;
+        }
+    }
+}
+
+template <typename Pix, bool FUSED>
+__global__ void __launch_bounds__(NT) motion_tile_kernel(const TileArgs a) {
+    using G = Geo<Pix>;
+    using Acc = typename SseAcc<Pix>::T;
+    constexpr int STAGE = FUSED ? G::STAGE_FUSED : G::STAGE_MOTION;
+    extern __shared__ __align__(16) unsigned char smem[];
+    uint32_t* sV = reinterpret_cast<uint32_t*>(smem + 2 * STAGE);
+    __shared__ unsigned long long red[NW][4];
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int x0 = blockIdx.x * TW, y0 = blockIdx.y * TH;
+    const bool full = (x0 + TW <= a.w) && (y0 + TH <= a.h);
+    const bool fast = a.aligned16 && (x0 - G::HX >= 0) && (x0 + TW + G::HX <= a.w) &&
+                      (y0 - 2 >= 0) && (y0 + TH + 2 <= a.h);
+    const uint32_t rnd = 1u << (a.bpc - 1);
+    const int sh = a.bpc;
+
+    // horizontal-pass ownership: quad q of 4 columns, rows rbase + 8k
+    const int q = lane, rbase = warp;
+    uint32_t bp[4][4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int y = y0 + rbase + 8 * k;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int x = x0 + 4 * q + i;
+            bp[k][i] = (a.has_prev && y < a.h && x < a.w) ? a.bprev[(long long)y * a.bprev_pitch + x] : 0u;
+        }
+    }
+
+    load_stage<Pix, FUSED>(a, 0, smem, x0, y0, fast);
+    cp_async_commit();
+    for (int f = 0; f < a.n; ++f) {
+        unsigned char* st = smem + (f & 1) * STAGE;
+        if (f + 1 < a.n) load_stage<Pix, FUSED>(a, f + 1, smem + ((f + 1) & 1) * STAGE, x0, y0, fast);
+        cp_async_commit();
+        cp_async_wait<1>();
+        __syncthreads();
+
+        const Pix* raw = reinterpret_cast<const Pix*>(st);
+        // ---- vertical pass: 32 quads x 8 runs of 4 rows; raw row r <-> y0 - 2 + r
+        {
+            const Pix* src = raw + (warp * 4) * G::RAW_W + G::HX + 4 * lane;
+            uint32_t p[8][4];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) unpack4(src + i * G::RAW_W, p[i]);
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                uint4 o;
+                o.x = vtap(p[r][0], p[r + 1][0], p[r + 2][0], p[r + 3][0], p[r + 4][0], rnd, sh);
+                o.y = vtap(p[r][1], p[r + 1][1], p[r + 2][1], p[r + 3][1], p[r + 4][1], rnd, sh);
+                o.z = vtap(p[r][2], p[r + 1][2], p[r + 2][2], p[r + 3][2], p[r + 4][2], rnd, sh);
+                o.w = vtap(p[r][3], p[r + 1][3], p[r + 2][3], p[r + 3][3], p[r + 4][3], rnd, sh);
+                *reinterpret_cast<uint4*>(sV + (warp * 4 + r) * SVW + 4 + 4 * lane) = o;
+            }
+            // the two halo columns on each side of the tile
+            if (tid < 4 * TH) {
+                const int r = tid >> 2, which = tid & 3;
+                const int off = which == 0 ? -2 : which == 1 ? -1 : which == 2 ? TW : TW + 1;
+                const Pix* s = raw + r * G::RAW_W + G::HX + off;
+                sV[r * SVW + 4 + off] = vtap(s[0], s[G::RAW_W], s[2 * G::RAW_W], s[3 * G::RAW_W],
+                                             s[4 * G::RAW_W], rnd, sh);
+            }
+        }
+        __syncthreads();
+
+        // ---- horizontal pass, SAD against B_prev, SSE of the luma
+        const bool do_sad = (f > 0) || a.has_prev;
+        uint32_t sad = 0;
+        Acc sse_y = 0, sse_u = 0, sse_v = 0;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int r = rbase + 8 * k;
+            const uint32_t* v = sV + r * SVW + 4 * q;
+            const uint4 A = *reinterpret_cast<const uint4*>(v);
+            const uint4 Bq = *reinterpret_cast<const uint4*>(v + 4);
+            const uint4 C = *reinterpret_cast<const uint4*>(v + 8);
+            const uint32_t wv[12] = {A.x, A.y, A.z, A.w, Bq.x, Bq.y, Bq.z, Bq.w, C.x, C.y, C.z, C.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const uint32_t b = (kT0 * (wv[2 + i] + wv[6 + i]) + kT1 * (wv[3 + i] + wv[5 + i]) +
+                                    kT2 * wv[4 + i] + 32768u) >> 16;
+                uint32_t d = b > bp[k][i] ? b - bp[k][i] : bp[k][i] - b;
+                if (!full) {
+                    const bool ok = (y0 + r < a.h) && (x0 + 4 * q + i < a.w);
+                    d = ok ? d : 0u;
+                }
+                sad += d;
+                bp[k][i] = b;
+            }
+            if constexpr (FUSED) {
+                uint32_t rf[4], ds[4];
+                unpack4(raw + (r + 2) * G::RAW_W + G::HX + 4 * q, rf);
+                unpack4(reinterpret_cast<const Pix*>(st + G::RAW_BYTES) + r * TW + 4 * q, ds);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int e = (int)rf[i] - (int)ds[i];
+                    sse_y += (Acc)((long long)e * e);
+                }
+            }
+        }
+        if constexpr (FUSED) {
+            const Pix* sc = reinterpret_cast<const Pix*>(st + G::RAW_BYTES + G::DIST_BYTES);
+            constexpr int CE = G::CH * G::CW;
+            const int off = (tid >> 4) * G::CW + 4 * (tid & 15);
+            uint32_t ru[4], du[4], rv[4], dv[4];
+            unpack4(sc + off, ru);
+            unpack4(sc + CE + off, du);
+            unpack4(sc + 2 * CE + off, rv);
+            unpack4(sc + 3 * CE + off, dv);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int eu = (int)ru[i] - (int)du[i], ev = (int)rv[i] - (int)dv[i];
+                sse_u += (Acc)((long long)eu * eu);
+                sse_v += (Acc)((long long)ev * ev);
+            }
+        }
+
+        // ---- one atomic per block per accumulator
+        if (do_sad || FUSED) {
+            sad = warp_sum(sad);
+            if constexpr (FUSED) {
+                sse_y = warp_sum(sse_y);
+                sse_u = warp_sum(sse_u);
+                sse_v = warp_sum(sse_v);
+            }
+            if (lane == 0) {
+                red[warp][0] = sad;
+                red[warp][1] = sse_y;
+                red[warp][2] = sse_u;
+                red[warp][3] = sse_v;
+            }
+        }
+        __syncthreads();
+        if ((do_sad || FUSED) && warp == 0) {
+            unsigned long long t0 = lane < NW ? red[lane][0] : 0ull;
+            unsigned long long t1 = 0, t2 = 0, t3 = 0;
+            if constexpr (FUSED) {
+                t1 = lane < NW ? red[lane][1] : 0ull;
+                t2 = lane < NW ? red[lane][2] : 0ull;
+                t3 = lane < NW ? red[lane][3] : 0ull;
+            }
+#pragma unroll
+            for (int o = NW / 2; o > 0; o >>= 1) {
+                t0 += __shfl_xor_sync(0xffffffffu, t0, o);
+                if constexpr (FUSED) {
+                    t1 += __shfl_xor_sync(0xffffffffu, t1, o);
+                    t2 += __shfl_xor_sync(0xffffffffu, t2, o);
+                    t3 += __shfl_xor_sync(0xffffffffu, t3, o);
+                }
+            }
+            if (lane == 0 && do_sad) atomicAdd(a.sad_out + f, t0);
+            if constexpr (FUSED) {
+                if (lane == 1) atomicAdd(a.sse_out + 3LL * f + 0, t1);
+                if (lane == 2) atomicAdd(a.sse_out + 3LL * f + 1, t2);
+                if (lane == 3) atomicAdd(a.sse_out + 3LL * f + 2, t3);
+            }
+        }
+    }
+
+    if (a.store_last && a.n > 0) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int y = y0 + rbase + 8 * k;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int x = x0 + 4 * q + i;
+                if (y < a.h && x < a.w) a.bprev[(long long)y * a.bprev_pitch + x] = (uint16_t)bp[k][i];
+            }
+        }
+    }
+}
+
+template <typename Pix, bool FUSED>
+static cudaError_t launch_one(const TileArgs& a, cudaStream_t s) {
+    using G = Geo<Pix>;
+    constexpr int STAGE = FUSED ? G::STAGE_FUSED : G::STAGE_MOTION;
+    constexpr int SMEM = 2 * STAGE + G::SV_BYTES;
+    // the shared-memory opt-in is per device; remember which devices have it
+    static unsigned long long configured = 0;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const unsigned long long bit = 1ull << (dev & 63);
+    if (!(__atomic_load_n(&configured, __ATOMIC_ACQUIRE) & bit)) {
+        e = cudaFuncSetAttribute(motion_tile_kernel<Pix, FUSED>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+        if (e != cudaSuccess) return e;
+        __atomic_fetch_or(&configured, bit, __ATOMIC_RELEASE);
+    }
+    dim3 grid((a.w + TW - 1) / TW, (a.h + TH - 1) / TH);
+    motion_tile_kernel<Pix, FUSED><<<grid, NT, SMEM, s>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_motion_tile(const TileArgs& a, bool fused, cudaStream_t s, int* launches) {
+    if (a.n <= 0) return cudaSuccess;
+    *launches += 1;
+    if (a.bpc == 8) return fused ? launch_one<uint8_t, true>(a, s) : launch_one<uint8_t, false>(a, s);
+    return fused ? launch_one<uint16_t, true>(a, s) : launch_one<uint16_t, false>(a, s);
+}
+
+}  // namespace mg

@@ -1,0 +1,164 @@
+"""CPU-side checks of the C-ABI library (no GPU needed): it loads, exports every
+symbol include/motion.h declares, validates arguments on the host, and its host
+helpers follow the score / PSNR definitions.  Also the source contracts of the
+kernels and the separation between the product and the oracle."""
+import os
+import re
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "motion.h")
+CSRC = os.path.join(ROOT, "integer_image_filter_gb300", "csrc")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import integer_image_filter_gb300 as iif
+    from integer_image_filter_gb300 import _build
+    _build.build()
+    return iif.load_library()
+
+
+def declared_functions():
+    names = []
+    for fn in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            names += re.findall(r"^MOTION_API\s+[\w\s\*]+?\b(\w+)\s*\(", text, flags=re.M)
+    return names
+
+
+def test_header_declares_the_boundary():
+    names = set(declared_functions())
+    for required in ("motion_init", "motion_submit", "motion_submit_batch", "psnr_sse",
+                     "psnr_sse_yuv420_batch", "motion_psnr_yuv420_batch"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} declared in include/ but not exported"
+
+
+def test_binding_names_match_the_header():
+    import integer_image_filter_gb300 as iif
+    for name in declared_functions():
+        assert name in iif.EXPORTED_SYMBOLS
+        if name != "motion_last_cuda_error":
+            assert callable(getattr(iif, name))
+
+
+def test_host_argument_validation(lib):
+    import ctypes
+    h = ctypes.c_void_p()
+    assert lib.motion_init(2, 10, 8, ctypes.byref(h)) == 2          # too small
+    assert lib.motion_init(10, 2, 8, ctypes.byref(h)) == 2
+    assert lib.motion_init(10, 10, 7, ctypes.byref(h)) == 3         # bpc
+    assert lib.motion_init(10, 10, 17, ctypes.byref(h)) == 3
+    assert lib.motion_init(40000, 10, 8, ctypes.byref(h)) == 5      # too large
+    assert lib.motion_init(10, 10, 8, None) == 1
+    assert lib.psnr_sse(None, None, 16, 16, 8, 8, 7, None, None) == 3
+    assert lib.psnr_sse(None, None, 16, 16, 0, 8, 8, None, None) == 1
+    assert lib.motion_destroy(None) == 0
+    assert lib.motion_reset(None) == 1
+    assert lib.motion_submit_batch(None, None, 0, 0, 0, None, None) == 1
+
+
+def test_init_without_device_reports_it(lib):
+    import ctypes
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a device is present")
+    h = ctypes.c_void_p()
+    assert lib.motion_init(64, 48, 8, ctypes.byref(h)) == 8
+
+
+def test_strerror_names_every_status(lib):
+    import integer_image_filter_gb300 as iif
+    for code in range(10):
+        assert iif.motion_strerror(code) != "unknown status"
+    assert iif.motion_strerror(99) == "unknown status"
+
+
+def test_scores_helper_matches_definition(lib, oracle):
+    import integer_image_filter_gb300 as iif
+    rng = np.random.default_rng(5)
+    sad = rng.integers(0, 2**40, size=33).astype(np.uint64)
+    sad[0] = 0
+    for (w, h) in ((64, 48), (3840, 2160), (3, 3)):
+        s, m2 = iif.motion_scores_from_sad(sad, w, h)
+        so, m2o = oracle.scores(sad, w, h)
+        assert np.array_equal(s, so) and np.array_equal(m2, m2o)
+        s, m2 = iif.motion_scores_from_sad(sad, w, h, next_score=0.5)
+        so, m2o = oracle.scores(sad, w, h, next_score=0.5)
+        assert np.array_equal(m2, m2o)
+    assert iif.motion_scores_from_sad(np.zeros(0, np.uint64), 4, 4)[0].size == 0
+
+
+def test_psnr_helper(lib):
+    import oracle
+    import integer_image_filter_gb300 as iif
+    mse, db = iif.psnr_from_sse(0, 100, 8)
+    assert mse == 0.0 and db == float("inf")
+    for sse, n, bpc in ((100, 100, 8), (12345, 999, 10), (7, 3, 16)):
+        mse, db = iif.psnr_from_sse(sse, n, bpc)
+        assert mse == sse / n
+        assert abs(db - oracle.psnr_db(sse, n, bpc)) <= 1e-12 * abs(db)
+
+
+# ---------------------------------------------------------------- source contracts
+def _kernel_sources():
+    return {f: open(os.path.join(CSRC, f)).read() for f in os.listdir(CSRC)
+            if f.endswith((".cu", ".cuh"))}
+
+
+def contract_violations(src: str) -> list:
+    """Checks in the spirit of a kernel source contract: no cluster multicast,
+    every atomic is a 64-bit add issued once per block per accumulator (inside
+    a lane-guarded branch), no runtime index into kernel-parameter arrays."""
+    bad = []
+    if "multicast::cluster" in src:
+        bad.append("cluster multicast")
+    for m in re.finditer(r"atomicAdd\(([^;]*)\);", src):
+        # the guard sits on the atomic's line or on the line before it
+        line_start = src.rfind("\n", 0, m.start())
+        line_start = src.rfind("\n", 0, max(line_start, 0)) + 1
+        line = src[line_start:m.start()]
+        if not re.search(r"if \((lane|threadIdx\.x) == \d", line):
+            bad.append("atomic not guarded by a single lane: " + line.strip())
+    if re.search(r"\ba\.\w+\[[^\]]*(threadIdx|blockIdx|plane|lane)", src):
+        bad.append("runtime index into a kernel-parameter array")
+    return bad
+
+
+def test_kernel_source_contract():
+    for name, src in _kernel_sources().items():
+        assert contract_violations(src) == [], name
+    tile = _kernel_sources()["motion_tile.cu"]
+    # the vertical pass writes a V tile that the horizontal pass reads
+    assert "sV" in tile and "vtap(" in tile
+
+
+@pytest.mark.parametrize("plant", [
+    'asm("cp.async.bulk.tensor.2d.shared::cluster.global.multicast::cluster");',
+    "    atomicAdd(a.sad_out + f, t0);",
+    "    const uint8_t* p = a.planes[plane];",
+])
+def test_contract_catches_planted_regressions(plant):
+    assert contract_violations(plant + "\n") != []
+
+
+def test_product_and_oracle_are_separate():
+    pkg = os.path.join(ROOT, "integer_image_filter_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert not re.search(r"^\s*(import|from)\s+oracle\b", text, flags=re.M), f
+                assert "oracle.c" not in text and "liboracle" not in text, f
+    for f in os.listdir(os.path.join(ROOT, "oracle")):
+        if f.endswith((".py", ".c")):
+            text = open(os.path.join(ROOT, "oracle", f)).read()
+            assert "integer_image_filter_gb300" not in text and "motion.h" not in text, f
