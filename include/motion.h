@@ -174,6 +174,19 @@ MOTION_API int motion_scores_from_sad(const uint64_t* sad, int n, int w, int h,
 MOTION_API int psnr_from_sse(uint64_t sse, uint64_t n_samples, int bpc, double* mse,
                   double* psnr_db);
 
+/* Kernel selection for a context (diagnostics and tests): MOTION_PATH_AUTO
+ * uses the TMA kernel whenever every plane is 16-byte aligned (base, pitch,
+ * stride) and the generic kernel otherwise; MOTION_PATH_GENERIC always uses
+ * the generic kernel.  Results are identical on both paths. */
+#define MOTION_PATH_AUTO 0
+#define MOTION_PATH_GENERIC 1
+MOTION_API int motion_set_kernel_path(motion_ctx* ctx, int path);
+
+/* Read and clear the context's device error word after waiting for the
+ * device: bit 0 set means a kernel's bounded wait for a staged tile ran out
+ * (its results are then incomplete).  *flags receives the word. */
+MOTION_API int motion_device_error(motion_ctx* ctx, int* flags);
+
 /* Number of this library's kernels launched by the calls above since load. */
 MOTION_API uint64_t motion_kernel_launch_count(void);
 

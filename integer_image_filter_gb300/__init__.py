@@ -25,6 +25,7 @@ __all__ = [
     "motion_psnr_yuv420_batch_host", "motion_reserve_host_staging", "psnr_sse",
     "psnr_sse_yuv420_batch", "motion_scores_from_sad", "psnr_from_sse",
     "motion_kernel_launch_count", "motion_strerror", "MotionContext", "EXPORTED_SYMBOLS",
+    "motion_set_kernel_path", "motion_device_error", "MOTION_PATH_AUTO", "MOTION_PATH_GENERIC",
 ]
 
 EXPORTED_SYMBOLS = (
@@ -32,6 +33,7 @@ EXPORTED_SYMBOLS = (
     "motion_psnr_yuv420_batch", "motion_psnr_yuv420_batch_host", "motion_reserve_host_staging",
     "psnr_sse", "psnr_sse_yuv420_batch", "motion_scores_from_sad", "psnr_from_sse",
     "motion_kernel_launch_count", "motion_strerror", "motion_last_cuda_error",
+    "motion_set_kernel_path", "motion_device_error",
 )
 
 _LIB: ctypes.CDLL | None = None
@@ -67,6 +69,8 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
         "motion_kernel_launch_count": ([], ctypes.c_uint64),
         "motion_strerror": ([I], ctypes.c_char_p),
         "motion_last_cuda_error": ([], I),
+        "motion_set_kernel_path": ([P, I], I),
+        "motion_device_error": ([P, ctypes.POINTER(I)], I),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -286,6 +290,20 @@ def psnr_from_sse(sse: int, n_samples: int, bpc: int):
     return float(mse.value), float(db.value)
 
 
+MOTION_PATH_AUTO = 0
+MOTION_PATH_GENERIC = 1
+
+
+def motion_set_kernel_path(ctx: int, path: int) -> None:
+    _check(load_library().motion_set_kernel_path(ctx, path), "motion_set_kernel_path")
+
+
+def motion_device_error(ctx: int) -> int:
+    v = ctypes.c_int()
+    _check(load_library().motion_device_error(ctx, ctypes.byref(v)), "motion_device_error")
+    return int(v.value)
+
+
 def motion_kernel_launch_count() -> int:
     return int(load_library().motion_kernel_launch_count())
 
@@ -320,6 +338,12 @@ class MotionContext:
 
     def reset(self) -> None:
         motion_reset(self.handle)
+
+    def set_kernel_path(self, path: int) -> None:
+        motion_set_kernel_path(self.handle, path)
+
+    def device_error(self) -> int:
+        return motion_device_error(self.handle)
 
     def submit(self, frame, stream=None):
         return motion_submit(self.handle, frame, stream=stream)

@@ -65,6 +65,8 @@ struct motion_ctx {
     int bprev_pitch = 0;            // elements per row of the resident plane
     uint16_t* d_bprev = nullptr;    // previous frame's blurred plane (B_{i-1})
     int has_prev = 0;
+    int* d_err = nullptr;           // device error word (bounded waits that timed out)
+    int force_generic = 0;          // diagnostics: always use the generic kernel
     unsigned long long* d_slot = nullptr;   // single-submit result
     unsigned long long* h_slot = nullptr;   // pinned readback slot
     // host-buffer pipeline
@@ -101,6 +103,19 @@ void free_staging(motion_ctx* c) {
     c->stage_pairs = 0;
 }
 
+// The TMA kernel when the layout allows it, else the generic kernel.
+int launch_motion(motion_ctx* c, const mg::TileArgs& a, bool fused, cudaStream_t s) {
+    int launched = 0;
+    bool used = false;
+    cudaError_t e = cudaSuccess;
+    if (!c->force_generic) e = mg::launch_motion_tma(a, fused, s, &launched, &used);
+    if (e == cudaSuccess && !used) e = mg::launch_motion_tile(a, fused, s, &launched);
+    g_launches += (uint64_t)launched;
+    if (e != cudaSuccess) return cuda_fail(e);
+    c->has_prev = 1;
+    return MOTION_OK;
+}
+
 mg::TileArgs motion_args(motion_ctx* c, int n) {
     mg::TileArgs a;
     std::memset(&a, 0, sizeof(a));
@@ -114,6 +129,7 @@ mg::TileArgs motion_args(motion_ctx* c, int n) {
     a.store_last = 1;
     a.bprev = c->d_bprev;
     a.bprev_pitch = c->bprev_pitch;
+    a.err = c->d_err;
     return a;
 }
 
@@ -152,12 +168,7 @@ int launch_fused(motion_ctx* c, int n, const void* ry, const void* ru, const voi
                   aligned16(du, pitch_uv, stride_uv, n) && aligned16(dv, pitch_uv, stride_uv, n);
     a.sad_out = (unsigned long long*)d_sad;
     a.sse_out = (unsigned long long*)d_sse;
-    int launched = 0;
-    cudaError_t e = mg::launch_motion_tile(a, true, s, &launched);
-    g_launches += (uint64_t)launched;
-    if (e != cudaSuccess) return cuda_fail(e);
-    c->has_prev = 1;
-    return MOTION_OK;
+    return launch_motion(c, a, true, s);
 }
 
 }  // namespace
@@ -188,6 +199,8 @@ int motion_init(int w, int h, int bpc, motion_ctx** out) {
     if (e == cudaSuccess)
         e = cudaMalloc(&c->d_bprev, sizeof(uint16_t) * (size_t)c->bprev_pitch * (size_t)h);
     if (e == cudaSuccess) e = cudaMalloc(&c->d_slot, sizeof(unsigned long long));
+    if (e == cudaSuccess) e = cudaMalloc(&c->d_err, sizeof(int));
+    if (e == cudaSuccess) e = cudaMemset(c->d_err, 0, sizeof(int));
     if (e == cudaSuccess) e = cudaMallocHost(&c->h_slot, sizeof(unsigned long long));
     if (e != cudaSuccess) {
         motion_destroy(c);
@@ -205,6 +218,7 @@ int motion_destroy(motion_ctx* c) {
     free_staging(c);
     if (c->d_bprev) cudaFree(c->d_bprev);
     if (c->d_slot) cudaFree(c->d_slot);
+    if (c->d_err) cudaFree(c->d_err);
     if (c->h_slot) cudaFreeHost(c->h_slot);
     if (prev >= 0) cudaSetDevice(prev);
     delete c;
@@ -233,12 +247,7 @@ int motion_submit_batch(motion_ctx* c, const void* d_frames, int n, size_t frame
     a.stride_y = (long long)frame_stride;
     a.aligned16 = aligned16(d_frames, pitch, frame_stride, n);
     a.sad_out = (unsigned long long*)d_sad_out;
-    int launched = 0;
-    cudaError_t e = mg::launch_motion_tile(a, false, s, &launched);
-    g_launches += (uint64_t)launched;
-    if (e != cudaSuccess) return cuda_fail(e);
-    c->has_prev = 1;
-    return MOTION_OK;
+    return launch_motion(c, a, false, s);
 }
 
 int motion_submit(motion_ctx* c, const void* d_frame, size_t pitch, void* stream,
@@ -470,6 +479,25 @@ int psnr_from_sse(uint64_t sse, uint64_t n_samples, int bpc, double* mse, double
         const double peak = (double)((1u << bpc) - 1u);
         *psnr_db = sse == 0 ? INFINITY : 10.0 * std::log10(peak * peak / m);
     }
+    return MOTION_OK;
+}
+
+int motion_set_kernel_path(motion_ctx* c, int path) {
+    if (!c || (path != MOTION_PATH_AUTO && path != MOTION_PATH_GENERIC))
+        return MOTION_ERR_INVALID_ARGUMENT;
+    c->force_generic = path == MOTION_PATH_GENERIC;
+    return MOTION_OK;
+}
+
+int motion_device_error(motion_ctx* c, int* flags) {
+    if (!c || !flags) return MOTION_ERR_INVALID_ARGUMENT;
+    int rc = ctx_device_ok(c);
+    if (rc) return rc;
+    MG_CUDA(cudaDeviceSynchronize());
+    int v = 0;
+    MG_CUDA(cudaMemcpy(&v, c->d_err, sizeof(int), cudaMemcpyDeviceToHost));
+    MG_CUDA(cudaMemset(c->d_err, 0, sizeof(int)));
+    *flags = v;
     return MOTION_OK;
 }
 

@@ -4,6 +4,9 @@
 
 #include <cstdint>
 #include <cstddef>
+#include <cstring>
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 namespace mg {
@@ -27,6 +30,14 @@ struct TileArgs {
     int bprev_pitch;
     unsigned long long* sad_out;  // [n], zeroed by the caller
     unsigned long long* sse_out;  // [n][3], zeroed by the caller (fused only)
+    int* err;                     // device error word (bit 0: a stage wait timed out)
+};
+
+// Tensor maps of one TMA launch (64-byte aligned, passed as a grid constant).
+struct TmaMaps {
+    CUtensorMap raw;              // reference luma, box (TW + 2 HX) x (TH + 4) x 1
+    CUtensorMap dist;             // distorted luma, box TW x TH x 1
+    CUtensorMap ru, du, rv, dv;   // chroma planes, box TW/2 x TH/2 x 1
 };
 
 // Arguments of one batched SSE launch over n pairs x (1 or 3) planes.
@@ -42,8 +53,13 @@ struct SseArgs {
     unsigned long long* sse_out;       // [n][planes], zeroed by the caller
 };
 
+// Generic kernel: any pitch / alignment (sample loads on border tiles).
 cudaError_t launch_motion_tile(const TileArgs& a, bool fused, cudaStream_t s,
                                int* launches);
+// TMA kernel: 16-byte aligned layouts.  *used is false when the layout does not
+// suit TMA (nothing launched; the caller falls back to launch_motion_tile).
+cudaError_t launch_motion_tma(const TileArgs& a, bool fused, cudaStream_t s, int* launches,
+                              bool* used);
 cudaError_t launch_sse(const SseArgs& a, cudaStream_t s, int sm_count, int* launches);
 
 }  // namespace mg

@@ -19,50 +19,10 @@
 //    and shared memory, then ONE 64-bit atomic per block per frame and per
 //    accumulator (same page, Decision 1).  Integer sums are order-independent,
 //    so the result is exact (same page, Context).
-#include "motion_common.cuh"
 #include "motion_internal.h"
+#include "tile_geometry.cuh"
 
 namespace mg {
-
-constexpr int TW = 128;            // output tile width, samples
-constexpr int TH = 32;             // output tile height, rows
-constexpr int NT = 256;            // threads per CTA
-constexpr int NW = NT / 32;
-constexpr int SVW = TW + 8;        // V tile row pitch (uint32); col j <-> x = x0 - 4 + j
-
-template <typename Pix>
-struct Geo {
-    static constexpr int S = sizeof(Pix);
-    static constexpr int HX = 16 / S;                 // halo columns staged on each side
-    static constexpr int RAW_W = TW + 2 * HX;         // staged luma row, samples
-    static constexpr int RAW_ROWS = TH + 4;
-    static constexpr int RAW_BYTES = RAW_ROWS * RAW_W * S;
-    static constexpr int DIST_BYTES = TH * TW * S;
-    static constexpr int CW = TW / 2, CH = TH / 2;    // 4:2:0 chroma tile
-    static constexpr int C_BYTES = CH * CW * S;
-    static constexpr int STAGE_MOTION = RAW_BYTES;
-    static constexpr int STAGE_FUSED = RAW_BYTES + DIST_BYTES + 4 * C_BYTES;
-    static constexpr int SV_BYTES = TH * SVW * 4;
-    static_assert(RAW_BYTES % 16 == 0 && DIST_BYTES % 16 == 0 && C_BYTES % 16 == 0, "16B");
-};
-
-template <typename Pix> struct SseAcc;
-template <> struct SseAcc<uint8_t> { using T = uint32_t; };            // 4096 * 255^2 < 2^32
-template <> struct SseAcc<uint16_t> { using T = unsigned long long; };
-
-__device__ __forceinline__ void unpack4(const uint8_t* p, uint32_t (&o)[4]) {
-    const uint32_t w = *reinterpret_cast<const uint32_t*>(p);
-    o[0] = w & 0xffu; o[1] = (w >> 8) & 0xffu; o[2] = (w >> 16) & 0xffu; o[3] = w >> 24;
-}
-__device__ __forceinline__ void unpack4(const uint16_t* p, uint32_t (&o)[4]) {
-    const uint2 w = *reinterpret_cast<const uint2*>(p);
-    o[0] = w.x & 0xffffu; o[1] = w.x >> 16; o[2] = w.y & 0xffffu; o[3] = w.y >> 16;
-}
-
-__device__ __forceinline__ uint32_t vtap(uint32_t a, uint32_t b, uint32_t c, uint32_t d,
-                                         uint32_t e, uint32_t rnd, int sh) {
-    return (kT0 * (a + e) + kT1 * (b + d) + kT2 * c + rnd) >> sh;
-}
 
 template <typename Pix, bool FUSED>
 __device__ __forceinline__ void load_stage(const TileArgs& a, int f, unsigned char* st,

@@ -1,0 +1,479 @@
+// motion_tma.cu -- the batched motion kernel (blur + SAD against the previous
+// frame), optionally fused with the per-plane SSE of 4:2:0 pairs, fed by the
+// Tensor Memory Accelerator.
+//
+// Structure (GB300 / sm_103a):
+//  * One CTA owns a TW x TH output tile and walks the batch of frames in time
+//    order; B_prev of its tile stays in registers, so every frame is read from
+//    HBM once ("Making it fast: three rounds on one pipeline", Round 1 --
+//    one kernel over all frames).
+//  * Thread 0 keeps STAGES frames in flight: for each frame it issues 3-D tiled
+//    TMA loads (cp.async.bulk.tensor, x / y / frame coordinates) of the luma
+//    box with its 2-row and 16-byte halo -- and, fused, the distorted luma
+//    tile and the four chroma tiles -- completing on that stage's mbarrier.
+//    Out-of-frame parts of a box arrive zero-filled; tiles on the frame border
+//    then write the mirrored halo in shared memory (i<0 -> -i, i>=n -> 2n-i-2),
+//    so no tile takes a sample-by-sample path.
+//  * Separable blur: the vertical 5-tap pass once per sample (rounded >> bpc)
+//    into a shared V tile, then the horizontal 5-tap pass (rounded >> 16)
+//    ("ADR-1392: CUDA motion, PSNR and moment kernels add one atomic per
+//    block, the motion SAD filters separably, ...", Decision 4).
+//  * Per frame each warp reduces its partial sums with one warp-reduce
+//    instruction, warp 0 combines the warps, and the block adds each
+//    accumulator to its 64-bit output with ONE atomic (same page, Decision 1;
+//    integer sums are order-independent, so the result is exact -- Context).
+//  * Every mbarrier wait is bounded: on time-out the CTA raises the device
+//    error word and leaves instead of spinning.
+#include <cuda.h>
+
+#include "motion_internal.h"
+#include "tile_geometry.cuh"
+
+namespace mg {
+
+constexpr long long kWaitCycles = 1LL << 31;  // about one second: a stage wait never lasts longer
+
+// Mirror the halo of a staged luma box in place for tiles on the frame border.
+template <typename Pix>
+__device__ __forceinline__ void patch_mirror(Pix* raw, const TileArgs& a, int x0, int y0,
+                                             bool pl, bool pr, bool pt, bool pb) {
+    using G = Geo<Pix>;
+    const int tid = threadIdx.x;
+    // columns first (every staged row), then whole rows (so corners follow)
+    if (pl || pr) {
+        const int cw0 = a.w - x0 + G::HX;  // staged column of x = w
+        for (int i = tid; i < 4 * G::RAW_ROWS; i += NT) {
+            const int r = i >> 2, which = i & 3;
+            Pix* row = raw + r * G::RAW_W;
+            if (which < 2) {
+                if (pl) row[G::HX - 1 - which] = row[G::HX + 1 + which];    // x=-1,-2 <- 1,2
+            } else if (pr) {
+                const int k = which - 2;                                      // x=w+k <- w-2-k
+                row[cw0 + k] = row[cw0 - 2 - k];
+            }
+        }
+        __syncthreads();
+    }
+    if (pt || pb) {
+        const int rh = a.h - y0 + 2;      // staged row of y = h
+        for (int i = tid; i < 4 * G::RAW_W; i += NT) {
+            const int which = i / G::RAW_W, c = i - which * G::RAW_W;
+            if (which < 2) {
+                if (pt) raw[(1 - which) * G::RAW_W + c] = raw[(3 + which) * G::RAW_W + c];  // y=-1,-2 <- 1,2
+            } else if (pb) {
+                const int k = which - 2;                                   // y=h+k <- h-2-k
+                if (rh + k < G::RAW_ROWS) raw[(rh + k) * G::RAW_W + c] = raw[(rh - 2 - k) * G::RAW_W + c];
+            }
+        }
+        __syncthreads();
+    }
+    // these generic writes precede a later TMA refill of the same stage
+    fence_proxy_async();
+}
+
+// The vertical 5-tap pass for one warp: 4 output rows (staged rows 4w..4w+7
+// feed them) x 128 columns, lane = quad of 4 columns; result V (uint32) into
+// the warp's own rows of sV.  8-bit samples use byte-pair dot products: the
+// rows are interleaved two at a time so that one dp2a applies two taps to two
+// rows of one column (exact: sums stay below 2^24).
+__device__ __forceinline__ void vertical_quad(const uint8_t* src, uint32_t* dst, uint32_t rnd,
+                                              int sh) {
+    constexpr int RW = Geo<uint8_t>::RAW_W;
+    uint32_t wv[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) wv[i] = *reinterpret_cast<const uint32_t*>(src + i * RW);
+    uint32_t lo[7], hi[7];  // rows (i, i+1): columns 0,1 in lo, columns 2,3 in hi
+#pragma unroll
+    for (int i = 0; i < 7; ++i) {
+        lo[i] = __byte_perm(wv[i], wv[i + 1], 0x5140);
+        hi[i] = __byte_perm(wv[i], wv[i + 1], 0x7362);
+    }
+    constexpr uint32_t T01 = kT0 | (kT1 << 16);   // taps of rows j, j+1
+    constexpr uint32_t T23 = kT2 | (kT1 << 16);   // rows j+2, j+3 (t3 = t1)
+    constexpr uint32_t T_4 = kT0 << 16;            // row j+4 as the upper row of (j+3, j+4)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        uint4 o;
+        o.x = __dp2a_lo(T01, lo[j], __dp2a_lo(T23, lo[j + 2], __dp2a_lo(T_4, lo[j + 3], rnd))) >> sh;
+        o.y = __dp2a_hi(T01, lo[j], __dp2a_hi(T23, lo[j + 2], __dp2a_hi(T_4, lo[j + 3], rnd))) >> sh;
+        o.z = __dp2a_lo(T01, hi[j], __dp2a_lo(T23, hi[j + 2], __dp2a_lo(T_4, hi[j + 3], rnd))) >> sh;
+        o.w = __dp2a_hi(T01, hi[j], __dp2a_hi(T23, hi[j + 2], __dp2a_hi(T_4, hi[j + 3], rnd))) >> sh;
+        *reinterpret_cast<uint4*>(dst + j * SVW) = o;
+    }
+}
+__device__ __forceinline__ void vertical_quad(const uint16_t* src, uint32_t* dst, uint32_t rnd,
+                                              int sh) {
+    constexpr int RW = Geo<uint16_t>::RAW_W;
+    uint32_t p[8][4];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) unpack4(src + i * RW, p[i]);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        uint4 o;
+        o.x = vtap(p[j][0], p[j + 1][0], p[j + 2][0], p[j + 3][0], p[j + 4][0], rnd, sh);
+        o.y = vtap(p[j][1], p[j + 1][1], p[j + 2][1], p[j + 3][1], p[j + 4][1], rnd, sh);
+        o.z = vtap(p[j][2], p[j + 1][2], p[j + 2][2], p[j + 3][2], p[j + 4][2], rnd, sh);
+        o.w = vtap(p[j][3], p[j + 1][3], p[j + 2][3], p[j + 3][3], p[j + 4][3], rnd, sh);
+        *reinterpret_cast<uint4*>(dst + j * SVW) = o;
+    }
+}
+
+template <typename Pix, bool FUSED, int STAGES>
+__global__ void __launch_bounds__(NT) motion_tma_kernel(const __grid_constant__ TmaMaps maps,
+                                                         const TileArgs a) {
+    using G = Geo<Pix>;
+    using Acc = typename SseAcc<Pix>::T;
+    constexpr int STAGE = FUSED ? G::STAGE_FUSED : G::STAGE_MOTION;
+    constexpr int SLOTS = 8;  // reduction slots; a warp runs at most STAGES frames ahead
+    static_assert(SLOTS > STAGES, "reduction slots must outnumber the stages");
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    // TMA destinations must sit on 128-byte boundaries; the launch adds 128 B of slack
+    unsigned char* smem = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);
+    __shared__ __align__(8) uint64_t full[STAGES];   // TMA bytes landed
+    __shared__ __align__(8) uint64_t empty[STAGES];  // every warp done with the stage
+    __shared__ unsigned long long acc_s[SLOTS][4];   // per-frame block sums
+    __shared__ unsigned cnt_s[SLOTS];                // warps that added to a slot
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    // each warp owns output rows 4w .. 4w+3 of the tile; its V rows are private
+    uint32_t* sV = reinterpret_cast<uint32_t*>(smem + STAGES * STAGE) + warp * 4 * SVW;
+    const int x0 = blockIdx.x * TW, y0 = blockIdx.y * TH;
+    const bool full_tile = (x0 + TW <= a.w) && (y0 + TH <= a.h);
+    const bool pl = x0 == 0, pt = y0 == 0;
+    const bool pr = x0 + TW + 2 > a.w, pb = y0 + TH + 2 > a.h;
+    const bool edge = pl || pr || pt || pb;
+    const uint32_t rnd = 1u << (a.bpc - 1);
+    const int sh = a.bpc;
+
+    if (tid == 0) {
+#pragma unroll
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], NW);
+        }
+        fence_mbar_init();
+        prefetch_tmap(&maps.raw);
+        if constexpr (FUSED) {
+            prefetch_tmap(&maps.dist);
+            prefetch_tmap(&maps.ru);
+            prefetch_tmap(&maps.du);
+            prefetch_tmap(&maps.rv);
+            prefetch_tmap(&maps.dv);
+        }
+    }
+    if (tid < SLOTS * 4) acc_s[tid >> 2][tid & 3] = 0;
+    if (tid < SLOTS) cnt_s[tid] = 0;
+    __syncthreads();
+
+    auto issue = [&](int f) {  // thread 0 only
+        const int s = f % STAGES;
+        unsigned char* st = smem + s * STAGE;
+        fence_proxy_async();
+        mbar_arrive_expect_tx(&full[s], STAGE);
+        tma_load_3d(st, &maps.raw, x0 - G::HX, y0 - 2, f, &full[s]);
+        if constexpr (FUSED) {
+            tma_load_3d(st + G::RAW_BYTES, &maps.dist, x0, y0, f, &full[s]);
+            unsigned char* sc = st + G::RAW_BYTES + G::DIST_BYTES;
+            tma_load_3d(sc, &maps.ru, x0 / 2, y0 / 2, f, &full[s]);
+            tma_load_3d(sc + G::C_BYTES, &maps.du, x0 / 2, y0 / 2, f, &full[s]);
+            tma_load_3d(sc + 2 * G::C_BYTES, &maps.rv, x0 / 2, y0 / 2, f, &full[s]);
+            tma_load_3d(sc + 3 * G::C_BYTES, &maps.dv, x0 / 2, y0 / 2, f, &full[s]);
+        }
+    };
+    if (tid == 0) {
+        const int pre = a.n < STAGES ? a.n : STAGES;
+        for (int f = 0; f < pre; ++f) issue(f);
+    }
+
+    // this thread's outputs: rows 4w + k, columns 4q .. 4q+3 (q = lane)
+    const int q = lane;
+    uint32_t bp[4][4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int y = y0 + 4 * warp + k;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int x = x0 + 4 * q + i;
+            bp[k][i] = (a.has_prev && y < a.h && x < a.w) ? a.bprev[(long long)y * a.bprev_pitch + x] : 0u;
+        }
+    }
+    // valid columns of this thread's quad in each of its rows (edge tiles)
+    int nvalid[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        int nv = (y0 + 4 * warp + k < a.h) ? a.w - (x0 + 4 * q) : 0;
+        nvalid[k] = nv < 0 ? 0 : (nv > 4 ? 4 : nv);
+    }
+
+    for (int f = 0; f < a.n; ++f) {
+        const int s = f % STAGES;
+        const unsigned parity = (unsigned)(f / STAGES) & 1u;
+        const bool ok = mbar_wait_bounded(&full[s], parity, kWaitCycles);
+        unsigned char* st = smem + s * STAGE;
+        Pix* raw = reinterpret_cast<Pix*>(st);
+        if (edge) {
+            // border tiles patch the mirrored halo together (block barriers)
+            if (!__syncthreads_and(ok)) {
+                if (tid == 0 && a.err) atomicOr(a.err, 1);
+                mbar_wait_bounded(&full[s], parity, kWaitCycles);
+                return;
+            }
+            patch_mirror<Pix>(raw, a, x0, y0, pl, pr, pt, pb);
+        } else if (!__all_sync(0xffffffffu, ok)) {
+            if (lane == 0 && a.err) atomicOr(a.err, 1);
+            mbar_wait_bounded(&full[s], parity, kWaitCycles);
+            return;
+        }
+
+        // ---- vertical pass of the warp's 4 rows (staged row r <-> y0 - 2 + r)
+        vertical_quad(raw + (warp * 4) * G::RAW_W + G::HX + 4 * lane, sV + 4 + 4 * lane, rnd, sh);
+        if (lane < 16) {  // the two halo columns on each side, 4 rows
+            const int r = lane >> 2, which = lane & 3;
+            const int off = which == 0 ? -2 : which == 1 ? -1 : which == 2 ? TW : TW + 1;
+            const Pix* c = raw + (warp * 4 + r) * G::RAW_W + G::HX + off;
+            sV[r * SVW + 4 + off] = vtap(c[0], c[G::RAW_W], c[2 * G::RAW_W], c[3 * G::RAW_W],
+                                         c[4 * G::RAW_W], rnd, sh);
+        }
+        __syncwarp();
+
+        // ---- horizontal pass, SAD against B_prev, squared errors
+        const bool do_sad = (f > 0) || a.has_prev;
+        uint32_t sad = 0;
+        Acc sse_y = 0, sse_u = 0, sse_v = 0;
+        const Pix* dist = reinterpret_cast<const Pix*>(st + G::RAW_BYTES);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int r = 4 * warp + k;
+            const uint32_t* v = sV + k * SVW + 4 * q;
+            const uint4 A = *reinterpret_cast<const uint4*>(v);
+            const uint4 Bq = *reinterpret_cast<const uint4*>(v + 4);
+            const uint4 C = *reinterpret_cast<const uint4*>(v + 8);
+            const uint32_t wv[12] = {A.x, A.y, A.z, A.w, Bq.x, Bq.y, Bq.z, Bq.w, C.x, C.y, C.z, C.w};
+            uint32_t b[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                b[i] = (kT0 * (wv[2 + i] + wv[6 + i]) + kT1 * (wv[3 + i] + wv[5 + i]) +
+                        kT2 * wv[4 + i] + 32768u) >> 16;
+            if (full_tile) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) sad = __sad(b[i], bp[k][i], sad);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) sad = __sad(b[i], i < nvalid[k] ? bp[k][i] : b[i], sad);
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) bp[k][i] = b[i];
+            if constexpr (FUSED) {
+                const Pix* rp = raw + (r + 2) * G::RAW_W + G::HX + 4 * q;
+                const Pix* dp = dist + r * TW + 4 * q;
+                if constexpr (sizeof(Pix) == 1) {
+                    uint32_t d = __vabsdiffu4(*reinterpret_cast<const uint32_t*>(rp),
+                                              *reinterpret_cast<const uint32_t*>(dp));
+                    if (!full_tile)
+                        d &= nvalid[k] <= 0 ? 0u : (0xffffffffu >> (8 * (4 - nvalid[k])));
+                    sse_y = __dp4a(d, d, sse_y);
+                } else {
+                    uint32_t rf[4], ds[4];
+                    unpack4(rp, rf);
+                    unpack4(dp, ds);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const long long e = (long long)rf[i] - (long long)ds[i];
+                        sse_y += i < nvalid[k] ? (Acc)(e * e) : (Acc)0;
+                    }
+                }
+            }
+        }
+        if constexpr (FUSED) {
+            // 4:2:0 chroma: 16 rows x 64 columns per plane; warp w takes rows
+            // 2w, 2w+1, 4 samples per lane; outside the picture both sides were
+            // zero-filled, so they add 0
+            const Pix* sc = reinterpret_cast<const Pix*>(st + G::RAW_BYTES + G::DIST_BYTES);
+            constexpr int CE = G::CH * G::CW;
+            const int off = (2 * warp + (lane >> 4)) * G::CW + 4 * (lane & 15);
+            if constexpr (sizeof(Pix) == 1) {
+                const uint32_t du = __vabsdiffu4(*reinterpret_cast<const uint32_t*>(sc + off),
+                                                 *reinterpret_cast<const uint32_t*>(sc + CE + off));
+                const uint32_t dv = __vabsdiffu4(*reinterpret_cast<const uint32_t*>(sc + 2 * CE + off),
+                                                 *reinterpret_cast<const uint32_t*>(sc + 3 * CE + off));
+                sse_u = __dp4a(du, du, 0u);
+                sse_v = __dp4a(dv, dv, 0u);
+            } else {
+                uint32_t ru[4], du[4], rv[4], dv[4];
+                unpack4(sc + off, ru);
+                unpack4(sc + CE + off, du);
+                unpack4(sc + 2 * CE + off, rv);
+                unpack4(sc + 3 * CE + off, dv);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const long long eu = (long long)ru[i] - (long long)du[i];
+                    const long long ev = (long long)rv[i] - (long long)dv[i];
+                    sse_u += (Acc)(eu * eu);
+                    sse_v += (Acc)(ev * ev);
+                }
+            }
+        }
+        // every lane has finished reading this stage: release it to the producer
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+
+        // ---- one atomic per block per accumulator: warps add into a shared
+        // slot; the last warp to finish the frame adds the slot to the output
+        if (do_sad || FUSED) {
+            const uint32_t wsad = __reduce_add_sync(0xffffffffu, sad);
+            unsigned long long wy = 0, wu = 0, wvv = 0;
+            if constexpr (FUSED) {
+                if constexpr (sizeof(Pix) == 1) {
+                    wy = __reduce_add_sync(0xffffffffu, sse_y);
+                    wu = __reduce_add_sync(0xffffffffu, sse_u);
+                    wvv = __reduce_add_sync(0xffffffffu, sse_v);
+                } else {
+                    wy = warp_sum(sse_y);
+                    wu = warp_sum(sse_u);
+                    wvv = warp_sum(sse_v);
+                }
+            }
+            if (lane == 0) {
+                const int slot = f & (SLOTS - 1);
+                atomicAdd_block(&acc_s[slot][0], (unsigned long long)wsad);
+                if constexpr (FUSED) {
+                    atomicAdd_block(&acc_s[slot][1], wy);
+                    atomicAdd_block(&acc_s[slot][2], wu);
+                    atomicAdd_block(&acc_s[slot][3], wvv);
+                }
+                __threadfence_block();
+                if (atomicAdd_block(&cnt_s[slot], 1u) == NW - 1) {
+                    __threadfence_block();
+                    const unsigned long long t0 = atomicExch_block(&acc_s[slot][0], 0ull);
+                    if (do_sad) atomicAdd(a.sad_out + f, t0);
+                    if constexpr (FUSED) {
+                        atomicAdd(a.sse_out + 3LL * f + 0, atomicExch_block(&acc_s[slot][1], 0ull));
+                        atomicAdd(a.sse_out + 3LL * f + 1, atomicExch_block(&acc_s[slot][2], 0ull));
+                        atomicAdd(a.sse_out + 3LL * f + 2, atomicExch_block(&acc_s[slot][3], 0ull));
+                    }
+                    cnt_s[slot] = 0;
+                }
+            }
+        }
+
+        // ---- refill: the stage of frame f-1 takes frame f+STAGES-1 once every
+        // warp has released it
+        if (tid == 0 && f >= 1 && f + STAGES - 1 < a.n) {
+            const int sp = (f - 1) % STAGES;
+            if (!mbar_wait_bounded(&empty[sp], (unsigned)((f - 1) / STAGES) & 1u, kWaitCycles)) {
+                if (a.err) atomicOr(a.err, 2);
+            } else {
+                issue(f + STAGES - 1);
+            }
+        }
+    }
+
+    if (a.store_last && a.n > 0) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int y = y0 + 4 * warp + k;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int x = x0 + 4 * q + i;
+                if (y < a.h && x < a.w) a.bprev[(long long)y * a.bprev_pitch + x] = (uint16_t)bp[k][i];
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------------ host side
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+        tried = true;
+    }
+    return fn;
+}
+
+bool encode(CUtensorMap* m, int bytes_per_sample, const void* base, int w, int h, int n,
+            long long pitch, long long stride, int box_w, int box_h) {
+    PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+    if (!fn || !base) return false;
+    if (n <= 1) stride = ((pitch * h) + 15) & ~15LL;  // never stepped through
+    cuuint64_t dims[3] = {(cuuint64_t)w, (cuuint64_t)h, (cuuint64_t)(n > 0 ? n : 1)};
+    cuuint64_t strides[2] = {(cuuint64_t)pitch, (cuuint64_t)stride};
+    cuuint32_t box[3] = {(cuuint32_t)box_w, (cuuint32_t)box_h, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    const CUtensorMapDataType dt =
+        bytes_per_sample == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16;
+    return fn(m, dt, 3, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <typename Pix, bool FUSED, int STAGES>
+cudaError_t launch_tma_one(const TmaMaps& maps, const TileArgs& a, cudaStream_t s) {
+    using G = Geo<Pix>;
+    constexpr int STAGE = FUSED ? G::STAGE_FUSED : G::STAGE_MOTION;
+    constexpr int SMEM = STAGES * STAGE + G::SV_BYTES + 128;
+    static unsigned long long configured = 0;  // per device bit
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const unsigned long long bit = 1ull << (dev & 63);
+    if (!(__atomic_load_n(&configured, __ATOMIC_ACQUIRE) & bit)) {
+        e = cudaFuncSetAttribute(motion_tma_kernel<Pix, FUSED, STAGES>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+        if (e != cudaSuccess) return e;
+        __atomic_fetch_or(&configured, bit, __ATOMIC_RELEASE);
+    }
+    dim3 grid((a.w + TW - 1) / TW, (a.h + TH - 1) / TH);
+    motion_tma_kernel<Pix, FUSED, STAGES><<<grid, NT, SMEM, s>>>(maps, a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool tma_usable(const TileArgs& a, bool fused) {
+    if (!encode_fn() || !a.aligned16) return false;
+    // TMA global strides must be multiples of 16 bytes below 2^40
+    if (a.pitch_y % 16 || a.pitch_y >= (1LL << 40)) return false;
+    if (a.n > 1 && (a.stride_y % 16 || a.stride_y >= (1LL << 40))) return false;
+    if (fused) {
+        if (a.pitch_uv % 16 || (a.n > 1 && a.stride_uv % 16)) return false;
+    }
+    return true;
+}
+
+cudaError_t launch_motion_tma(const TileArgs& a, bool fused, cudaStream_t s, int* launches,
+                              bool* used) {
+    *used = false;
+    if (a.n <= 0) return cudaSuccess;
+    if (!tma_usable(a, fused)) return cudaSuccess;
+    const int S = a.bpc == 8 ? 1 : 2;
+    TmaMaps maps;
+    std::memset(&maps, 0, sizeof(maps));
+    const int rawW = TW + 2 * (16 / S), rawH = TH + 4;
+    bool ok = encode(&maps.raw, S, a.ref_y, a.w, a.h, a.n, a.pitch_y, a.stride_y, rawW, rawH);
+    if (fused) {
+        ok = ok && encode(&maps.dist, S, a.dist_y, a.w, a.h, a.n, a.pitch_y, a.stride_y, TW, TH);
+        ok = ok && encode(&maps.ru, S, a.ref_u, a.cw, a.ch, a.n, a.pitch_uv, a.stride_uv, TW / 2, TH / 2);
+        ok = ok && encode(&maps.du, S, a.dist_u, a.cw, a.ch, a.n, a.pitch_uv, a.stride_uv, TW / 2, TH / 2);
+        ok = ok && encode(&maps.rv, S, a.ref_v, a.cw, a.ch, a.n, a.pitch_uv, a.stride_uv, TW / 2, TH / 2);
+        ok = ok && encode(&maps.dv, S, a.dist_v, a.cw, a.ch, a.n, a.pitch_uv, a.stride_uv, TW / 2, TH / 2);
+    }
+    if (!ok) return cudaSuccess;  // the caller falls back to the generic kernel
+    *used = true;
+    *launches += 1;
+    if (S == 1)
+        return fused ? launch_tma_one<uint8_t, true, 4>(maps, a, s)
+                     : launch_tma_one<uint8_t, false, 4>(maps, a, s);
+    return fused ? launch_tma_one<uint16_t, true, 3>(maps, a, s)
+                 : launch_tma_one<uint16_t, false, 4>(maps, a, s);
+}
+
+}  // namespace mg

@@ -23,16 +23,31 @@ def iif():
     return m
 
 
-def run_batches(iif, frames, bpc, batch):
+def padded_dev(frames, align_bytes=16):
+    """Device copy whose row pitch is rounded up to align_bytes (a view of the
+    first w samples of each row), so that 16-byte-aligned layouts reach the
+    TMA kernel whatever the width."""
+    n, h, w = frames.shape
+    s = frames.itemsize
+    wp = ((w * s + align_bytes - 1) // align_bytes * align_bytes) // s
+    big = np.zeros((n, h, wp), dtype=frames.dtype)
+    big[:, :, :w] = frames
+    return to_dev(big)[:, :, :w]
+
+
+def run_batches(iif, frames, bpc, batch, path=None, padded=False):
     import torch
     n, h, w = frames.shape
-    d = to_dev(frames)
+    d = padded_dev(frames) if padded else to_dev(frames)
     out = dev_zeros(n)
     with iif.MotionContext(w, h, bpc) as ctx:
+        if path is not None:
+            ctx.set_kernel_path(path)
         for s in range(0, n, batch):
             e = min(n, s + batch)
             ctx.submit_batch(d[s:e], out[s:e])
         torch.cuda.synchronize()
+        assert ctx.device_error() == 0
     return to_u64(out)
 
 
@@ -72,6 +87,8 @@ def test_seq_1920x1080_cuts_batch16(iif, oracle):
     frames = synth.make("seq_1920x1080_u8_cuts")
     want = oracle_sad(oracle, frames, 8)
     assert np.array_equal(run_batches(iif, frames, 8, 16), want)
+    assert np.array_equal(run_batches(iif, frames[:40], 8, 16, path=iif.MOTION_PATH_GENERIC),
+                          want[:40])
 
 
 def test_yuv420_4k_fused_full(iif, oracle):
@@ -136,6 +153,38 @@ def test_tiny_and_ragged_frames(iif, oracle, bpc):
         want = oracle.motion_sad_sequence(frames, bpc)
         got = run_batches(iif, frames, bpc, 3)
         assert np.array_equal(got, want), (w, h, bpc)
+
+
+@pytest.mark.parametrize("bpc", [8, 10, 16])
+def test_tma_and_generic_paths_on_aligned_layouts(iif, oracle, bpc):
+    """16-byte-aligned pitches: the TMA kernel (mirror halo written in shared
+    memory on border tiles) and the generic kernel both equal the oracle."""
+    rng = np.random.default_rng(100 + bpc)
+    for (w, h) in SIZES:
+        frames = synth.uniform_frames(int(rng.integers(1 << 30)), 4, w, h, bpc)
+        want = oracle.motion_sad_sequence(frames, bpc)
+        for path in (iif.MOTION_PATH_AUTO, iif.MOTION_PATH_GENERIC):
+            got = run_batches(iif, frames, bpc, 3, path=path, padded=True)
+            assert np.array_equal(got, want), (w, h, bpc, path)
+
+
+@pytest.mark.parametrize("bpc", [8, 10])
+def test_fused_paths_on_aligned_layouts(iif, oracle, bpc):
+    import torch
+    for (w, h) in ((3, 3), (64, 48), (130, 66), (257, 131), (300, 97)):
+        b = synth.yuv420_pairs(w * 3 + h, 5, w, h, bpc=bpc)
+        want_sad = oracle.motion_sad_sequence(b.ref_y, bpc)
+        want_sse = oracle_sse420(oracle, b)
+        planes = [padded_dev(p) for p in b.planes()]
+        for path in (iif.MOTION_PATH_AUTO, iif.MOTION_PATH_GENERIC):
+            sad, sse = dev_zeros(5), dev_zeros((5, 3))
+            with iif.MotionContext(w, h, bpc) as ctx:
+                ctx.set_kernel_path(path)
+                ctx.yuv420_batch(*planes, sad, sse)
+                torch.cuda.synchronize()
+                assert ctx.device_error() == 0
+            assert np.array_equal(to_u64(sad), want_sad), (w, h, path)
+            assert np.array_equal(to_u64(sse), want_sse), (w, h, path)
 
 
 @pytest.mark.parametrize("bpc", [8, 10])
