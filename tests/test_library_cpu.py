@@ -121,13 +121,19 @@ def contract_violations(src: str) -> list:
     bad = []
     if "multicast::cluster" in src:
         bad.append("cluster multicast")
-    for m in re.finditer(r"atomicAdd\(([^;]*)\);", src):
-        # the guard sits on the atomic's line or on the line before it
-        line_start = src.rfind("\n", 0, m.start())
-        line_start = src.rfind("\n", 0, max(line_start, 0)) + 1
-        line = src[line_start:m.start()]
-        if not re.search(r"if \((lane|threadIdx\.x) == \d", line):
-            bad.append("atomic not guarded by a single lane: " + line.strip())
+    for m in re.finditer(r"\batomicAdd\(([^;]*)\);", src):
+        # a single-lane guard (lane / tid / threadIdx.x == k) within the 16
+        # lines before the global atomic
+        start = m.start()
+        for _ in range(16):
+            start = src.rfind("\n", 0, max(start - 1, 0))
+            if start <= 0:
+                start = 0
+                break
+        window = src[start:m.start()]
+        if not re.search(r"if \((lane|tid|threadIdx\.x) == \d", window):
+            line_start = src.rfind("\n", 0, m.start()) + 1
+            bad.append("atomic not guarded by a single lane: " + src[line_start:m.end()].strip())
     if re.search(r"\ba\.\w+\[[^\]]*(threadIdx|blockIdx|plane|lane)", src):
         bad.append("runtime index into a kernel-parameter array")
     return bad
