@@ -114,6 +114,36 @@ def _kernel_sources():
             if f.endswith((".cu", ".cuh"))}
 
 
+_GUARD = re.compile(r"if \((lane|tid|threadIdx\.x) == \d")
+
+
+def _single_lane_guarded(src: str, pos: int) -> bool:
+    """True when the statement at pos, or one of the blocks enclosing it, is
+    under an `if (lane|tid|threadIdx.x == k ...)` condition."""
+    line_start = src.rfind("\n", 0, pos) + 1
+    if _GUARD.search(src[line_start:pos]):
+        return True
+    prev_start = src.rfind("\n", 0, max(line_start - 1, 0)) + 1
+    prev = src[prev_start:line_start].strip()
+    if _GUARD.search(prev) and not prev.endswith((";", "{", "}")):
+        return True          # `if (...)` on the line before, without braces
+    depth = 0
+    i = pos
+    while i > 0:
+        i -= 1
+        c = src[i]
+        if c == "}":
+            depth += 1
+        elif c == "{":
+            if depth == 0:
+                header_start = src.rfind("\n", 0, i) + 1
+                if _GUARD.search(src[header_start:i]):
+                    return True
+            else:
+                depth -= 1
+    return False
+
+
 def contract_violations(src: str) -> list:
     """Checks in the spirit of a kernel source contract: no cluster multicast,
     every atomic is a 64-bit add issued once per block per accumulator (inside
@@ -122,16 +152,7 @@ def contract_violations(src: str) -> list:
     if "multicast::cluster" in src:
         bad.append("cluster multicast")
     for m in re.finditer(r"\batomicAdd\(([^;]*)\);", src):
-        # a single-lane guard (lane / tid / threadIdx.x == k) within the 16
-        # lines before the global atomic
-        start = m.start()
-        for _ in range(16):
-            start = src.rfind("\n", 0, max(start - 1, 0))
-            if start <= 0:
-                start = 0
-                break
-        window = src[start:m.start()]
-        if not re.search(r"if \((lane|tid|threadIdx\.x) == \d", window):
+        if not _single_lane_guarded(src, m.start()):
             line_start = src.rfind("\n", 0, m.start()) + 1
             bad.append("atomic not guarded by a single lane: " + src[line_start:m.end()].strip())
     if re.search(r"\ba\.\w+\[[^\]]*(threadIdx|blockIdx|plane|lane)", src):
