@@ -26,6 +26,8 @@
 //    error word and leaves instead of spinning.
 #include <cuda.h>
 
+#include <type_traits>
+
 #include "motion_internal.h"
 #include "tile_geometry.cuh"
 
@@ -119,8 +121,8 @@ __device__ __forceinline__ void vertical_quad(const uint16_t* src, uint32_t* dst
 }
 
 template <typename Pix, bool FUSED, int STAGES>
-__global__ void __launch_bounds__(NT) motion_tma_kernel(const __grid_constant__ TmaMaps maps,
-                                                         const TileArgs a) {
+__global__ void __launch_bounds__(NT, 3) motion_tma_kernel(const __grid_constant__ TmaMaps maps,
+                                                            const TileArgs a) {
     using G = Geo<Pix>;
     using Acc = typename SseAcc<Pix>::T;
     constexpr int STAGE = FUSED ? G::STAGE_FUSED : G::STAGE_MOTION;
@@ -131,8 +133,8 @@ __global__ void __launch_bounds__(NT) motion_tma_kernel(const __grid_constant__ 
     unsigned char* smem = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);
     __shared__ __align__(8) uint64_t full[STAGES];   // TMA bytes landed
     __shared__ __align__(8) uint64_t empty[STAGES];  // every warp done with the stage
-    __shared__ unsigned long long acc_s[SLOTS][4];   // per-frame block sums
-    __shared__ unsigned cnt_s[SLOTS];                // warps that added to a slot
+    __shared__ unsigned long long part[SLOTS][NW][4];  // per-warp partial sums of a frame
+    __shared__ unsigned cnt_s[SLOTS];                  // warps that stored a partial
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     // each warp owns output rows 4w .. 4w+3 of the tile; its V rows are private
@@ -161,7 +163,6 @@ __global__ void __launch_bounds__(NT) motion_tma_kernel(const __grid_constant__ 
             prefetch_tmap(&maps.dv);
         }
     }
-    if (tid < SLOTS * 4) acc_s[tid >> 2][tid & 3] = 0;
     if (tid < SLOTS) cnt_s[tid] = 0;
     __syncthreads();
 
@@ -204,9 +205,17 @@ __global__ void __launch_bounds__(NT) motion_tma_kernel(const __grid_constant__ 
         int nv = (y0 + 4 * warp + k < a.h) ? a.w - (x0 + 4 * q) : 0;
         nvalid[k] = nv < 0 ? 0 : (nv > 4 ? 4 : nv);
     }
+    // per-thread offsets inside a stage (identical for every stage)
+    const int off_vsrc = ((warp * 4) * G::RAW_W + G::HX + 4 * lane) * G::S;
+    const int halo_r = (lane >> 2) & 3, halo_which = lane & 3;
+    const int halo_off = halo_which == 0 ? -2 : halo_which == 1 ? -1 : halo_which == 2 ? TW : TW + 1;
+    const int off_halo = ((warp * 4 + halo_r) * G::RAW_W + G::HX + halo_off) * G::S;
+    const int off_coff = ((2 * warp + (lane >> 4)) * G::CW + 4 * (lane & 15)) * G::S;
+    bool alive = true;
 
-    for (int f = 0; f < a.n; ++f) {
-        const int s = f % STAGES;
+    // one frame; S_ is the stage index as a compile-time constant
+    auto step = [&](auto S_, int f) {
+        constexpr int s = decltype(S_)::value;
         const unsigned parity = (unsigned)(f / STAGES) & 1u;
         const bool ok = mbar_wait_bounded(&full[s], parity, kWaitCycles);
         unsigned char* st = smem + s * STAGE;
@@ -216,34 +225,32 @@ __global__ void __launch_bounds__(NT) motion_tma_kernel(const __grid_constant__ 
             if (!__syncthreads_and(ok)) {
                 if (tid == 0 && a.err) atomicOr(a.err, 1);
                 mbar_wait_bounded(&full[s], parity, kWaitCycles);
+                alive = false;
                 return;
             }
             patch_mirror<Pix>(raw, a, x0, y0, pl, pr, pt, pb);
         } else if (!__all_sync(0xffffffffu, ok)) {
             if (lane == 0 && a.err) atomicOr(a.err, 1);
             mbar_wait_bounded(&full[s], parity, kWaitCycles);
+            alive = false;
             return;
         }
 
         // ---- vertical pass of the warp's 4 rows (staged row r <-> y0 - 2 + r)
-        vertical_quad(raw + (warp * 4) * G::RAW_W + G::HX + 4 * lane, sV + 4 + 4 * lane, rnd, sh);
+        vertical_quad(reinterpret_cast<const Pix*>(st + off_vsrc), sV + 4 + 4 * lane, rnd, sh);
         if (lane < 16) {  // the two halo columns on each side, 4 rows
-            const int r = lane >> 2, which = lane & 3;
-            const int off = which == 0 ? -2 : which == 1 ? -1 : which == 2 ? TW : TW + 1;
-            const Pix* c = raw + (warp * 4 + r) * G::RAW_W + G::HX + off;
-            sV[r * SVW + 4 + off] = vtap(c[0], c[G::RAW_W], c[2 * G::RAW_W], c[3 * G::RAW_W],
-                                         c[4 * G::RAW_W], rnd, sh);
+            const Pix* c = reinterpret_cast<const Pix*>(st + off_halo);
+            sV[halo_r * SVW + 4 + halo_off] = vtap(c[0], c[G::RAW_W], c[2 * G::RAW_W],
+                                                   c[3 * G::RAW_W], c[4 * G::RAW_W], rnd, sh);
         }
         __syncwarp();
 
         // ---- horizontal pass, SAD against B_prev, squared errors
         const bool do_sad = (f > 0) || a.has_prev;
         uint32_t sad = 0;
-        Acc sse_y = 0, sse_u = 0, sse_v = 0;
-        const Pix* dist = reinterpret_cast<const Pix*>(st + G::RAW_BYTES);
+        [[maybe_unused]] Acc sse_y = 0, sse_u = 0, sse_v = 0;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-            const int r = 4 * warp + k;
             const uint32_t* v = sV + k * SVW + 4 * q;
             const uint4 A = *reinterpret_cast<const uint4*>(v);
             const uint4 Bq = *reinterpret_cast<const uint4*>(v + 4);
@@ -264,18 +271,18 @@ __global__ void __launch_bounds__(NT) motion_tma_kernel(const __grid_constant__ 
 #pragma unroll
             for (int i = 0; i < 4; ++i) bp[k][i] = b[i];
             if constexpr (FUSED) {
-                const Pix* rp = raw + (r + 2) * G::RAW_W + G::HX + 4 * q;
-                const Pix* dp = dist + r * TW + 4 * q;
+                const int roff = ((4 * warp + k + 2) * G::RAW_W + G::HX + 4 * q) * G::S;
+                const int doff = G::RAW_BYTES + ((4 * warp + k) * TW + 4 * q) * G::S;
                 if constexpr (sizeof(Pix) == 1) {
-                    uint32_t d = __vabsdiffu4(*reinterpret_cast<const uint32_t*>(rp),
-                                              *reinterpret_cast<const uint32_t*>(dp));
+                    uint32_t d = __vabsdiffu4(*reinterpret_cast<const uint32_t*>(st + roff),
+                                              *reinterpret_cast<const uint32_t*>(st + doff));
                     if (!full_tile)
                         d &= nvalid[k] <= 0 ? 0u : (0xffffffffu >> (8 * (4 - nvalid[k])));
                     sse_y = __dp4a(d, d, sse_y);
                 } else {
                     uint32_t rf[4], ds[4];
-                    unpack4(rp, rf);
-                    unpack4(dp, ds);
+                    unpack4(reinterpret_cast<const Pix*>(st + roff), rf);
+                    unpack4(reinterpret_cast<const Pix*>(st + doff), ds);
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
                         const long long e = (long long)rf[i] - (long long)ds[i];
@@ -288,22 +295,20 @@ __global__ void __launch_bounds__(NT) motion_tma_kernel(const __grid_constant__ 
             // 4:2:0 chroma: 16 rows x 64 columns per plane; warp w takes rows
             // 2w, 2w+1, 4 samples per lane; outside the picture both sides were
             // zero-filled, so they add 0
-            const Pix* sc = reinterpret_cast<const Pix*>(st + G::RAW_BYTES + G::DIST_BYTES);
-            constexpr int CE = G::CH * G::CW;
-            const int off = (2 * warp + (lane >> 4)) * G::CW + 4 * (lane & 15);
+            const unsigned char* sc = st + G::RAW_BYTES + G::DIST_BYTES + off_coff;
             if constexpr (sizeof(Pix) == 1) {
-                const uint32_t du = __vabsdiffu4(*reinterpret_cast<const uint32_t*>(sc + off),
-                                                 *reinterpret_cast<const uint32_t*>(sc + CE + off));
-                const uint32_t dv = __vabsdiffu4(*reinterpret_cast<const uint32_t*>(sc + 2 * CE + off),
-                                                 *reinterpret_cast<const uint32_t*>(sc + 3 * CE + off));
+                const uint32_t du = __vabsdiffu4(*reinterpret_cast<const uint32_t*>(sc),
+                                                 *reinterpret_cast<const uint32_t*>(sc + G::C_BYTES));
+                const uint32_t dv = __vabsdiffu4(*reinterpret_cast<const uint32_t*>(sc + 2 * G::C_BYTES),
+                                                 *reinterpret_cast<const uint32_t*>(sc + 3 * G::C_BYTES));
                 sse_u = __dp4a(du, du, 0u);
                 sse_v = __dp4a(dv, dv, 0u);
             } else {
                 uint32_t ru[4], du[4], rv[4], dv[4];
-                unpack4(sc + off, ru);
-                unpack4(sc + CE + off, du);
-                unpack4(sc + 2 * CE + off, rv);
-                unpack4(sc + 3 * CE + off, dv);
+                unpack4(reinterpret_cast<const Pix*>(sc), ru);
+                unpack4(reinterpret_cast<const Pix*>(sc + G::C_BYTES), du);
+                unpack4(reinterpret_cast<const Pix*>(sc + 2 * G::C_BYTES), rv);
+                unpack4(reinterpret_cast<const Pix*>(sc + 3 * G::C_BYTES), dv);
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const long long eu = (long long)ru[i] - (long long)du[i];
@@ -317,10 +322,11 @@ __global__ void __launch_bounds__(NT) motion_tma_kernel(const __grid_constant__ 
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
 
-        // ---- one atomic per block per accumulator: warps add into a shared
-        // slot; the last warp to finish the frame adds the slot to the output
+        // ---- one atomic per block per accumulator: each warp stores its
+        // partials in the frame's slot; the last warp to arrive sums the slot
+        // and adds it to the outputs
         if (do_sad || FUSED) {
-            const uint32_t wsad = __reduce_add_sync(0xffffffffu, sad);
+            const unsigned long long wsad = __reduce_add_sync(0xffffffffu, sad);
             unsigned long long wy = 0, wu = 0, wvv = 0;
             if constexpr (FUSED) {
                 if constexpr (sizeof(Pix) == 1) {
@@ -335,23 +341,30 @@ __global__ void __launch_bounds__(NT) motion_tma_kernel(const __grid_constant__ 
             }
             if (lane == 0) {
                 const int slot = f & (SLOTS - 1);
-                atomicAdd_block(&acc_s[slot][0], (unsigned long long)wsad);
-                if constexpr (FUSED) {
-                    atomicAdd_block(&acc_s[slot][1], wy);
-                    atomicAdd_block(&acc_s[slot][2], wu);
-                    atomicAdd_block(&acc_s[slot][3], wvv);
-                }
+                part[slot][warp][0] = wsad;
+                part[slot][warp][1] = wy;
+                part[slot][warp][2] = wu;
+                part[slot][warp][3] = wvv;
                 __threadfence_block();
                 if (atomicAdd_block(&cnt_s[slot], 1u) == NW - 1) {
                     __threadfence_block();
-                    const unsigned long long t0 = atomicExch_block(&acc_s[slot][0], 0ull);
-                    if (do_sad) atomicAdd(a.sad_out + f, t0);
-                    if constexpr (FUSED) {
-                        atomicAdd(a.sse_out + 3LL * f + 0, atomicExch_block(&acc_s[slot][1], 0ull));
-                        atomicAdd(a.sse_out + 3LL * f + 1, atomicExch_block(&acc_s[slot][2], 0ull));
-                        atomicAdd(a.sse_out + 3LL * f + 2, atomicExch_block(&acc_s[slot][3], 0ull));
+                    unsigned long long t[4] = {0, 0, 0, 0};
+#pragma unroll
+                    for (int w = 0; w < NW; ++w) {
+                        t[0] += part[slot][w][0];
+                        if constexpr (FUSED) {
+                            t[1] += part[slot][w][1];
+                            t[2] += part[slot][w][2];
+                            t[3] += part[slot][w][3];
+                        }
                     }
                     cnt_s[slot] = 0;
+                    if (do_sad) atomicAdd(a.sad_out + f, t[0]);
+                    if constexpr (FUSED) {
+                        atomicAdd(a.sse_out + 3LL * f + 0, t[1]);
+                        atomicAdd(a.sse_out + 3LL * f + 1, t[2]);
+                        atomicAdd(a.sse_out + 3LL * f + 2, t[3]);
+                    }
                 }
             }
         }
@@ -366,7 +379,17 @@ __global__ void __launch_bounds__(NT) motion_tma_kernel(const __grid_constant__ 
                 issue(f + STAGES - 1);
             }
         }
+    };
+
+    // frames in groups of STAGES so that every stage index is a constant
+    for (int f = 0; f < a.n && alive; f += STAGES) {
+        step(std::integral_constant<int, 0>{}, f);
+        if constexpr (STAGES > 1) if (alive && f + 1 < a.n) step(std::integral_constant<int, 1>{}, f + 1);
+        if constexpr (STAGES > 2) if (alive && f + 2 < a.n) step(std::integral_constant<int, 2>{}, f + 2);
+        if constexpr (STAGES > 3) if (alive && f + 3 < a.n) step(std::integral_constant<int, 3>{}, f + 3);
+        static_assert(STAGES <= 4, "unrolled for up to 4 stages");
     }
+    if (!alive) return;
 
     if (a.store_last && a.n > 0) {
 #pragma unroll
