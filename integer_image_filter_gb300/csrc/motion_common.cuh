@@ -86,15 +86,15 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, unsigned by
         : "memory");
 }
 
-// try_wait with a suspend-time hint: the warp sleeps in hardware until the
-// phase completes or about 0.1 ms pass, instead of polling.
+// One potentially blocking test of an mbarrier phase (the hardware holds the
+// warp for a short, implementation-defined time before reporting "not yet").
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, unsigned parity) {
     unsigned ok;
     asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
         " selp.u32 %0, 1, 0, p;\n}\n"
         : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity), "r"(100000u)
+        : "r"(smem_u32(bar)), "r"(parity)
         : "memory");
     return ok != 0;
 }

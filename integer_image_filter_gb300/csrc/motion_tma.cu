@@ -75,15 +75,18 @@ __device__ __forceinline__ void patch_mirror(Pix* raw, const TileArgs& a, int x0
 
 // The vertical 5-tap pass for one warp: 4 output rows (staged rows 4w..4w+7
 // feed them) x 128 columns, lane = quad of 4 columns; result V (uint32) into
-// the warp's own rows of sV.  8-bit samples use byte-pair dot products: the
-// rows are interleaved two at a time so that one dp2a applies two taps to two
-// rows of one column (exact: sums stay below 2^24).
+// the warp's own rows of sV, and the 4 centre-row words (the reference luma
+// of the warp's output rows) for the squared error.  8-bit samples use
+// byte-pair dot products: rows are interleaved two at a time so that one dp2a
+// applies two taps to two rows of one column (exact: sums stay below 2^24).
 __device__ __forceinline__ void vertical_quad(const uint8_t* src, uint32_t* dst, uint32_t rnd,
-                                              int sh) {
+                                              int sh, uint32_t (&center)[4]) {
     constexpr int RW = Geo<uint8_t>::RAW_W;
     uint32_t wv[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) wv[i] = *reinterpret_cast<const uint32_t*>(src + i * RW);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) center[i] = wv[i + 2];
     uint32_t lo[7], hi[7];  // rows (i, i+1): columns 0,1 in lo, columns 2,3 in hi
 #pragma unroll
     for (int i = 0; i < 7; ++i) {
@@ -104,11 +107,13 @@ __device__ __forceinline__ void vertical_quad(const uint8_t* src, uint32_t* dst,
     }
 }
 __device__ __forceinline__ void vertical_quad(const uint16_t* src, uint32_t* dst, uint32_t rnd,
-                                              int sh) {
+                                              int sh, uint32_t (&center)[4]) {
     constexpr int RW = Geo<uint16_t>::RAW_W;
     uint32_t p[8][4];
 #pragma unroll
     for (int i = 0; i < 8; ++i) unpack4(src + i * RW, p[i]);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) center[i] = 0;  // 16-bit SSE reloads its samples
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
         uint4 o;
@@ -120,21 +125,40 @@ __device__ __forceinline__ void vertical_quad(const uint16_t* src, uint32_t* dst
     }
 }
 
+// The horizontal 5-tap pass of 4 outputs from V at columns -2 .. +9 around
+// the quad: t0 W5 + (t1 - t0) W3 + (t2 - t1) c with the 5- and 3-wide window
+// sums slid one column at a time (the same integers as the tap-by-tap sum,
+// kept exact in uint32; three-input adds leave the multiplier pipe to the
+// three products).
+__device__ __forceinline__ void horizontal_quad(const uint32_t (&wv)[12], uint32_t (&b)[4]) {
+    uint32_t w3 = wv[3] + wv[4] + wv[5];
+    uint32_t w5 = w3 + wv[2] + wv[6];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        if (i > 0) {
+            w3 = w3 + wv[5 + i] - wv[2 + i];
+            w5 = w5 + wv[6 + i] - wv[1 + i];
+        }
+        b[i] = (kT0 * w5 + (kT1 - kT0) * w3 + (kT2 - kT1) * wv[4 + i] + 32768u) >> 16;
+    }
+}
+
 template <typename Pix, bool FUSED, int STAGES>
 __global__ void __launch_bounds__(NT, 3) motion_tma_kernel(const __grid_constant__ TmaMaps maps,
                                                             const TileArgs a) {
     using G = Geo<Pix>;
     using Acc = typename SseAcc<Pix>::T;
     constexpr int STAGE = FUSED ? G::STAGE_FUSED : G::STAGE_MOTION;
-    constexpr int SLOTS = 8;  // reduction slots; a warp runs at most STAGES frames ahead
-    static_assert(SLOTS > STAGES, "reduction slots must outnumber the stages");
+    constexpr int FLUSH = 8;           // frames between block reductions
+    constexpr int SLOTS = 2 * FLUSH;   // partial-sum slots (two flush windows)
     extern __shared__ __align__(128) unsigned char smem_raw[];
     // TMA destinations must sit on 128-byte boundaries; the launch adds 128 B of slack
     unsigned char* smem = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);
     __shared__ __align__(8) uint64_t full[STAGES];   // TMA bytes landed
     __shared__ __align__(8) uint64_t empty[STAGES];  // every warp done with the stage
-    __shared__ unsigned long long part[SLOTS][NW][4];  // per-warp partial sums of a frame
-    __shared__ unsigned cnt_s[SLOTS];                  // warps that stored a partial
+    // warp sums per frame (32-bit suffice for 8-bit samples: at most 512 x 255^2)
+    using Part = typename std::conditional<sizeof(Pix) == 1, uint32_t, unsigned long long>::type;
+    __shared__ __align__(16) Part part[SLOTS][NW][4];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     // each warp owns output rows 4w .. 4w+3 of the tile; its V rows are private
@@ -163,7 +187,6 @@ __global__ void __launch_bounds__(NT, 3) motion_tma_kernel(const __grid_constant
             prefetch_tmap(&maps.dv);
         }
     }
-    if (tid < SLOTS) cnt_s[tid] = 0;
     __syncthreads();
 
     auto issue = [&](int f) {  // thread 0 only
@@ -205,39 +228,45 @@ __global__ void __launch_bounds__(NT, 3) motion_tma_kernel(const __grid_constant
         int nv = (y0 + 4 * warp + k < a.h) ? a.w - (x0 + 4 * q) : 0;
         nvalid[k] = nv < 0 ? 0 : (nv > 4 ? 4 : nv);
     }
-    // per-thread offsets inside a stage (identical for every stage)
+    // per-thread byte offsets inside a stage (the same for every stage)
     const int off_vsrc = ((warp * 4) * G::RAW_W + G::HX + 4 * lane) * G::S;
     const int halo_r = (lane >> 2) & 3, halo_which = lane & 3;
     const int halo_off = halo_which == 0 ? -2 : halo_which == 1 ? -1 : halo_which == 2 ? TW : TW + 1;
     const int off_halo = ((warp * 4 + halo_r) * G::RAW_W + G::HX + halo_off) * G::S;
-    const int off_coff = ((2 * warp + (lane >> 4)) * G::CW + 4 * (lane & 15)) * G::S;
-    bool alive = true;
+    const int off_ref = ((4 * warp + 2) * G::RAW_W + G::HX + 4 * q) * G::S;   // row k: + k RAW_W S
+    const int off_dist = G::RAW_BYTES + ((4 * warp) * TW + 4 * q) * G::S;     // row k: + k TW S
+    const int off_chroma = G::RAW_BYTES + G::DIST_BYTES +
+                           ((2 * warp + (lane >> 4)) * G::CW + 4 * (lane & 15)) * G::S;
+    bool timed_out = false;
 
-    // one frame; S_ is the stage index as a compile-time constant
-    auto step = [&](auto S_, int f) {
-        constexpr int s = decltype(S_)::value;
+    for (int f = 0; f < a.n; ++f) {
+        const int s = f % STAGES;
         const unsigned parity = (unsigned)(f / STAGES) & 1u;
         const bool ok = mbar_wait_bounded(&full[s], parity, kWaitCycles);
+        timed_out |= !ok;
         unsigned char* st = smem + s * STAGE;
-        Pix* raw = reinterpret_cast<Pix*>(st);
+        // the stage of frame f-1 takes frame f+STAGES-1 as soon as every warp
+        // has released it
+        if (tid == 0 && f >= 1 && f + STAGES - 1 < a.n) {
+            const int sp = (f - 1) % STAGES;
+            if (mbar_wait_bounded(&empty[sp], (unsigned)((f - 1) / STAGES) & 1u, kWaitCycles))
+                issue(f + STAGES - 1);
+            else
+                timed_out = true;
+        }
         if (edge) {
-            // border tiles patch the mirrored halo together (block barriers)
+            // border tiles write the mirrored halo together (block barriers)
             if (!__syncthreads_and(ok)) {
                 if (tid == 0 && a.err) atomicOr(a.err, 1);
                 mbar_wait_bounded(&full[s], parity, kWaitCycles);
-                alive = false;
                 return;
             }
-            patch_mirror<Pix>(raw, a, x0, y0, pl, pr, pt, pb);
-        } else if (!__all_sync(0xffffffffu, ok)) {
-            if (lane == 0 && a.err) atomicOr(a.err, 1);
-            mbar_wait_bounded(&full[s], parity, kWaitCycles);
-            alive = false;
-            return;
+            patch_mirror<Pix>(reinterpret_cast<Pix*>(st), a, x0, y0, pl, pr, pt, pb);
         }
 
         // ---- vertical pass of the warp's 4 rows (staged row r <-> y0 - 2 + r)
-        vertical_quad(reinterpret_cast<const Pix*>(st + off_vsrc), sV + 4 + 4 * lane, rnd, sh);
+        uint32_t center[4];
+        vertical_quad(reinterpret_cast<const Pix*>(st + off_vsrc), sV + 4 + 4 * lane, rnd, sh, center);
         if (lane < 16) {  // the two halo columns on each side, 4 rows
             const Pix* c = reinterpret_cast<const Pix*>(st + off_halo);
             sV[halo_r * SVW + 4 + halo_off] = vtap(c[0], c[G::RAW_W], c[2 * G::RAW_W],
@@ -257,32 +286,28 @@ __global__ void __launch_bounds__(NT, 3) motion_tma_kernel(const __grid_constant
             const uint4 C = *reinterpret_cast<const uint4*>(v + 8);
             const uint32_t wv[12] = {A.x, A.y, A.z, A.w, Bq.x, Bq.y, Bq.z, Bq.w, C.x, C.y, C.z, C.w};
             uint32_t b[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-                b[i] = (kT0 * (wv[2 + i] + wv[6 + i]) + kT1 * (wv[3 + i] + wv[5 + i]) +
-                        kT2 * wv[4 + i] + 32768u) >> 16;
+            horizontal_quad(wv, b);
             if (full_tile) {
 #pragma unroll
                 for (int i = 0; i < 4; ++i) sad = __sad(b[i], bp[k][i], sad);
             } else {
+                // an invalid sample compares with itself and adds 0
 #pragma unroll
                 for (int i = 0; i < 4; ++i) sad = __sad(b[i], i < nvalid[k] ? bp[k][i] : b[i], sad);
             }
 #pragma unroll
             for (int i = 0; i < 4; ++i) bp[k][i] = b[i];
             if constexpr (FUSED) {
-                const int roff = ((4 * warp + k + 2) * G::RAW_W + G::HX + 4 * q) * G::S;
-                const int doff = G::RAW_BYTES + ((4 * warp + k) * TW + 4 * q) * G::S;
+                const Pix* dp = reinterpret_cast<const Pix*>(st + off_dist + k * TW * G::S);
                 if constexpr (sizeof(Pix) == 1) {
-                    uint32_t d = __vabsdiffu4(*reinterpret_cast<const uint32_t*>(st + roff),
-                                              *reinterpret_cast<const uint32_t*>(st + doff));
+                    uint32_t d = __vabsdiffu4(center[k], *reinterpret_cast<const uint32_t*>(dp));
                     if (!full_tile)
                         d &= nvalid[k] <= 0 ? 0u : (0xffffffffu >> (8 * (4 - nvalid[k])));
                     sse_y = __dp4a(d, d, sse_y);
                 } else {
                     uint32_t rf[4], ds[4];
-                    unpack4(reinterpret_cast<const Pix*>(st + roff), rf);
-                    unpack4(reinterpret_cast<const Pix*>(st + doff), ds);
+                    unpack4(reinterpret_cast<const Pix*>(st + off_ref + k * G::RAW_W * G::S), rf);
+                    unpack4(dp, ds);
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
                         const long long e = (long long)rf[i] - (long long)ds[i];
@@ -295,7 +320,7 @@ __global__ void __launch_bounds__(NT, 3) motion_tma_kernel(const __grid_constant
             // 4:2:0 chroma: 16 rows x 64 columns per plane; warp w takes rows
             // 2w, 2w+1, 4 samples per lane; outside the picture both sides were
             // zero-filled, so they add 0
-            const unsigned char* sc = st + G::RAW_BYTES + G::DIST_BYTES + off_coff;
+            const unsigned char* sc = st + off_chroma;
             if constexpr (sizeof(Pix) == 1) {
                 const uint32_t du = __vabsdiffu4(*reinterpret_cast<const uint32_t*>(sc),
                                                  *reinterpret_cast<const uint32_t*>(sc + G::C_BYTES));
@@ -322,10 +347,10 @@ __global__ void __launch_bounds__(NT, 3) motion_tma_kernel(const __grid_constant
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
 
-        // ---- one atomic per block per accumulator: each warp stores its
-        // partials in the frame's slot; the last warp to arrive sums the slot
-        // and adds it to the outputs
-        if (do_sad || FUSED) {
+        // ---- warp sums of this frame into its slot; every FLUSH frames the
+        // block adds the slots to the outputs, one atomic per accumulator and
+        // frame (warp 0, lane = frame x accumulator)
+        {
             const unsigned long long wsad = __reduce_add_sync(0xffffffffu, sad);
             unsigned long long wy = 0, wu = 0, wvv = 0;
             if constexpr (FUSED) {
@@ -340,56 +365,31 @@ __global__ void __launch_bounds__(NT, 3) motion_tma_kernel(const __grid_constant
                 }
             }
             if (lane == 0) {
-                const int slot = f & (SLOTS - 1);
-                part[slot][warp][0] = wsad;
-                part[slot][warp][1] = wy;
-                part[slot][warp][2] = wu;
-                part[slot][warp][3] = wvv;
-                __threadfence_block();
-                if (atomicAdd_block(&cnt_s[slot], 1u) == NW - 1) {
-                    __threadfence_block();
-                    unsigned long long t[4] = {0, 0, 0, 0};
+                Part* pp = &part[f & (SLOTS - 1)][warp][0];
+                pp[0] = do_sad ? (Part)wsad : (Part)0;
+                pp[1] = (Part)wy;
+                pp[2] = (Part)wu;
+                pp[3] = (Part)wvv;
+            }
+        }
+        if ((f & (FLUSH - 1)) == FLUSH - 1 || f == a.n - 1) {
+            if (__syncthreads_or(timed_out)) {
+                // a stage wait ran out somewhere in the block: leave together
+                if (tid == 0 && a.err) atomicOr(a.err, 1);
+                mbar_wait_bounded(&full[s], parity, kWaitCycles);
+                return;
+            }
+            if (warp == 0) {
+                const int j = (f & ~(FLUSH - 1)) + (lane >> 2), acc = lane & 3;
+                if (j <= f && (acc != 0 || j > 0 || a.has_prev) && (FUSED || acc == 0)) {
+                    unsigned long long t = 0;
 #pragma unroll
-                    for (int w = 0; w < NW; ++w) {
-                        t[0] += part[slot][w][0];
-                        if constexpr (FUSED) {
-                            t[1] += part[slot][w][1];
-                            t[2] += part[slot][w][2];
-                            t[3] += part[slot][w][3];
-                        }
-                    }
-                    cnt_s[slot] = 0;
-                    if (do_sad) atomicAdd(a.sad_out + f, t[0]);
-                    if constexpr (FUSED) {
-                        atomicAdd(a.sse_out + 3LL * f + 0, t[1]);
-                        atomicAdd(a.sse_out + 3LL * f + 1, t[2]);
-                        atomicAdd(a.sse_out + 3LL * f + 2, t[3]);
-                    }
+                    for (int w = 0; w < NW; ++w) t += part[j & (SLOTS - 1)][w][acc];
+                    atomicAdd(acc == 0 ? a.sad_out + j : a.sse_out + 3LL * j + (acc - 1), t);
                 }
             }
         }
-
-        // ---- refill: the stage of frame f-1 takes frame f+STAGES-1 once every
-        // warp has released it
-        if (tid == 0 && f >= 1 && f + STAGES - 1 < a.n) {
-            const int sp = (f - 1) % STAGES;
-            if (!mbar_wait_bounded(&empty[sp], (unsigned)((f - 1) / STAGES) & 1u, kWaitCycles)) {
-                if (a.err) atomicOr(a.err, 2);
-            } else {
-                issue(f + STAGES - 1);
-            }
-        }
-    };
-
-    // frames in groups of STAGES so that every stage index is a constant
-    for (int f = 0; f < a.n && alive; f += STAGES) {
-        step(std::integral_constant<int, 0>{}, f);
-        if constexpr (STAGES > 1) if (alive && f + 1 < a.n) step(std::integral_constant<int, 1>{}, f + 1);
-        if constexpr (STAGES > 2) if (alive && f + 2 < a.n) step(std::integral_constant<int, 2>{}, f + 2);
-        if constexpr (STAGES > 3) if (alive && f + 3 < a.n) step(std::integral_constant<int, 3>{}, f + 3);
-        static_assert(STAGES <= 4, "unrolled for up to 4 stages");
     }
-    if (!alive) return;
 
     if (a.store_last && a.n > 0) {
 #pragma unroll

@@ -114,7 +114,8 @@ def _kernel_sources():
             if f.endswith((".cu", ".cuh"))}
 
 
-_GUARD = re.compile(r"if \((lane|tid|threadIdx\.x) == \d")
+# a single thread, or warp 0 whose lanes each own one (frame, accumulator)
+_GUARD = re.compile(r"if \((lane|tid|threadIdx\.x|warp) == \d")
 
 
 def _single_lane_guarded(src: str, pos: int) -> bool:
