@@ -187,6 +187,33 @@ MOTION_API int motion_set_kernel_path(motion_ctx* ctx, int path);
  * (its results are then incomplete).  *flags receives the word. */
 MOTION_API int motion_device_error(motion_ctx* ctx, int* flags);
 
+/* Largest frame of motion_submit_batch_noalloc: rows of round_up(w, 8)
+ * samples times h must not exceed this (3840x2160 and 4096x2048 fit). */
+#define MOTION_NOALLOC_MAX_SAMPLES (8u * 1024u * 1024u)
+
+/* Batched motion SAD that allocates nothing (no counterpart in the paper: it
+ * exists for callers that may not allocate device memory -- a host program
+ * that owns all device memory through its own pool and forbids libraries to
+ * call cudaMalloc, or a latency-critical loop where an allocation, which can
+ * synchronise the device, is not acceptable).  Same result as
+ * motion_submit_batch on a context of size w x h at bpc bits, without a
+ * context: the previous frame's blurred plane is kept in a fixed 16 MiB array
+ * built into the library (MOTION_NOALLOC_MAX_SAMPLES uint16 values; every GPU
+ * that loads the library holds it until the process exits).  continue_sequence
+ * = 0 starts a sequence (SAD_0 = 0); 1 compares frame 0 with the last frame of
+ * the previous call on this device, which must have had the same w, h and bpc
+ * (else MOTION_ERR_INVALID_ARGUMENT).  Frames larger than the array give
+ * MOTION_ERR_TOO_LARGE.  d_sad_out (device, n uint64) is zeroed on `stream`
+ * and filled asynchronously.  The first call on a device, with that device
+ * current, looks up the array's device address (no allocation); make that
+ * first call before any stream capture.  All calls on a device share the one
+ * array and keep the last call's contents: calls that overlap on the GPU race,
+ * so order them on one stream. */
+MOTION_API int motion_submit_batch_noalloc(const void* d_frames, int n, int w, int h, int bpc,
+                                           size_t frame_stride_bytes, size_t pitch_bytes,
+                                           int continue_sequence, void* stream,
+                                           uint64_t* d_sad_out);
+
 /* Number of this library's kernels launched by the calls above since load. */
 MOTION_API uint64_t motion_kernel_launch_count(void);
 

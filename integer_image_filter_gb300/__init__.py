@@ -26,6 +26,7 @@ __all__ = [
     "psnr_sse_yuv420_batch", "motion_scores_from_sad", "psnr_from_sse",
     "motion_kernel_launch_count", "motion_strerror", "MotionContext", "EXPORTED_SYMBOLS",
     "motion_set_kernel_path", "motion_device_error", "MOTION_PATH_AUTO", "MOTION_PATH_GENERIC",
+    "motion_submit_batch_noalloc",
 ]
 
 EXPORTED_SYMBOLS = (
@@ -33,7 +34,7 @@ EXPORTED_SYMBOLS = (
     "motion_psnr_yuv420_batch", "motion_psnr_yuv420_batch_host", "motion_reserve_host_staging",
     "psnr_sse", "psnr_sse_yuv420_batch", "motion_scores_from_sad", "psnr_from_sse",
     "motion_kernel_launch_count", "motion_strerror", "motion_last_cuda_error",
-    "motion_set_kernel_path", "motion_device_error",
+    "motion_set_kernel_path", "motion_device_error", "motion_submit_batch_noalloc",
 )
 
 _LIB: ctypes.CDLL | None = None
@@ -71,6 +72,7 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
         "motion_last_cuda_error": ([], I),
         "motion_set_kernel_path": ([P, I], I),
         "motion_device_error": ([P, ctypes.POINTER(I)], I),
+        "motion_submit_batch_noalloc": ([P, I, I, I, I, Z, Z, I, P, P], I),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -288,6 +290,26 @@ def psnr_from_sse(sse: int, n_samples: int, bpc: int):
     _check(load_library().psnr_from_sse(sse, n_samples, bpc, ctypes.byref(mse), ctypes.byref(db)),
            "psnr_from_sse")
     return float(mse.value), float(db.value)
+
+
+def motion_submit_batch_noalloc(frames, sad_out, w: int | None = None, h: int | None = None,
+                                bpc: int = 8, n: int | None = None,
+                                frame_stride: int | None = None, pitch_bytes: int | None = None,
+                                continue_sequence: bool = False, stream=None) -> None:
+    """Batched motion SAD without a context and without any allocation: the
+    previous frame's blurred plane lives in a fixed array inside the library
+    (for callers that may not allocate device memory)."""
+    if n is None:
+        n = int(frames.shape[0])
+    if h is None or w is None:
+        h, w = int(frames.shape[-2]), int(frames.shape[-1])
+    if pitch_bytes is None or frame_stride is None:
+        p, s = _layout(frames)
+        pitch_bytes = p if pitch_bytes is None else pitch_bytes
+        frame_stride = s if frame_stride is None else frame_stride
+    _check(load_library().motion_submit_batch_noalloc(
+        _addr(frames), n, w, h, bpc, frame_stride, pitch_bytes, 1 if continue_sequence else 0,
+        _stream(stream), _addr(sad_out)), "motion_submit_batch_noalloc")
 
 
 MOTION_PATH_AUTO = 0

@@ -58,6 +58,10 @@ int current_device(int* dev) {
 
 }  // namespace
 
+namespace mg {
+void note_launches(int n) { g_launches += (uint64_t)n; }
+}  // namespace mg
+
 struct motion_ctx {
     int device = -1;
     int w = 0, h = 0, bpc = 8, cw = 0, ch = 0;

@@ -62,4 +62,7 @@ cudaError_t launch_motion_tma(const TileArgs& a, bool fused, cudaStream_t s, int
                               bool* used);
 cudaError_t launch_sse(const SseArgs& a, cudaStream_t s, int sm_count, int* launches);
 
+// Adds to the library-wide kernel launch count (motion_kernel_launch_count).
+void note_launches(int n);
+
 }  // namespace mg

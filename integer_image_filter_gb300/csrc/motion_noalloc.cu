@@ -1,0 +1,124 @@
+// motion_noalloc.cu -- the allocation-free form of the batched motion submit.
+//
+// Some callers cannot allocate device memory: a host application that hands
+// all device memory out through its own pool and does not let libraries call
+// cudaMalloc, or a latency-critical loop in which an allocation (which can
+// synchronise the device) is not acceptable.  For them this entry point keeps
+// the one piece of scratch the motion kernel needs between calls -- the
+// previous frame's blurred plane -- in a fixed array compiled into the
+// library, instead of in memory that a context allocates.
+//
+// The array is static device memory: every GPU that loads the library holds
+// it until the process exits.  Host code cannot use the array's name as a
+// device address (it names a host-side stand-in), so the entry point asks the
+// runtime for the device address once per device, on its first call on that
+// device with the device current, and keeps it.
+#include <cstdint>
+#include <cstring>
+
+#include "motion.h"
+#include "motion_internal.h"
+
+namespace {
+
+// The previous frame's blurred plane, rows of round_up(w, 8) uint16 values.
+constexpr size_t kNoallocSamples = MOTION_NOALLOC_MAX_SAMPLES;
+static __device__ __align__(256) uint16_t g_noalloc_bprev[kNoallocSamples];
+// Device error word of the kernels launched from here (bounded waits).
+static __device__ __align__(256) int g_noalloc_err;
+
+constexpr int kMaxDevices = 64;
+struct DeviceSlot {
+    uint16_t* bprev = nullptr;   // device address of g_noalloc_bprev on this device
+    int* err = nullptr;          // device address of g_noalloc_err on this device
+    // the sequence the array currently continues (written by the last call)
+    int w = 0, h = 0, bpc = 0;
+    bool valid = false;
+};
+DeviceSlot g_slots[kMaxDevices];
+
+int setup_device(int dev, DeviceSlot** out) {
+    if (dev < 0 || dev >= kMaxDevices) return MOTION_ERR_INVALID_ARGUMENT;
+    DeviceSlot& s = g_slots[dev];
+    if (!s.bprev) {
+        void* p = nullptr;
+        void* e = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_bprev) != cudaSuccess ||
+            cudaGetSymbolAddress(&e, g_noalloc_err) != cudaSuccess) {
+            cudaGetLastError();
+            return MOTION_ERR_CUDA;
+        }
+        s.bprev = static_cast<uint16_t*>(p);
+        s.err = static_cast<int*>(e);
+    }
+    *out = &s;
+    return MOTION_OK;
+}
+
+}  // namespace
+
+extern "C" int motion_submit_batch_noalloc(const void* d_frames, int n, int w, int h, int bpc,
+                                           size_t frame_stride, size_t pitch,
+                                           int continue_sequence, void* stream,
+                                           uint64_t* d_sad_out) {
+    if (n < 0) return MOTION_ERR_INVALID_ARGUMENT;
+    if (bpc < 8 || bpc > 16) return MOTION_ERR_UNSUPPORTED_BITDEPTH;
+    if (w < 3 || h < 3) return MOTION_ERR_FRAME_TOO_SMALL;
+    if (w > MOTION_MAX_DIM || h > MOTION_MAX_DIM) return MOTION_ERR_TOO_LARGE;
+    const size_t bprev_pitch = ((size_t)w + 7) & ~(size_t)7;
+    if (bprev_pitch * (size_t)h > kNoallocSamples) return MOTION_ERR_TOO_LARGE;
+    if (n == 0) return MOTION_OK;
+    if (!d_frames || !d_sad_out) return MOTION_ERR_INVALID_ARGUMENT;
+    const size_t s = bpc == 8 ? 1 : 2;
+    if (pitch < (size_t)w * s) return MOTION_ERR_BAD_PITCH;
+    if (s == 2 && ((((uintptr_t)d_frames) & 1) || (pitch & 1) || (n > 1 && (frame_stride & 1))))
+        return MOTION_ERR_BAD_PITCH;
+
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return MOTION_ERR_CUDA;
+    }
+    DeviceSlot* slot = nullptr;
+    int rc = setup_device(dev, &slot);
+    if (rc) return rc;
+    // continuing needs the array to hold the last frame of a sequence of the
+    // same size and depth
+    if (continue_sequence && !(slot->valid && slot->w == w && slot->h == h && slot->bpc == bpc))
+        return MOTION_ERR_INVALID_ARGUMENT;
+
+    cudaStream_t st = (cudaStream_t)stream;
+    if (cudaMemsetAsync(d_sad_out, 0, sizeof(uint64_t) * (size_t)n, st) != cudaSuccess) {
+        cudaGetLastError();
+        return MOTION_ERR_CUDA;
+    }
+    mg::TileArgs a;
+    std::memset(&a, 0, sizeof(a));
+    a.ref_y = (const uint8_t*)d_frames;
+    a.pitch_y = (long long)pitch;
+    a.stride_y = (long long)frame_stride;
+    a.w = w;
+    a.h = h;
+    a.cw = (w + 1) / 2;
+    a.ch = (h + 1) / 2;
+    a.bpc = bpc;
+    a.n = n;
+    a.has_prev = continue_sequence ? 1 : 0;
+    a.store_last = 1;
+    a.aligned16 = ((((uintptr_t)d_frames) | pitch) % 16 == 0) && (n <= 1 || frame_stride % 16 == 0);
+    a.bprev = slot->bprev;
+    a.bprev_pitch = (int)bprev_pitch;
+    a.sad_out = (unsigned long long*)d_sad_out;
+    a.err = slot->err;
+    int launched = 0;
+    bool used = false;
+    cudaError_t e = mg::launch_motion_tma(a, false, st, &launched, &used);
+    if (e == cudaSuccess && !used) e = mg::launch_motion_tile(a, false, st, &launched);
+    mg::note_launches(launched);
+    if (e != cudaSuccess) return MOTION_ERR_CUDA;
+    slot->w = w;
+    slot->h = h;
+    slot->bpc = bpc;
+    slot->valid = true;
+    return MOTION_OK;
+}
