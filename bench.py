@@ -339,6 +339,147 @@ def run_gpu(args):
     return 0
 
 
+def run_sequence_workload(args):
+    """Motion-only workloads (not the headline): frames/s and GB/s of the
+    batched motion kernel on one of the sequence configurations, with the
+    batch size of the configuration (or --batch), optionally swept."""
+    import numpy as np
+    import torch
+
+    import integer_image_filter_gb300 as iif
+    import synth
+
+    c = synth.CONFIGS[args.workload]
+    w, h, bpc = c["w"], c["h"], c["bpc"]
+    frames = synth.make(args.workload)
+    n = frames.shape[0]
+    s = 1 if bpc == 8 else 2
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    d = torch.from_numpy(frames.view(np.int16) if bpc > 8 else frames).to(dev)
+    sad = torch.zeros(n, dtype=torch.int64, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    peak, peak_kind = peaks()
+    batches = [args.batch] if args.batch else [c.get("batch", n)]
+    if args.sweep:
+        batches = [1, 2, 4, 8, 16, 32]
+    lines = []
+    for batch in batches:
+        ctx = iif.MotionContext(w, h, bpc)
+
+        def step():
+            ctx.reset()
+            for b0 in range(0, n, batch):
+                ctx.submit_batch(d[b0:b0 + batch], sad[b0:b0 + batch], stream=stream)
+
+        for _ in range(max(args.warmup, 3)):
+            step()
+        torch.cuda.synchronize(dev)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        l0 = iif.motion_kernel_launch_count()
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        ms = e0.elapsed_time(e1) / args.steps
+        launches = (iif.motion_kernel_launch_count() - l0) / args.steps
+        alg = w * h * s * n
+        lines.append({"metric": "frames/s (batched motion SAD)", "value": n / (ms * 1e-3),
+                      "unit": "frames/s", "n_gpus": 1, "steps": args.steps,
+                      "warmup": max(args.warmup, 3), "ms_per_step": ms, "higher_is_better": True,
+                      "dtype": "u8" if bpc == 8 else "u16", "data": "synthetic",
+                      "config": {"workload": args.workload, "w": w, "h": h, "bpc": bpc,
+                                 "frames_per_step": n, "batch": batch,
+                                 "launches_per_step": launches},
+                      "roofline": {"bound": "hbm", "achieved": alg / (ms * 1e-3) / 1e9,
+                                   "peak": peak, "unit": "GB/s",
+                                   "frac": alg / (ms * 1e-3) / 1e9 / peak, "peak_kind": peak_kind,
+                                   "algorithmic_bytes_per_step": alg}})
+        ctx.close()
+    for ln in lines:
+        print(json.dumps(ln), flush=True)
+    return 0
+
+
+def run_sse_workload(args):
+    """The stand-alone SSE launch (all planes of all pairs) on the 4:2:0 pairs."""
+    import torch
+
+    import integer_image_filter_gb300 as iif
+    import synth
+
+    n = args.pairs
+    batch = synth.yuv420_pairs(4, n, args.w, args.h, max_shift=2, dist_sigma=3.0)
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    planes = [torch.from_numpy(p).to(dev) for p in batch.planes()]
+    sse = torch.zeros((n, 3), dtype=torch.int64, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        iif.psnr_sse_yuv420_batch(args.w, args.h, 8, *planes, sse, stream=stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = e0.elapsed_time(e1) / args.steps
+    peak, peak_kind = peaks()
+    alg = algorithmic_bytes_per_pair(args.w, args.h, 8) * n
+    print(json.dumps({"metric": "pairs/s (PSNR SSE of Y, U, V)", "value": n / (ms * 1e-3),
+                      "unit": "frames/s", "ms_per_step": ms, "steps": args.steps,
+                      "config": {"workload": "sse_yuv420_%dx%d_u8_pairs" % (args.w, args.h),
+                                 "pairs_per_step": n},
+                      "roofline": {"bound": "hbm", "achieved": alg / (ms * 1e-3) / 1e9,
+                                   "peak": peak, "unit": "GB/s",
+                                   "frac": alg / (ms * 1e-3) / 1e9 / peak,
+                                   "peak_kind": peak_kind}}), flush=True)
+    return 0
+
+
+def run_latency_workload(args):
+    """Per-frame submit latency (one launch and one 8-byte readback per frame)
+    on the small configurations."""
+    import numpy as np
+    import torch
+
+    import integer_image_filter_gb300 as iif
+    import synth
+
+    c = synth.CONFIGS[args.workload]
+    w, h, bpc = c["w"], c["h"], c["bpc"]
+    frames = synth.make(args.workload)
+    n = frames.shape[0]
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    d = torch.from_numpy(frames).to(dev)
+    ctx = iif.MotionContext(w, h, bpc)
+    for _ in range(3):
+        ctx.reset()
+        for i in range(n):
+            ctx.submit(d[i])
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        ctx.reset()
+        for i in range(n):
+            ctx.submit(d[i])
+    us = (time.perf_counter() - t0) / (args.steps * n) * 1e6
+    ctx.close()
+    print(json.dumps({"metric": "us per submitted frame (launch + 8-byte readback)", "value": us,
+                      "unit": "us/frame", "higher_is_better": False, "steps": args.steps,
+                      "config": {"workload": args.workload, "w": w, "h": h, "bpc": bpc,
+                                 "frames_per_step": n}}), flush=True)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -350,7 +491,19 @@ def main(argv=None):
     ap.add_argument("--h", type=int, default=2160)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", default=WORKLOAD,
+                    help="the headline 4:2:0 workload (default) or one of the motion-only "
+                         "configurations: seq_3840x2160_u10, seq_1920x1080_u8_cuts, "
+                         "seq_576x324_u8, pair_64x48_u8")
+    ap.add_argument("--batch", type=int, default=0, help="frames per launch (sequence workloads)")
+    ap.add_argument("--sweep", action="store_true", help="sweep batch sizes 1..32")
     args = ap.parse_args(argv)
+    if args.workload == "sse_yuv420_3840x2160_u8_pairs" and args.impl == "ours":
+        return run_sse_workload(args)
+    if args.workload in ("seq_3840x2160_u10", "seq_1920x1080_u8_cuts") and args.impl == "ours":
+        return run_sequence_workload(args)
+    if args.workload in ("seq_576x324_u8", "pair_64x48_u8") and args.impl == "ours":
+        return run_latency_workload(args) if not args.batch else run_sequence_workload(args)
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
     if args.impl == "reference":
