@@ -79,8 +79,10 @@ enum motion_status {
 typedef struct motion_ctx motion_ctx;  /* opaque, library-owned */
 
 /* Create a motion context for frames of w x h samples at bpc bits on the
- * current CUDA device.  All device scratch (the previous frame's blurred plane,
- * w*h uint16) is allocated here, never on a submit.  *out receives the handle. */
+ * current CUDA device.  All device scratch (two w*h uint16 planes that take
+ * turns holding the previous frame's blur, so that one launch can read one and
+ * write the other) is allocated here, never on a submit.  *out receives the
+ * handle. */
 MOTION_API int motion_init(int w, int h, int bpc, motion_ctx** out);
 
 /* Free the context and its device memory.  NULL is accepted. */

@@ -67,7 +67,8 @@ struct motion_ctx {
     int w = 0, h = 0, bpc = 8, cw = 0, ch = 0;
     int sm_count = 0;
     int bprev_pitch = 0;            // elements per row of the resident plane
-    uint16_t* d_bprev = nullptr;    // previous frame's blurred plane (B_{i-1})
+    uint16_t* d_bprev[2] = {nullptr, nullptr};  // previous frame's blurred plane, ping-pong
+    int cur = 0;                    // index of the plane that holds B_{i-1}
     int has_prev = 0;
     int* d_err = nullptr;           // device error word (bounded waits that timed out)
     int force_generic = 0;          // diagnostics: always use the generic kernel
@@ -117,6 +118,7 @@ int launch_motion(motion_ctx* c, const mg::TileArgs& a, bool fused, cudaStream_t
     g_launches += (uint64_t)launched;
     if (e != cudaSuccess) return cuda_fail(e);
     c->has_prev = 1;
+    c->cur ^= 1;   // the plane just written holds B of the last frame
     return MOTION_OK;
 }
 
@@ -131,7 +133,8 @@ mg::TileArgs motion_args(motion_ctx* c, int n) {
     a.n = n;
     a.has_prev = c->has_prev;
     a.store_last = 1;
-    a.bprev = c->d_bprev;
+    a.bprev = c->d_bprev[c->cur];
+    a.bprev_out = c->d_bprev[c->cur ^ 1];
     a.bprev_pitch = c->bprev_pitch;
     a.err = c->d_err;
     return a;
@@ -201,7 +204,9 @@ int motion_init(int w, int h, int bpc, motion_ctx** out) {
     if (e == cudaSuccess)
         e = cudaDeviceGetAttribute(&c->sm_count, cudaDevAttrMultiProcessorCount, c->device);
     if (e == cudaSuccess)
-        e = cudaMalloc(&c->d_bprev, sizeof(uint16_t) * (size_t)c->bprev_pitch * (size_t)h);
+        e = cudaMalloc(&c->d_bprev[0], sizeof(uint16_t) * (size_t)c->bprev_pitch * (size_t)h);
+    if (e == cudaSuccess)
+        e = cudaMalloc(&c->d_bprev[1], sizeof(uint16_t) * (size_t)c->bprev_pitch * (size_t)h);
     if (e == cudaSuccess) e = cudaMalloc(&c->d_slot, sizeof(unsigned long long));
     if (e == cudaSuccess) e = cudaMalloc(&c->d_err, sizeof(int));
     if (e == cudaSuccess) e = cudaMemset(c->d_err, 0, sizeof(int));
@@ -220,7 +225,8 @@ int motion_destroy(motion_ctx* c) {
     cudaGetDevice(&prev);
     if (c->device >= 0) cudaSetDevice(c->device);
     free_staging(c);
-    if (c->d_bprev) cudaFree(c->d_bprev);
+    if (c->d_bprev[0]) cudaFree(c->d_bprev[0]);
+    if (c->d_bprev[1]) cudaFree(c->d_bprev[1]);
     if (c->d_slot) cudaFree(c->d_slot);
     if (c->d_err) cudaFree(c->d_err);
     if (c->h_slot) cudaFreeHost(c->h_slot);

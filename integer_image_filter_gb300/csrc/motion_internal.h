@@ -26,11 +26,13 @@ struct TileArgs {
     int has_prev;       // B of the previous frame is in bprev
     int store_last;     // write B of the last frame to bprev
     int aligned16;      // every plane base, pitch and stride is 16-byte aligned
-    uint16_t* bprev;    // resident blurred plane, bprev_pitch elements per row
+    uint16_t* bprev;      // resident blurred plane read as B_prev (has_prev), bprev_pitch per row
+    uint16_t* bprev_out;  // plane that receives B of the last frame (store_last)
     int bprev_pitch;
     unsigned long long* sad_out;  // [n], zeroed by the caller
     unsigned long long* sse_out;  // [n][3], zeroed by the caller (fused only)
     int* err;                     // device error word (bit 0: a stage wait timed out)
+    int chunk;                    // TMA kernel: frames per CTA (grid.z = ceil(n / chunk))
 };
 
 // Tensor maps of one TMA launch (64-byte aligned, passed as a grid constant).

@@ -107,6 +107,7 @@ extern "C" int motion_submit_batch_noalloc(const void* d_frames, int n, int w, i
     a.store_last = 1;
     a.aligned16 = ((((uintptr_t)d_frames) | pitch) % 16 == 0) && (n <= 1 || frame_stride % 16 == 0);
     a.bprev = slot->bprev;
+    a.bprev_out = slot->bprev;   // one array: a continuing launch stays in one chunk
     a.bprev_pitch = (int)bprev_pitch;
     a.sad_out = (unsigned long long*)d_sad_out;
     a.err = slot->err;

@@ -267,7 +267,7 @@ __global__ void __launch_bounds__(NT) motion_tile_kernel(const TileArgs a) {
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const int x = x0 + 4 * q + i;
-                if (y < a.h && x < a.w) a.bprev[(long long)y * a.bprev_pitch + x] = (uint16_t)bp[k][i];
+                if (y < a.h && x < a.w) a.bprev_out[(long long)y * a.bprev_pitch + x] = (uint16_t)bp[k][i];
             }
         }
     }

@@ -26,6 +26,7 @@
 //    error word and leaves instead of spinning.
 #include <cuda.h>
 
+#include <cmath>
 #include <type_traits>
 
 #include "motion_internal.h"
@@ -189,13 +190,25 @@ __global__ void __launch_bounds__(NT, 3) motion_tma_kernel(const __grid_constant
     }
     __syncthreads();
 
-    auto issue = [&](int f) {  // thread 0 only
-        const int s = f % STAGES;
+    // this CTA's frames: chunk blockIdx.z of the launch; a chunk after the
+    // first starts one frame early to rebuild B_prev (no outputs for it)
+    const int chunk = a.chunk > 0 ? a.chunk : a.n;
+    const int f_begin = blockIdx.z * chunk;
+    const int f_end = min(a.n, f_begin + chunk);
+    const bool warm = blockIdx.z > 0;
+    const int first = f_begin - (warm ? 1 : 0);
+    const int cnt = f_end - first;
+    const bool use_prev = !warm && a.has_prev;
+
+    auto issue = [&](int l) {  // thread 0 only; l = frame index within the chunk
+        const int s = l % STAGES;
+        const int f = first + l;
         unsigned char* st = smem + s * STAGE;
+        const bool luma_only = warm && l == 0;
         fence_proxy_async();
-        mbar_arrive_expect_tx(&full[s], STAGE);
+        mbar_arrive_expect_tx(&full[s], luma_only ? G::RAW_BYTES : STAGE);
         tma_load_3d(st, &maps.raw, x0 - G::HX, y0 - 2, f, &full[s]);
-        if constexpr (FUSED) {
+        if (FUSED && !luma_only) {
             tma_load_3d(st + G::RAW_BYTES, &maps.dist, x0, y0, f, &full[s]);
             unsigned char* sc = st + G::RAW_BYTES + G::DIST_BYTES;
             tma_load_3d(sc, &maps.ru, x0 / 2, y0 / 2, f, &full[s]);
@@ -205,8 +218,8 @@ __global__ void __launch_bounds__(NT, 3) motion_tma_kernel(const __grid_constant
         }
     };
     if (tid == 0) {
-        const int pre = a.n < STAGES ? a.n : STAGES;
-        for (int f = 0; f < pre; ++f) issue(f);
+        const int pre = cnt < STAGES ? cnt : STAGES;
+        for (int l = 0; l < pre; ++l) issue(l);
     }
 
     // this thread's outputs: rows 4w + k, columns 4q .. 4q+3 (q = lane)
@@ -218,7 +231,7 @@ __global__ void __launch_bounds__(NT, 3) motion_tma_kernel(const __grid_constant
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const int x = x0 + 4 * q + i;
-            bp[k][i] = (a.has_prev && y < a.h && x < a.w) ? a.bprev[(long long)y * a.bprev_pitch + x] : 0u;
+            bp[k][i] = (use_prev && y < a.h && x < a.w) ? a.bprev[(long long)y * a.bprev_pitch + x] : 0u;
         }
     }
     // valid columns of this thread's quad in each of its rows (edge tiles)
@@ -239,18 +252,19 @@ __global__ void __launch_bounds__(NT, 3) motion_tma_kernel(const __grid_constant
                            ((2 * warp + (lane >> 4)) * G::CW + 4 * (lane & 15)) * G::S;
     bool timed_out = false;
 
-    for (int f = 0; f < a.n; ++f) {
-        const int s = f % STAGES;
-        const unsigned parity = (unsigned)(f / STAGES) & 1u;
+    for (int l = 0; l < cnt; ++l) {
+        const int f = first + l;   // frame index in the launch
+        const int s = l % STAGES;
+        const unsigned parity = (unsigned)(l / STAGES) & 1u;
         const bool ok = mbar_wait_bounded(&full[s], parity, kWaitCycles);
         timed_out |= !ok;
         unsigned char* st = smem + s * STAGE;
         // the stage of frame f-1 takes frame f+STAGES-1 as soon as every warp
         // has released it
-        if (tid == 0 && f >= 1 && f + STAGES - 1 < a.n) {
-            const int sp = (f - 1) % STAGES;
-            if (mbar_wait_bounded(&empty[sp], (unsigned)((f - 1) / STAGES) & 1u, kWaitCycles))
-                issue(f + STAGES - 1);
+        if (tid == 0 && l >= 1 && l + STAGES - 1 < cnt) {
+            const int sp = (l - 1) % STAGES;
+            if (mbar_wait_bounded(&empty[sp], (unsigned)((l - 1) / STAGES) & 1u, kWaitCycles))
+                issue(l + STAGES - 1);
             else
                 timed_out = true;
         }
@@ -275,7 +289,8 @@ __global__ void __launch_bounds__(NT, 3) motion_tma_kernel(const __grid_constant
         __syncwarp();
 
         // ---- horizontal pass, SAD against B_prev, squared errors
-        const bool do_sad = (f > 0) || a.has_prev;
+        const bool do_out = l > 0 || !warm;          // not the warm-up frame
+        const bool do_sad = l > 0 || use_prev;
         uint32_t sad = 0;
         [[maybe_unused]] Acc sse_y = 0, sse_u = 0, sse_v = 0;
 #pragma unroll
@@ -297,7 +312,7 @@ __global__ void __launch_bounds__(NT, 3) motion_tma_kernel(const __grid_constant
             }
 #pragma unroll
             for (int i = 0; i < 4; ++i) bp[k][i] = b[i];
-            if constexpr (FUSED) {
+            if (FUSED && do_out) {
                 const Pix* dp = reinterpret_cast<const Pix*>(st + off_dist + k * TW * G::S);
                 if constexpr (sizeof(Pix) == 1) {
                     uint32_t d = __vabsdiffu4(center[k], *reinterpret_cast<const uint32_t*>(dp));
@@ -316,7 +331,7 @@ __global__ void __launch_bounds__(NT, 3) motion_tma_kernel(const __grid_constant
                 }
             }
         }
-        if constexpr (FUSED) {
+        if (FUSED && do_out) {
             // 4:2:0 chroma: 16 rows x 64 columns per plane; warp w takes rows
             // 2w, 2w+1, 4 samples per lane; outside the picture both sides were
             // zero-filled, so they add 0
@@ -365,14 +380,14 @@ __global__ void __launch_bounds__(NT, 3) motion_tma_kernel(const __grid_constant
                 }
             }
             if (lane == 0) {
-                Part* pp = &part[f & (SLOTS - 1)][warp][0];
+                Part* pp = &part[l & (SLOTS - 1)][warp][0];
                 pp[0] = do_sad ? (Part)wsad : (Part)0;
                 pp[1] = (Part)wy;
                 pp[2] = (Part)wu;
                 pp[3] = (Part)wvv;
             }
         }
-        if ((f & (FLUSH - 1)) == FLUSH - 1 || f == a.n - 1) {
+        if ((l & (FLUSH - 1)) == FLUSH - 1 || l == cnt - 1) {
             if (__syncthreads_or(timed_out)) {
                 // a stage wait ran out somewhere in the block: leave together
                 if (tid == 0 && a.err) atomicOr(a.err, 1);
@@ -380,25 +395,27 @@ __global__ void __launch_bounds__(NT, 3) motion_tma_kernel(const __grid_constant
                 return;
             }
             if (warp == 0) {
-                const int j = (f & ~(FLUSH - 1)) + (lane >> 2), acc = lane & 3;
-                if (j <= f && (acc != 0 || j > 0 || a.has_prev) && (FUSED || acc == 0)) {
+                const int j = (l & ~(FLUSH - 1)) + (lane >> 2), acc = lane & 3;
+                const bool j_out = j > 0 || !warm, j_sad = j > 0 || use_prev;
+                if (j <= l && (acc == 0 ? j_sad : j_out) && (FUSED || acc == 0)) {
                     unsigned long long t = 0;
 #pragma unroll
                     for (int w = 0; w < NW; ++w) t += part[j & (SLOTS - 1)][w][acc];
-                    atomicAdd(acc == 0 ? a.sad_out + j : a.sse_out + 3LL * j + (acc - 1), t);
+                    const long long g = first + j;
+                    atomicAdd(acc == 0 ? a.sad_out + g : a.sse_out + 3LL * g + (acc - 1), t);
                 }
             }
         }
     }
 
-    if (a.store_last && a.n > 0) {
+    if (a.store_last && cnt > 0 && f_end == a.n) {
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
             const int y = y0 + 4 * warp + k;
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const int x = x0 + 4 * q + i;
-                if (y < a.h && x < a.w) a.bprev[(long long)y * a.bprev_pitch + x] = (uint16_t)bp[k][i];
+                if (y < a.h && x < a.w) a.bprev_out[(long long)y * a.bprev_pitch + x] = (uint16_t)bp[k][i];
             }
         }
     }
@@ -454,8 +471,46 @@ cudaError_t launch_tma_one(const TmaMaps& maps, const TileArgs& a, cudaStream_t 
         if (e != cudaSuccess) return e;
         __atomic_fetch_or(&configured, bit, __ATOMIC_RELEASE);
     }
-    dim3 grid((a.w + TW - 1) / TW, (a.h + TH - 1) / TH);
-    motion_tma_kernel<Pix, FUSED, STAGES><<<grid, NT, SMEM, s>>>(maps, a);
+    // Size the launch by the SM count (ADR-1226): split the frames into
+    // chunks so that tiles x chunks fill whole waves of resident CTAs, each
+    // chunk after the first paying one warm-up frame.
+    static int slots_per_sm[64] = {0};
+    int& spm = slots_per_sm[dev & 63];
+    if (spm == 0) {
+        int per_sm = 0, sms = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, motion_tma_kernel<Pix, FUSED, STAGES>,
+                                                          NT, SMEM);
+        if (e != cudaSuccess) return e;
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        spm = (per_sm > 0 ? per_sm : 1) * sms;
+    }
+    TileArgs b = a;
+    const long long tiles = (long long)((a.w + TW - 1) / TW) * ((a.h + TH - 1) / TH);
+    int best_c = 1;
+    double best = 1e30;
+    // a launch that reads and writes the same resident plane keeps one chunk:
+    // the last chunk's store must not overtake the first chunk's read.  A
+    // grid that already fills 1.5 waves stays whole as well: every chunk pays
+    // its own pipeline fill, which costs more than the partial last wave.
+    const bool same_plane = a.has_prev && a.bprev == a.bprev_out;
+    const int max_c = (same_plane || tiles * 2 >= 3LL * spm) ? 1 : 8;
+    for (int c = 1; c <= max_c && c <= a.n; ++c) {
+        const int len = (a.n + c - 1) / c;
+        const int cz = (a.n + len - 1) / len;
+        const double units = (double)tiles * cz;
+        const double waves = units / spm;
+        const double fill = waves / std::ceil(waves);
+        const double work = (double)(a.n + cz - 1) / a.n;
+        const double cost = work / fill;
+        if (cost < best - 1e-9) {
+            best = cost;
+            best_c = cz;
+        }
+    }
+    b.chunk = (a.n + best_c - 1) / best_c;
+    dim3 grid((a.w + TW - 1) / TW, (a.h + TH - 1) / TH, (a.n + b.chunk - 1) / b.chunk);
+    motion_tma_kernel<Pix, FUSED, STAGES><<<grid, NT, SMEM, s>>>(maps, b);
     return cudaGetLastError();
 }
 
