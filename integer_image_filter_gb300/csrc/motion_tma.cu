@@ -312,7 +312,7 @@ __global__ void __launch_bounds__(NT, 3) motion_tma_kernel(const __grid_constant
             }
 #pragma unroll
             for (int i = 0; i < 4; ++i) bp[k][i] = b[i];
-            if (FUSED && do_out) {
+            if constexpr (FUSED) {
                 const Pix* dp = reinterpret_cast<const Pix*>(st + off_dist + k * TW * G::S);
                 if constexpr (sizeof(Pix) == 1) {
                     uint32_t d = __vabsdiffu4(center[k], *reinterpret_cast<const uint32_t*>(dp));
@@ -331,7 +331,7 @@ __global__ void __launch_bounds__(NT, 3) motion_tma_kernel(const __grid_constant
                 }
             }
         }
-        if (FUSED && do_out) {
+        if constexpr (FUSED) {
             // 4:2:0 chroma: 16 rows x 64 columns per plane; warp w takes rows
             // 2w, 2w+1, 4 samples per lane; outside the picture both sides were
             // zero-filled, so they add 0
@@ -382,9 +382,9 @@ __global__ void __launch_bounds__(NT, 3) motion_tma_kernel(const __grid_constant
             if (lane == 0) {
                 Part* pp = &part[l & (SLOTS - 1)][warp][0];
                 pp[0] = do_sad ? (Part)wsad : (Part)0;
-                pp[1] = (Part)wy;
-                pp[2] = (Part)wu;
-                pp[3] = (Part)wvv;
+                pp[1] = do_out ? (Part)wy : (Part)0;
+                pp[2] = do_out ? (Part)wu : (Part)0;
+                pp[3] = do_out ? (Part)wvv : (Part)0;
             }
         }
         if ((l & (FLUSH - 1)) == FLUSH - 1 || l == cnt - 1) {
