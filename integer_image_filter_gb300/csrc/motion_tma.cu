@@ -252,161 +252,171 @@ __global__ void __launch_bounds__(NT, 3) motion_tma_kernel(const __grid_constant
                            ((2 * warp + (lane >> 4)) * G::CW + 4 * (lane & 15)) * G::S;
     bool timed_out = false;
 
-    for (int l = 0; l < cnt; ++l) {
-        const int f = first + l;   // frame index in the launch
-        const int s = l % STAGES;
-        const unsigned parity = (unsigned)(l / STAGES) & 1u;
-        const bool ok = mbar_wait_bounded(&full[s], parity, kWaitCycles);
-        timed_out |= !ok;
-        unsigned char* st = smem + s * STAGE;
-        // the stage of frame f-1 takes frame f+STAGES-1 as soon as every warp
-        // has released it
-        if (tid == 0 && l >= 1 && l + STAGES - 1 < cnt) {
-            const int sp = (l - 1) % STAGES;
-            if (mbar_wait_bounded(&empty[sp], (unsigned)((l - 1) / STAGES) & 1u, kWaitCycles))
-                issue(l + STAGES - 1);
-            else
-                timed_out = true;
-        }
-        if (edge) {
-            // border tiles write the mirrored halo together (block barriers)
-            if (!__syncthreads_and(ok)) {
-                if (tid == 0 && a.err) atomicOr(a.err, 1);
-                mbar_wait_bounded(&full[s], parity, kWaitCycles);
-                return;
+    // The frame loop, compiled twice: for interior tiles (no mirror patch, no
+    // masks) and for tiles on the frame border.  A runtime test per frame
+    // costs the interior tiles several percent.
+    auto frames = [&](auto interior_tag) -> bool {
+        constexpr bool INTERIOR = decltype(interior_tag)::value;
+        for (int l = 0; l < cnt; ++l) {
+            const int f = first + l;   // frame index in the launch
+            const int s = l % STAGES;
+            const unsigned parity = (unsigned)(l / STAGES) & 1u;
+            const bool ok = mbar_wait_bounded(&full[s], parity, kWaitCycles);
+            timed_out |= !ok;
+            unsigned char* st = smem + s * STAGE;
+            // the stage of frame f-1 takes frame f+STAGES-1 as soon as every warp
+            // has released it
+            if (tid == 0 && l >= 1 && l + STAGES - 1 < cnt) {
+                const int sp = (l - 1) % STAGES;
+                if (mbar_wait_bounded(&empty[sp], (unsigned)((l - 1) / STAGES) & 1u, kWaitCycles))
+                    issue(l + STAGES - 1);
+                else
+                    timed_out = true;
             }
-            patch_mirror<Pix>(reinterpret_cast<Pix*>(st), a, x0, y0, pl, pr, pt, pb);
-        }
-
-        // ---- vertical pass of the warp's 4 rows (staged row r <-> y0 - 2 + r)
-        uint32_t center[4];
-        vertical_quad(reinterpret_cast<const Pix*>(st + off_vsrc), sV + 4 + 4 * lane, rnd, sh, center);
-        if (lane < 16) {  // the two halo columns on each side, 4 rows
-            const Pix* c = reinterpret_cast<const Pix*>(st + off_halo);
-            sV[halo_r * SVW + 4 + halo_off] = vtap(c[0], c[G::RAW_W], c[2 * G::RAW_W],
-                                                   c[3 * G::RAW_W], c[4 * G::RAW_W], rnd, sh);
-        }
-        __syncwarp();
-
-        // ---- horizontal pass, SAD against B_prev, squared errors
-        const bool do_out = l > 0 || !warm;          // not the warm-up frame
-        const bool do_sad = l > 0 || use_prev;
-        uint32_t sad = 0;
-        [[maybe_unused]] Acc sse_y = 0, sse_u = 0, sse_v = 0;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const uint32_t* v = sV + k * SVW + 4 * q;
-            const uint4 A = *reinterpret_cast<const uint4*>(v);
-            const uint4 Bq = *reinterpret_cast<const uint4*>(v + 4);
-            const uint4 C = *reinterpret_cast<const uint4*>(v + 8);
-            const uint32_t wv[12] = {A.x, A.y, A.z, A.w, Bq.x, Bq.y, Bq.z, Bq.w, C.x, C.y, C.z, C.w};
-            uint32_t b[4];
-            horizontal_quad(wv, b);
-            if (full_tile) {
-#pragma unroll
-                for (int i = 0; i < 4; ++i) sad = __sad(b[i], bp[k][i], sad);
-            } else {
-                // an invalid sample compares with itself and adds 0
-#pragma unroll
-                for (int i = 0; i < 4; ++i) sad = __sad(b[i], i < nvalid[k] ? bp[k][i] : b[i], sad);
+            if (!INTERIOR && edge) {
+                // border tiles write the mirrored halo together (block barriers)
+                if (!__syncthreads_and(ok)) {
+                    if (tid == 0 && a.err) atomicOr(a.err, 1);
+                    mbar_wait_bounded(&full[s], parity, kWaitCycles);
+                    return false;
+                }
+                patch_mirror<Pix>(reinterpret_cast<Pix*>(st), a, x0, y0, pl, pr, pt, pb);
             }
-#pragma unroll
-            for (int i = 0; i < 4; ++i) bp[k][i] = b[i];
-            if constexpr (FUSED) {
-                const Pix* dp = reinterpret_cast<const Pix*>(st + off_dist + k * TW * G::S);
-                if constexpr (sizeof(Pix) == 1) {
-                    uint32_t d = __vabsdiffu4(center[k], *reinterpret_cast<const uint32_t*>(dp));
-                    if (!full_tile)
-                        d &= nvalid[k] <= 0 ? 0u : (0xffffffffu >> (8 * (4 - nvalid[k])));
-                    sse_y = __dp4a(d, d, sse_y);
+
+            // ---- vertical pass of the warp's 4 rows (staged row r <-> y0 - 2 + r)
+            uint32_t center[4];
+            vertical_quad(reinterpret_cast<const Pix*>(st + off_vsrc), sV + 4 + 4 * lane, rnd, sh, center);
+            if (lane < 16) {  // the two halo columns on each side, 4 rows
+                const Pix* c = reinterpret_cast<const Pix*>(st + off_halo);
+                sV[halo_r * SVW + 4 + halo_off] = vtap(c[0], c[G::RAW_W], c[2 * G::RAW_W],
+                                                       c[3 * G::RAW_W], c[4 * G::RAW_W], rnd, sh);
+            }
+            __syncwarp();
+
+            // ---- horizontal pass, SAD against B_prev, squared errors
+            const bool do_out = l > 0 || !warm;          // not the warm-up frame
+            const bool do_sad = l > 0 || use_prev;
+            uint32_t sad = 0;
+            [[maybe_unused]] Acc sse_y = 0, sse_u = 0, sse_v = 0;
+    #pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const uint32_t* v = sV + k * SVW + 4 * q;
+                const uint4 A = *reinterpret_cast<const uint4*>(v);
+                const uint4 Bq = *reinterpret_cast<const uint4*>(v + 4);
+                const uint4 C = *reinterpret_cast<const uint4*>(v + 8);
+                const uint32_t wv[12] = {A.x, A.y, A.z, A.w, Bq.x, Bq.y, Bq.z, Bq.w, C.x, C.y, C.z, C.w};
+                uint32_t b[4];
+                horizontal_quad(wv, b);
+                if (INTERIOR || full_tile) {
+    #pragma unroll
+                    for (int i = 0; i < 4; ++i) sad = __sad(b[i], bp[k][i], sad);
                 } else {
-                    uint32_t rf[4], ds[4];
-                    unpack4(reinterpret_cast<const Pix*>(st + off_ref + k * G::RAW_W * G::S), rf);
-                    unpack4(dp, ds);
-#pragma unroll
+                    // an invalid sample compares with itself and adds 0
+    #pragma unroll
+                    for (int i = 0; i < 4; ++i) sad = __sad(b[i], i < nvalid[k] ? bp[k][i] : b[i], sad);
+                }
+    #pragma unroll
+                for (int i = 0; i < 4; ++i) bp[k][i] = b[i];
+                if constexpr (FUSED) {
+                    const Pix* dp = reinterpret_cast<const Pix*>(st + off_dist + k * TW * G::S);
+                    if constexpr (sizeof(Pix) == 1) {
+                        uint32_t d = __vabsdiffu4(center[k], *reinterpret_cast<const uint32_t*>(dp));
+                        if (!INTERIOR && !full_tile)
+                            d &= nvalid[k] <= 0 ? 0u : (0xffffffffu >> (8 * (4 - nvalid[k])));
+                        sse_y = __dp4a(d, d, sse_y);
+                    } else {
+                        uint32_t rf[4], ds[4];
+                        unpack4(reinterpret_cast<const Pix*>(st + off_ref + k * G::RAW_W * G::S), rf);
+                        unpack4(dp, ds);
+    #pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const long long e = (long long)rf[i] - (long long)ds[i];
+                            sse_y += (INTERIOR || i < nvalid[k]) ? (Acc)(e * e) : (Acc)0;
+                        }
+                    }
+                }
+            }
+            if constexpr (FUSED) {
+                // 4:2:0 chroma: 16 rows x 64 columns per plane; warp w takes rows
+                // 2w, 2w+1, 4 samples per lane; outside the picture both sides were
+                // zero-filled, so they add 0
+                const unsigned char* sc = st + off_chroma;
+                if constexpr (sizeof(Pix) == 1) {
+                    const uint32_t du = __vabsdiffu4(*reinterpret_cast<const uint32_t*>(sc),
+                                                     *reinterpret_cast<const uint32_t*>(sc + G::C_BYTES));
+                    const uint32_t dv = __vabsdiffu4(*reinterpret_cast<const uint32_t*>(sc + 2 * G::C_BYTES),
+                                                     *reinterpret_cast<const uint32_t*>(sc + 3 * G::C_BYTES));
+                    sse_u = __dp4a(du, du, 0u);
+                    sse_v = __dp4a(dv, dv, 0u);
+                } else {
+                    uint32_t ru[4], du[4], rv[4], dv[4];
+                    unpack4(reinterpret_cast<const Pix*>(sc), ru);
+                    unpack4(reinterpret_cast<const Pix*>(sc + G::C_BYTES), du);
+                    unpack4(reinterpret_cast<const Pix*>(sc + 2 * G::C_BYTES), rv);
+                    unpack4(reinterpret_cast<const Pix*>(sc + 3 * G::C_BYTES), dv);
+    #pragma unroll
                     for (int i = 0; i < 4; ++i) {
-                        const long long e = (long long)rf[i] - (long long)ds[i];
-                        sse_y += i < nvalid[k] ? (Acc)(e * e) : (Acc)0;
+                        const long long eu = (long long)ru[i] - (long long)du[i];
+                        const long long ev = (long long)rv[i] - (long long)dv[i];
+                        sse_u += (Acc)(eu * eu);
+                        sse_v += (Acc)(ev * ev);
+                    }
+                }
+            }
+            // every lane has finished reading this stage: release it to the producer
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[s]);
+
+            // ---- warp sums of this frame into its slot; every FLUSH frames the
+            // block adds the slots to the outputs, one atomic per accumulator and
+            // frame (warp 0, lane = frame x accumulator)
+            {
+                const unsigned long long wsad = __reduce_add_sync(0xffffffffu, sad);
+                unsigned long long wy = 0, wu = 0, wvv = 0;
+                if constexpr (FUSED) {
+                    if constexpr (sizeof(Pix) == 1) {
+                        wy = __reduce_add_sync(0xffffffffu, sse_y);
+                        wu = __reduce_add_sync(0xffffffffu, sse_u);
+                        wvv = __reduce_add_sync(0xffffffffu, sse_v);
+                    } else {
+                        wy = warp_sum(sse_y);
+                        wu = warp_sum(sse_u);
+                        wvv = warp_sum(sse_v);
+                    }
+                }
+                if (lane == 0) {
+                    Part* pp = &part[l & (SLOTS - 1)][warp][0];
+                    pp[0] = do_sad ? (Part)wsad : (Part)0;
+                    pp[1] = do_out ? (Part)wy : (Part)0;
+                    pp[2] = do_out ? (Part)wu : (Part)0;
+                    pp[3] = do_out ? (Part)wvv : (Part)0;
+                }
+            }
+            if ((l & (FLUSH - 1)) == FLUSH - 1 || l == cnt - 1) {
+                if (__syncthreads_or(timed_out)) {
+                    // a stage wait ran out somewhere in the block: leave together
+                    if (tid == 0 && a.err) atomicOr(a.err, 1);
+                    mbar_wait_bounded(&full[s], parity, kWaitCycles);
+                    return false;
+                }
+                if (warp == 0) {
+                    const int j = (l & ~(FLUSH - 1)) + (lane >> 2), acc = lane & 3;
+                    const bool j_out = j > 0 || !warm, j_sad = j > 0 || use_prev;
+                    if (j <= l && (acc == 0 ? j_sad : j_out) && (FUSED || acc == 0)) {
+                        unsigned long long t = 0;
+    #pragma unroll
+                        for (int w = 0; w < NW; ++w) t += part[j & (SLOTS - 1)][w][acc];
+                        const long long g = first + j;
+                        atomicAdd(acc == 0 ? a.sad_out + g : a.sse_out + 3LL * g + (acc - 1), t);
                     }
                 }
             }
         }
-        if constexpr (FUSED) {
-            // 4:2:0 chroma: 16 rows x 64 columns per plane; warp w takes rows
-            // 2w, 2w+1, 4 samples per lane; outside the picture both sides were
-            // zero-filled, so they add 0
-            const unsigned char* sc = st + off_chroma;
-            if constexpr (sizeof(Pix) == 1) {
-                const uint32_t du = __vabsdiffu4(*reinterpret_cast<const uint32_t*>(sc),
-                                                 *reinterpret_cast<const uint32_t*>(sc + G::C_BYTES));
-                const uint32_t dv = __vabsdiffu4(*reinterpret_cast<const uint32_t*>(sc + 2 * G::C_BYTES),
-                                                 *reinterpret_cast<const uint32_t*>(sc + 3 * G::C_BYTES));
-                sse_u = __dp4a(du, du, 0u);
-                sse_v = __dp4a(dv, dv, 0u);
-            } else {
-                uint32_t ru[4], du[4], rv[4], dv[4];
-                unpack4(reinterpret_cast<const Pix*>(sc), ru);
-                unpack4(reinterpret_cast<const Pix*>(sc + G::C_BYTES), du);
-                unpack4(reinterpret_cast<const Pix*>(sc + 2 * G::C_BYTES), rv);
-                unpack4(reinterpret_cast<const Pix*>(sc + 3 * G::C_BYTES), dv);
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const long long eu = (long long)ru[i] - (long long)du[i];
-                    const long long ev = (long long)rv[i] - (long long)dv[i];
-                    sse_u += (Acc)(eu * eu);
-                    sse_v += (Acc)(ev * ev);
-                }
-            }
-        }
-        // every lane has finished reading this stage: release it to the producer
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[s]);
-
-        // ---- warp sums of this frame into its slot; every FLUSH frames the
-        // block adds the slots to the outputs, one atomic per accumulator and
-        // frame (warp 0, lane = frame x accumulator)
-        {
-            const unsigned long long wsad = __reduce_add_sync(0xffffffffu, sad);
-            unsigned long long wy = 0, wu = 0, wvv = 0;
-            if constexpr (FUSED) {
-                if constexpr (sizeof(Pix) == 1) {
-                    wy = __reduce_add_sync(0xffffffffu, sse_y);
-                    wu = __reduce_add_sync(0xffffffffu, sse_u);
-                    wvv = __reduce_add_sync(0xffffffffu, sse_v);
-                } else {
-                    wy = warp_sum(sse_y);
-                    wu = warp_sum(sse_u);
-                    wvv = warp_sum(sse_v);
-                }
-            }
-            if (lane == 0) {
-                Part* pp = &part[l & (SLOTS - 1)][warp][0];
-                pp[0] = do_sad ? (Part)wsad : (Part)0;
-                pp[1] = do_out ? (Part)wy : (Part)0;
-                pp[2] = do_out ? (Part)wu : (Part)0;
-                pp[3] = do_out ? (Part)wvv : (Part)0;
-            }
-        }
-        if ((l & (FLUSH - 1)) == FLUSH - 1 || l == cnt - 1) {
-            if (__syncthreads_or(timed_out)) {
-                // a stage wait ran out somewhere in the block: leave together
-                if (tid == 0 && a.err) atomicOr(a.err, 1);
-                mbar_wait_bounded(&full[s], parity, kWaitCycles);
-                return;
-            }
-            if (warp == 0) {
-                const int j = (l & ~(FLUSH - 1)) + (lane >> 2), acc = lane & 3;
-                const bool j_out = j > 0 || !warm, j_sad = j > 0 || use_prev;
-                if (j <= l && (acc == 0 ? j_sad : j_out) && (FUSED || acc == 0)) {
-                    unsigned long long t = 0;
-#pragma unroll
-                    for (int w = 0; w < NW; ++w) t += part[j & (SLOTS - 1)][w][acc];
-                    const long long g = first + j;
-                    atomicAdd(acc == 0 ? a.sad_out + g : a.sse_out + 3LL * g + (acc - 1), t);
-                }
-            }
-        }
-    }
+        return true;
+    };
+    const bool interior = full_tile && !edge;
+    const bool alive = interior ? frames(std::true_type{}) : frames(std::false_type{});
+    if (!alive) return;
 
     if (a.store_last && cnt > 0 && f_end == a.n) {
 #pragma unroll
