@@ -184,6 +184,13 @@ MOTION_API int psnr_from_sse(uint64_t sse, uint64_t n_samples, int bpc, double* 
 #define MOTION_PATH_GENERIC 1
 MOTION_API int motion_set_kernel_path(motion_ctx* ctx, int path);
 
+/* Test hook for the kernels' bounded waits (no counterpart in the paper):
+ * while on, TMA launches on this context expect 16 bytes per stage more than
+ * their boxes deliver, so no stage wait can complete, and bound every wait at
+ * about 2 ms; the kernels then set bit 0 of the device error word and leave.
+ * Results of such launches are incomplete.  Turn it off to compute again. */
+MOTION_API int motion_set_stall_injection(motion_ctx* ctx, int on);
+
 /* Read and clear the context's device error word after waiting for the
  * device: bit 0 set means a kernel's bounded wait for a staged tile ran out
  * (its results are then incomplete).  *flags receives the word. */

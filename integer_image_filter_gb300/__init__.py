@@ -26,7 +26,7 @@ __all__ = [
     "psnr_sse_yuv420_batch", "motion_scores_from_sad", "psnr_from_sse",
     "motion_kernel_launch_count", "motion_strerror", "MotionContext", "EXPORTED_SYMBOLS",
     "motion_set_kernel_path", "motion_device_error", "MOTION_PATH_AUTO", "MOTION_PATH_GENERIC",
-    "motion_submit_batch_noalloc",
+    "motion_submit_batch_noalloc", "motion_set_stall_injection",
 ]
 
 EXPORTED_SYMBOLS = (
@@ -35,6 +35,7 @@ EXPORTED_SYMBOLS = (
     "psnr_sse", "psnr_sse_yuv420_batch", "motion_scores_from_sad", "psnr_from_sse",
     "motion_kernel_launch_count", "motion_strerror", "motion_last_cuda_error",
     "motion_set_kernel_path", "motion_device_error", "motion_submit_batch_noalloc",
+    "motion_set_stall_injection",
 )
 
 _LIB: ctypes.CDLL | None = None
@@ -73,6 +74,7 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
         "motion_set_kernel_path": ([P, I], I),
         "motion_device_error": ([P, ctypes.POINTER(I)], I),
         "motion_submit_batch_noalloc": ([P, I, I, I, I, Z, Z, I, P, P], I),
+        "motion_set_stall_injection": ([P, I], I),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -318,6 +320,11 @@ MOTION_PATH_GENERIC = 1
 
 def motion_set_kernel_path(ctx: int, path: int) -> None:
     _check(load_library().motion_set_kernel_path(ctx, path), "motion_set_kernel_path")
+
+
+def motion_set_stall_injection(ctx: int, on: bool) -> None:
+    _check(load_library().motion_set_stall_injection(ctx, 1 if on else 0),
+           "motion_set_stall_injection")
 
 
 def motion_device_error(ctx: int) -> int:

@@ -72,6 +72,7 @@ struct motion_ctx {
     int has_prev = 0;
     int* d_err = nullptr;           // device error word (bounded waits that timed out)
     int force_generic = 0;          // diagnostics: always use the generic kernel
+    int stall_injection = 0;        // test hook: stage waits that can never complete
     unsigned long long* d_slot = nullptr;   // single-submit result
     unsigned long long* h_slot = nullptr;   // pinned readback slot
     // host-buffer pipeline
@@ -137,6 +138,10 @@ mg::TileArgs motion_args(motion_ctx* c, int n) {
     a.bprev_out = c->d_bprev[c->cur ^ 1];
     a.bprev_pitch = c->bprev_pitch;
     a.err = c->d_err;
+    if (c->stall_injection) {
+        a.tx_extra = 16;               // the stage expects 16 bytes that never arrive
+        a.wait_cycles = 1LL << 22;     // and gives up after about 2 ms
+    }
     return a;
 }
 
@@ -496,6 +501,12 @@ int motion_set_kernel_path(motion_ctx* c, int path) {
     if (!c || (path != MOTION_PATH_AUTO && path != MOTION_PATH_GENERIC))
         return MOTION_ERR_INVALID_ARGUMENT;
     c->force_generic = path == MOTION_PATH_GENERIC;
+    return MOTION_OK;
+}
+
+int motion_set_stall_injection(motion_ctx* c, int on) {
+    if (!c) return MOTION_ERR_INVALID_ARGUMENT;
+    c->stall_injection = on ? 1 : 0;
     return MOTION_OK;
 }
 

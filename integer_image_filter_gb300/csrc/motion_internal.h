@@ -33,6 +33,8 @@ struct TileArgs {
     unsigned long long* sse_out;  // [n][3], zeroed by the caller (fused only)
     int* err;                     // device error word (bit 0: a stage wait timed out)
     int chunk;                    // TMA kernel: frames per CTA (grid.z = ceil(n / chunk))
+    long long wait_cycles;        // bound of every mbarrier wait (0: about one second)
+    int tx_extra;                 // test hook: bytes a stage expects beyond its boxes (0)
 };
 
 // Tensor maps of one TMA launch (64-byte aligned, passed as a grid constant).

@@ -34,7 +34,7 @@
 
 namespace mg {
 
-constexpr long long kWaitCycles = 1LL << 31;  // about one second: a stage wait never lasts longer
+constexpr long long kWaitCycles = 1LL << 31;  // default wait bound: about one second
 
 // Mirror the halo of a staged luma box in place for tiles on the frame border.
 template <typename Pix>
@@ -171,6 +171,7 @@ __global__ void __launch_bounds__(NT, 3) motion_tma_kernel(const __grid_constant
     const bool edge = pl || pr || pt || pb;
     const uint32_t rnd = 1u << (a.bpc - 1);
     const int sh = a.bpc;
+    const long long wait_cycles = a.wait_cycles > 0 ? a.wait_cycles : kWaitCycles;
 
     if (tid == 0) {
 #pragma unroll
@@ -206,7 +207,7 @@ __global__ void __launch_bounds__(NT, 3) motion_tma_kernel(const __grid_constant
         unsigned char* st = smem + s * STAGE;
         const bool luma_only = warm && l == 0;
         fence_proxy_async();
-        mbar_arrive_expect_tx(&full[s], luma_only ? G::RAW_BYTES : STAGE);
+        mbar_arrive_expect_tx(&full[s], (luma_only ? G::RAW_BYTES : STAGE) + a.tx_extra);
         tma_load_3d(st, &maps.raw, x0 - G::HX, y0 - 2, f, &full[s]);
         if (FUSED && !luma_only) {
             tma_load_3d(st + G::RAW_BYTES, &maps.dist, x0, y0, f, &full[s]);
@@ -261,14 +262,14 @@ __global__ void __launch_bounds__(NT, 3) motion_tma_kernel(const __grid_constant
             const int f = first + l;   // frame index in the launch
             const int s = l % STAGES;
             const unsigned parity = (unsigned)(l / STAGES) & 1u;
-            const bool ok = mbar_wait_bounded(&full[s], parity, kWaitCycles);
+            const bool ok = mbar_wait_bounded(&full[s], parity, wait_cycles);
             timed_out |= !ok;
             unsigned char* st = smem + s * STAGE;
             // the stage of frame f-1 takes frame f+STAGES-1 as soon as every warp
             // has released it
             if (tid == 0 && l >= 1 && l + STAGES - 1 < cnt) {
                 const int sp = (l - 1) % STAGES;
-                if (mbar_wait_bounded(&empty[sp], (unsigned)((l - 1) / STAGES) & 1u, kWaitCycles))
+                if (mbar_wait_bounded(&empty[sp], (unsigned)((l - 1) / STAGES) & 1u, wait_cycles))
                     issue(l + STAGES - 1);
                 else
                     timed_out = true;
@@ -277,7 +278,7 @@ __global__ void __launch_bounds__(NT, 3) motion_tma_kernel(const __grid_constant
                 // border tiles write the mirrored halo together (block barriers)
                 if (!__syncthreads_and(ok)) {
                     if (tid == 0 && a.err) atomicOr(a.err, 1);
-                    mbar_wait_bounded(&full[s], parity, kWaitCycles);
+                    mbar_wait_bounded(&full[s], parity, wait_cycles);
                     return false;
                 }
                 patch_mirror<Pix>(reinterpret_cast<Pix*>(st), a, x0, y0, pl, pr, pt, pb);
@@ -396,7 +397,7 @@ __global__ void __launch_bounds__(NT, 3) motion_tma_kernel(const __grid_constant
                 if (__syncthreads_or(timed_out)) {
                     // a stage wait ran out somewhere in the block: leave together
                     if (tid == 0 && a.err) atomicOr(a.err, 1);
-                    mbar_wait_bounded(&full[s], parity, kWaitCycles);
+                    mbar_wait_bounded(&full[s], parity, wait_cycles);
                     return false;
                 }
                 if (warp == 0) {
