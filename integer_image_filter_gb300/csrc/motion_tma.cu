@@ -19,11 +19,15 @@
 //    ("ADR-1392: CUDA motion, PSNR and moment kernels add one atomic per
 //    block, the motion SAD filters separably, ...", Decision 4).
 //  * Per frame each warp reduces its partial sums with one warp-reduce
-//    instruction, warp 0 combines the warps, and the block adds each
-//    accumulator to its 64-bit output with ONE atomic (same page, Decision 1;
-//    integer sums are order-independent, so the result is exact -- Context).
-//  * Every mbarrier wait is bounded: on time-out the CTA raises the device
-//    error word and leaves instead of spinning.
+//    instruction and keeps them in lane (frame mod 32); every 32 frames the
+//    warps add their lanes into the block's window sums in shared memory and
+//    the last warp adds each accumulator of each frame to its 64-bit output
+//    with ONE atomic (same page, Decision 1; integer sums are
+//    order-independent, so the result is exact -- Context).  No block-wide
+//    barrier is left in the frame loop of interior tiles.
+//  * Every mbarrier wait is bounded: on time-out a warp raises the device
+//    error word and leaves instead of spinning; thread 0 waits (bounded) for
+//    the copies it issued before the block exits.
 #include <cuda.h>
 
 #include <cmath>
@@ -150,16 +154,18 @@ __global__ void __launch_bounds__(NT, 3) motion_tma_kernel(const __grid_constant
     using G = Geo<Pix>;
     using Acc = typename SseAcc<Pix>::T;
     constexpr int STAGE = FUSED ? G::STAGE_FUSED : G::STAGE_MOTION;
-    constexpr int FLUSH = 8;           // frames between block reductions
-    constexpr int SLOTS = 2 * FLUSH;   // partial-sum slots (two flush windows)
     extern __shared__ __align__(128) unsigned char smem_raw[];
     // TMA destinations must sit on 128-byte boundaries; the launch adds 128 B of slack
     unsigned char* smem = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);
     __shared__ __align__(8) uint64_t full[STAGES];   // TMA bytes landed
     __shared__ __align__(8) uint64_t empty[STAGES];  // every warp done with the stage
-    // warp sums per frame (32-bit suffice for 8-bit samples: at most 512 x 255^2)
-    using Part = typename std::conditional<sizeof(Pix) == 1, uint32_t, unsigned long long>::type;
-    __shared__ __align__(16) Part part[SLOTS][NW][4];
+    // Block sums of a window of 32 frames, [window parity][accumulator][frame]:
+    // every warp adds its sums once per window, the last warp to do so adds
+    // them to the outputs (32 bits suffice for 8-bit samples: a tile's SAD is
+    // at most 4096 x 65280 and its luma SSE 4096 x 255^2).
+    using Win = typename std::conditional<sizeof(Pix) == 1, uint32_t, unsigned long long>::type;
+    __shared__ __align__(16) Win wsum[2][4][32];
+    __shared__ int wcount[2];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     // each warp owns output rows 4w .. 4w+3 of the tile; its V rows are private
@@ -188,7 +194,9 @@ __global__ void __launch_bounds__(NT, 3) motion_tma_kernel(const __grid_constant
             prefetch_tmap(&maps.rv);
             prefetch_tmap(&maps.dv);
         }
+        wcount[0] = wcount[1] = 0;
     }
+    for (int i = tid; i < 2 * 4 * 32; i += NT) (&wsum[0][0][0])[i] = 0;
     __syncthreads();
 
     // this CTA's frames: chunk blockIdx.z of the launch; a chunk after the
@@ -201,7 +209,9 @@ __global__ void __launch_bounds__(NT, 3) motion_tma_kernel(const __grid_constant
     const int cnt = f_end - first;
     const bool use_prev = !warm && a.has_prev;
 
+    int issued = 0;  // thread 0: frames issued so far
     auto issue = [&](int l) {  // thread 0 only; l = frame index within the chunk
+        issued = l + 1;
         const int s = l % STAGES;
         const int f = first + l;
         unsigned char* st = smem + s * STAGE;
@@ -252,20 +262,63 @@ __global__ void __launch_bounds__(NT, 3) motion_tma_kernel(const __grid_constant
     const int off_chroma = G::RAW_BYTES + G::DIST_BYTES +
                            ((2 * warp + (lane >> 4)) * G::CW + 4 * (lane & 15)) * G::S;
     bool timed_out = false;
+    // lane j holds the warp's sums of frame 32 m + j of the current window
+    uint32_t acc_s = 0;
+    [[maybe_unused]] Win acc_y = 0, acc_u = 0, acc_v = 0;
+    // End of a window of 32 frames (or of the chunk) at frame l: each warp adds
+    // its lanes to the block's window sums; the last warp to arrive adds them
+    // to the 64-bit outputs, one atomic per frame and accumulator (ADR-1392,
+    // Decision 1, with the atomics of 32 frames issued together) and clears
+    // them.  Warps are at most STAGES frames apart, so two windows suffice.
+    auto flush_window = [&](int l) {
+        const int jl = (l & ~31) + lane;   // this lane's frame
+        const bool v = jl <= l;
+        const int wb = (l >> 5) & 1;
+        if (v) {
+            atomicAdd(&wsum[wb][0][lane], (Win)acc_s);
+            if constexpr (FUSED) {
+                atomicAdd(&wsum[wb][1][lane], acc_y);
+                atomicAdd(&wsum[wb][2][lane], acc_u);
+                atomicAdd(&wsum[wb][3][lane], acc_v);
+            }
+        }
+        __syncwarp();
+        int last = 0;
+        if (lane == 0) {
+            __threadfence_block();
+            last = atomicAdd(&wcount[wb], 1) == NW - 1;
+        }
+        if (__shfl_sync(0xffffffffu, last, 0)) {
+            __threadfence_block();
+            if (v) {
+                const long long g = first + jl;
+                const unsigned long long t = atomicExch(&wsum[wb][0][lane], (Win)0);
+                if (t) atomicAdd(a.sad_out + g, t);
+                if constexpr (FUSED) {
+                    const unsigned long long ty = atomicExch(&wsum[wb][1][lane], (Win)0);
+                    const unsigned long long tu = atomicExch(&wsum[wb][2][lane], (Win)0);
+                    const unsigned long long tv = atomicExch(&wsum[wb][3][lane], (Win)0);
+                    if (ty) atomicAdd(a.sse_out + 3LL * g, ty);
+                    if (tu) atomicAdd(a.sse_out + 3LL * g + 1, tu);
+                    if (tv) atomicAdd(a.sse_out + 3LL * g + 2, tv);
+                }
+            }
+            if (lane == 0) wcount[wb] = 0;
+        }
+    };
 
     // The frame loop, compiled twice: for interior tiles (no mirror patch, no
-    // masks) and for tiles on the frame border.  A runtime test per frame
-    // costs the interior tiles several percent.
+    // masks, no block barrier) and for tiles on the frame border.  A runtime
+    // test per frame costs the interior tiles several percent.
     auto frames = [&](auto interior_tag) -> bool {
         constexpr bool INTERIOR = decltype(interior_tag)::value;
         for (int l = 0; l < cnt; ++l) {
-            const int f = first + l;   // frame index in the launch
             const int s = l % STAGES;
             const unsigned parity = (unsigned)(l / STAGES) & 1u;
             const bool ok = mbar_wait_bounded(&full[s], parity, wait_cycles);
             timed_out |= !ok;
             unsigned char* st = smem + s * STAGE;
-            // the stage of frame f-1 takes frame f+STAGES-1 as soon as every warp
+            // the stage of frame l-1 takes frame l+STAGES-1 as soon as every warp
             // has released it
             if (tid == 0 && l >= 1 && l + STAGES - 1 < cnt) {
                 const int sp = (l - 1) % STAGES;
@@ -274,11 +327,17 @@ __global__ void __launch_bounds__(NT, 3) motion_tma_kernel(const __grid_constant
                 else
                     timed_out = true;
             }
-            if (!INTERIOR && edge) {
+            if (INTERIOR || !edge) {
+                // a stage that never landed: this warp records it and leaves (the
+                // others then run out of stages and leave too)
+                if (__any_sync(0xffffffffu, !ok)) {
+                    if (lane == 0 && a.err) atomicOr(a.err, 1);
+                    return false;
+                }
+            } else {
                 // border tiles write the mirrored halo together (block barriers)
                 if (!__syncthreads_and(ok)) {
                     if (tid == 0 && a.err) atomicOr(a.err, 1);
-                    mbar_wait_bounded(&full[s], parity, wait_cycles);
                     return false;
                 }
                 patch_mirror<Pix>(reinterpret_cast<Pix*>(st), a, x0, y0, pl, pr, pt, pb);
@@ -295,11 +354,11 @@ __global__ void __launch_bounds__(NT, 3) motion_tma_kernel(const __grid_constant
             __syncwarp();
 
             // ---- horizontal pass, SAD against B_prev, squared errors
-            const bool do_out = l > 0 || !warm;          // not the warm-up frame
+            [[maybe_unused]] const bool do_out = l > 0 || !warm;   // not the warm-up frame
             const bool do_sad = l > 0 || use_prev;
             uint32_t sad = 0;
             [[maybe_unused]] Acc sse_y = 0, sse_u = 0, sse_v = 0;
-    #pragma unroll
+#pragma unroll
             for (int k = 0; k < 4; ++k) {
                 const uint32_t* v = sV + k * SVW + 4 * q;
                 const uint4 A = *reinterpret_cast<const uint4*>(v);
@@ -309,14 +368,14 @@ __global__ void __launch_bounds__(NT, 3) motion_tma_kernel(const __grid_constant
                 uint32_t b[4];
                 horizontal_quad(wv, b);
                 if (INTERIOR || full_tile) {
-    #pragma unroll
+#pragma unroll
                     for (int i = 0; i < 4; ++i) sad = __sad(b[i], bp[k][i], sad);
                 } else {
                     // an invalid sample compares with itself and adds 0
-    #pragma unroll
+#pragma unroll
                     for (int i = 0; i < 4; ++i) sad = __sad(b[i], i < nvalid[k] ? bp[k][i] : b[i], sad);
                 }
-    #pragma unroll
+#pragma unroll
                 for (int i = 0; i < 4; ++i) bp[k][i] = b[i];
                 if constexpr (FUSED) {
                     const Pix* dp = reinterpret_cast<const Pix*>(st + off_dist + k * TW * G::S);
@@ -329,7 +388,7 @@ __global__ void __launch_bounds__(NT, 3) motion_tma_kernel(const __grid_constant
                         uint32_t rf[4], ds[4];
                         unpack4(reinterpret_cast<const Pix*>(st + off_ref + k * G::RAW_W * G::S), rf);
                         unpack4(dp, ds);
-    #pragma unroll
+#pragma unroll
                         for (int i = 0; i < 4; ++i) {
                             const long long e = (long long)rf[i] - (long long)ds[i];
                             sse_y += (INTERIOR || i < nvalid[k]) ? (Acc)(e * e) : (Acc)0;
@@ -355,7 +414,7 @@ __global__ void __launch_bounds__(NT, 3) motion_tma_kernel(const __grid_constant
                     unpack4(reinterpret_cast<const Pix*>(sc + G::C_BYTES), du);
                     unpack4(reinterpret_cast<const Pix*>(sc + 2 * G::C_BYTES), rv);
                     unpack4(reinterpret_cast<const Pix*>(sc + 3 * G::C_BYTES), dv);
-    #pragma unroll
+#pragma unroll
                     for (int i = 0; i < 4; ++i) {
                         const long long eu = (long long)ru[i] - (long long)du[i];
                         const long long ev = (long long)rv[i] - (long long)dv[i];
@@ -368,55 +427,40 @@ __global__ void __launch_bounds__(NT, 3) motion_tma_kernel(const __grid_constant
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[s]);
 
-            // ---- warp sums of this frame into its slot; every FLUSH frames the
-            // block adds the slots to the outputs, one atomic per accumulator and
-            // frame (warp 0, lane = frame x accumulator)
-            {
-                const unsigned long long wsad = __reduce_add_sync(0xffffffffu, sad);
-                unsigned long long wy = 0, wu = 0, wvv = 0;
+            // ---- warp sums of this frame into lane l mod 32
+            const uint32_t wsad = __reduce_add_sync(0xffffffffu, sad);
+            [[maybe_unused]] Win wy = 0, wu = 0, wvv = 0;
+            if constexpr (FUSED) {
+                if constexpr (sizeof(Pix) == 1) {
+                    wy = __reduce_add_sync(0xffffffffu, sse_y);
+                    wu = __reduce_add_sync(0xffffffffu, sse_u);
+                    wvv = __reduce_add_sync(0xffffffffu, sse_v);
+                } else {
+                    wy = warp_sum(sse_y);
+                    wu = warp_sum(sse_u);
+                    wvv = warp_sum(sse_v);
+                }
+            }
+            if (lane == (l & 31)) {
+                acc_s = do_sad ? wsad : 0u;
                 if constexpr (FUSED) {
-                    if constexpr (sizeof(Pix) == 1) {
-                        wy = __reduce_add_sync(0xffffffffu, sse_y);
-                        wu = __reduce_add_sync(0xffffffffu, sse_u);
-                        wvv = __reduce_add_sync(0xffffffffu, sse_v);
-                    } else {
-                        wy = warp_sum(sse_y);
-                        wu = warp_sum(sse_u);
-                        wvv = warp_sum(sse_v);
-                    }
-                }
-                if (lane == 0) {
-                    Part* pp = &part[l & (SLOTS - 1)][warp][0];
-                    pp[0] = do_sad ? (Part)wsad : (Part)0;
-                    pp[1] = do_out ? (Part)wy : (Part)0;
-                    pp[2] = do_out ? (Part)wu : (Part)0;
-                    pp[3] = do_out ? (Part)wvv : (Part)0;
+                    acc_y = do_out ? wy : (Win)0;
+                    acc_u = do_out ? wu : (Win)0;
+                    acc_v = do_out ? wvv : (Win)0;
                 }
             }
-            if ((l & (FLUSH - 1)) == FLUSH - 1 || l == cnt - 1) {
-                if (__syncthreads_or(timed_out)) {
-                    // a stage wait ran out somewhere in the block: leave together
-                    if (tid == 0 && a.err) atomicOr(a.err, 1);
-                    mbar_wait_bounded(&full[s], parity, wait_cycles);
-                    return false;
-                }
-                if (warp == 0) {
-                    const int j = (l & ~(FLUSH - 1)) + (lane >> 2), acc = lane & 3;
-                    const bool j_out = j > 0 || !warm, j_sad = j > 0 || use_prev;
-                    if (j <= l && (acc == 0 ? j_sad : j_out) && (FUSED || acc == 0)) {
-                        unsigned long long t = 0;
-    #pragma unroll
-                        for (int w = 0; w < NW; ++w) t += part[j & (SLOTS - 1)][w][acc];
-                        const long long g = first + j;
-                        atomicAdd(acc == 0 ? a.sad_out + g : a.sse_out + 3LL * g + (acc - 1), t);
-                    }
-                }
-            }
+            if ((l & 31) == 31 || l == cnt - 1) flush_window(l);
         }
         return true;
     };
     const bool interior = full_tile && !edge;
     const bool alive = interior ? frames(std::true_type{}) : frames(std::false_type{});
+    if (tid == 0) {
+        // no copy may still be landing in this block's shared memory when it
+        // exits: wait (bounded) for the last phase of every stage issued
+        for (int m = issued - STAGES < 0 ? 0 : issued - STAGES; m < issued; ++m)
+            mbar_wait_bounded(&full[m % STAGES], (unsigned)(m / STAGES) & 1u, wait_cycles);
+    }
     if (!alive) return;
 
     if (a.store_last && cnt > 0 && f_end == a.n) {

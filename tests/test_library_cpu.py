@@ -114,8 +114,11 @@ def _kernel_sources():
             if f.endswith((".cu", ".cuh"))}
 
 
-# a single thread, or warp 0 whose lanes each own one (frame, accumulator)
-_GUARD = re.compile(r"if \((lane|tid|threadIdx\.x|warp) == \d")
+# a single thread, warp 0 whose lanes each own one (frame, accumulator), or
+# the last warp of the block to finish a window of frames, whose lanes each
+# own one frame
+_GUARD = re.compile(r"if \((lane|tid|threadIdx\.x|warp) == \d|if \(__shfl_sync\(0xffffffffu, last, 0\)\)")
+_SHARED = re.compile(r"__shared__[^;]*?\b(\w+)\[")
 
 
 def _single_lane_guarded(src: str, pos: int) -> bool:
@@ -147,12 +150,18 @@ def _single_lane_guarded(src: str, pos: int) -> bool:
 
 def contract_violations(src: str) -> list:
     """Checks in the spirit of a kernel source contract: no cluster multicast,
-    every atomic is a 64-bit add issued once per block per accumulator (inside
-    a lane-guarded branch), no runtime index into kernel-parameter arrays."""
+    every atomic on an output is a 64-bit add issued once per block per
+    accumulator (inside a lane-guarded branch; adds into the block's own
+    shared-memory sums are exempt), no runtime index into kernel-parameter
+    arrays."""
     bad = []
     if "multicast::cluster" in src:
         bad.append("cluster multicast")
+    shared = set(_SHARED.findall(src))
     for m in re.finditer(r"\batomicAdd\(([^;]*)\);", src):
+        target = re.match(r"\s*&(\w+)\[", m.group(1))
+        if target and target.group(1) in shared:
+            continue         # a block-local sum in shared memory, not an output
         if not _single_lane_guarded(src, m.start()):
             line_start = src.rfind("\n", 0, m.start()) + 1
             bad.append("atomic not guarded by a single lane: " + src[line_start:m.end()].strip())
@@ -172,6 +181,7 @@ def test_kernel_source_contract():
 @pytest.mark.parametrize("plant", [
     'asm("cp.async.bulk.tensor.2d.shared::cluster.global.multicast::cluster");',
     "    atomicAdd(a.sad_out + f, t0);",
+    "    __shared__ unsigned wsum[4];\n    atomicAdd(&out[f], t0);",
     "    const uint8_t* p = a.planes[plane];",
 ])
 def test_contract_catches_planted_regressions(plant):
