@@ -128,9 +128,11 @@ MOTION_API int motion_psnr_yuv420_batch(motion_ctx* ctx, int n,
  * chunks of pairs host->device into its own staging buffers (allocated on the
  * first call and kept; size them with motion_reserve_host_staging to keep the
  * first call allocation-free) on two streams so that copies overlap the
- * kernels, and copies the results back.  Blocks until h_sad_out (uint64[n])
- * and h_sse_out (uint64[n][3]) are written.  Host planes are tightly packed
- * with the given pitches and strides.  Pinned host memory recommended. */
+ * kernels, and copies the results back through a pinned result buffer the
+ * context keeps (grown to n pairs when a call needs more; the caller's result
+ * arrays may be pageable).  Blocks until h_sad_out (uint64[n]) and h_sse_out
+ * (uint64[n][3]) are written.  Host planes are tightly packed with the given
+ * pitches and strides.  Pinned host memory recommended for the pictures. */
 MOTION_API int motion_psnr_yuv420_batch_host(motion_ctx* ctx, int n,
                                   const void* h_ref_y, const void* h_ref_u,
                                   const void* h_ref_v, const void* h_dist_y,

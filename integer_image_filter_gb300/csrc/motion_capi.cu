@@ -82,6 +82,11 @@ struct motion_ctx {
     unsigned long long* d_res[2] = {nullptr, nullptr};
     cudaStream_t s_copy = nullptr, s_comp = nullptr;
     cudaEvent_t ev_in[2] = {nullptr, nullptr}, ev_done[2] = {nullptr, nullptr};
+    // pinned result staging of a host-buffer call (SAD + 3 SSE per pair), so
+    // that its device-to-host copies stay asynchronous and the next chunk's
+    // uploads are queued without waiting for this chunk's kernel
+    unsigned long long* h_res = nullptr;
+    size_t h_res_pairs = 0;
 };
 
 namespace {
@@ -107,6 +112,9 @@ void free_staging(motion_ctx* c) {
     if (c->s_comp) cudaStreamDestroy(c->s_comp);
     c->s_copy = c->s_comp = nullptr;
     c->stage_pairs = 0;
+    if (c->h_res) cudaFreeHost(c->h_res);
+    c->h_res = nullptr;
+    c->h_res_pairs = 0;
 }
 
 // The TMA kernel when the layout allows it, else the generic kernel.
@@ -345,6 +353,15 @@ int motion_psnr_yuv420_batch_host(motion_ctx* c, int n, const void* ry, const vo
         stride_uv < pitch_uv * (size_t)(c->ch - 1) + (size_t)c->cw * s)
         return MOTION_ERR_BAD_PITCH;  // host pairs must not overlap
     if ((rc = motion_reserve_host_staging(c, c->stage_pairs, stride_y, stride_uv))) return rc;
+    if (c->h_res_pairs < (size_t)n) {
+        if (c->h_res) cudaFreeHost(c->h_res);
+        c->h_res = nullptr;
+        c->h_res_pairs = 0;
+        MG_CUDA(cudaHostAlloc(&c->h_res, sizeof(unsigned long long) * 4 * (size_t)n, cudaHostAllocDefault));
+        c->h_res_pairs = (size_t)n;
+    }
+    unsigned long long* h_sad = c->h_res;
+    unsigned long long* h_sse = c->h_res + n;
     const int P = c->stage_pairs;
     const size_t ybytes = (size_t)P * stride_y, cbytes = (size_t)P * stride_uv;
     const void* src[6] = {ry, ru, rv, dy, du, dv};
@@ -378,13 +395,15 @@ int motion_psnr_yuv420_batch_host(motion_ctx* c, int n, const void* ry, const vo
         rc = launch_fused(c, m, dst[0], dst[1], dst[2], dst[3], dst[4], dst[5], pitch_y, pitch_uv,
                           stride_y, stride_uv, c->s_comp, d_sad, d_sse);
         if (rc) return rc;
-        MG_CUDA(cudaMemcpyAsync(h_sad_out + first, d_sad, sizeof(uint64_t) * (size_t)m,
+        MG_CUDA(cudaMemcpyAsync(h_sad + first, d_sad, sizeof(uint64_t) * (size_t)m,
                                 cudaMemcpyDeviceToHost, c->s_comp));
-        MG_CUDA(cudaMemcpyAsync(h_sse_out + 3 * (size_t)first, d_sse, sizeof(uint64_t) * 3 * (size_t)m,
+        MG_CUDA(cudaMemcpyAsync(h_sse + 3 * (size_t)first, d_sse, sizeof(uint64_t) * 3 * (size_t)m,
                                 cudaMemcpyDeviceToHost, c->s_comp));
         MG_CUDA(cudaEventRecord(c->ev_done[k], c->s_comp));
     }
     MG_CUDA(cudaStreamSynchronize(c->s_comp));
+    std::memcpy(h_sad_out, h_sad, sizeof(uint64_t) * (size_t)n);
+    std::memcpy(h_sse_out, h_sse, sizeof(uint64_t) * 3 * (size_t)n);
     return MOTION_OK;
 }
 

@@ -3,10 +3,10 @@
 // Tensor Memory Accelerator.
 //
 // Structure (GB300 / sm_103a):
-//  * One CTA owns a TW x TH output tile and walks the batch of frames in time
-//    order; B_prev of its tile stays in registers, so every frame is read from
-//    HBM once ("Making it fast: three rounds on one pipeline", Round 1 --
-//    one kernel over all frames).
+//  * One CTA owns a TW x TH output tile and walks the batch of frames (or one
+//    chunk of it) in time order; B_prev of its tile stays in registers, so
+//    every frame is read from HBM once ("Making it fast: three rounds on one
+//    pipeline", Round 1 -- one kernel over all frames).
 //  * Thread 0 keeps STAGES frames in flight: for each frame it issues 3-D tiled
 //    TMA loads (cp.async.bulk.tensor, x / y / frame coordinates) of the luma
 //    box with its 2-row and 16-byte halo -- and, fused, the distorted luma
@@ -41,7 +41,7 @@ namespace mg {
 constexpr long long kWaitCycles = 1LL << 31;  // default wait bound: about one second
 
 // Mirror the halo of a staged luma box in place for tiles on the frame border.
-template <typename Pix>
+template <typename Pix, int NTK>
 __device__ __forceinline__ void patch_mirror(Pix* raw, const TileArgs& a, int x0, int y0,
                                              bool pl, bool pr, bool pt, bool pb) {
     using G = Geo<Pix>;
@@ -49,7 +49,7 @@ __device__ __forceinline__ void patch_mirror(Pix* raw, const TileArgs& a, int x0
     // columns first (every staged row), then whole rows (so corners follow)
     if (pl || pr) {
         const int cw0 = a.w - x0 + G::HX;  // staged column of x = w
-        for (int i = tid; i < 4 * G::RAW_ROWS; i += NT) {
+        for (int i = tid; i < 4 * G::RAW_ROWS; i += NTK) {
             const int r = i >> 2, which = i & 3;
             Pix* row = raw + r * G::RAW_W;
             if (which < 2) {
@@ -63,7 +63,7 @@ __device__ __forceinline__ void patch_mirror(Pix* raw, const TileArgs& a, int x0
     }
     if (pt || pb) {
         const int rh = a.h - y0 + 2;      // staged row of y = h
-        for (int i = tid; i < 4 * G::RAW_W; i += NT) {
+        for (int i = tid; i < 4 * G::RAW_W; i += NTK) {
             const int which = i / G::RAW_W, c = i - which * G::RAW_W;
             if (which < 2) {
                 if (pt) raw[(1 - which) * G::RAW_W + c] = raw[(3 + which) * G::RAW_W + c];  // y=-1,-2 <- 1,2
@@ -78,8 +78,8 @@ __device__ __forceinline__ void patch_mirror(Pix* raw, const TileArgs& a, int x0
     fence_proxy_async();
 }
 
-// The vertical 5-tap pass for one warp: 4 output rows (staged rows 4w..4w+7
-// feed them) x 128 columns, lane = quad of 4 columns; result V (uint32) into
+// The vertical 5-tap pass for one warp: 4 output rows (8 staged rows from
+// src feed them) x 128 columns, lane = quad of 4 columns; result V (uint32) into
 // the warp's own rows of sV, and the 4 centre-row words (the reference luma
 // of the warp's output rows) for the squared error.  8-bit samples use
 // byte-pair dot products: rows are interleaved two at a time so that one dp2a
@@ -148,10 +148,28 @@ __device__ __forceinline__ void horizontal_quad(const uint32_t (&wv)[12], uint32
     }
 }
 
+// Thread layout: each warp owns RPW = 8 output rows of the tile and runs them
+// in two halves of 4 rows through its own 4-row V buffer; 4 warps cover the
+// 32 rows.  Eight rows per warp halve the per-frame cost of stage waits,
+// reductions and loop control per pixel against four, and the 32 halo
+// values of a warp's rows then occupy every lane once.
+struct Shape {
+    static constexpr int RPW = 8;                 // output rows per warp
+    static constexpr int NWK = TH / RPW;          // warps per CTA
+    static constexpr int NTK = NWK * 32;          // threads per CTA
+    static constexpr int MINB = 4;                // resident CTAs per SM (<= 128 registers)
+    static constexpr int SV = NWK * 4 * SVW * 4;  // V buffers, bytes
+    static constexpr int CRW = 16 / NWK;          // chroma rows per warp
+    static constexpr int SPL = RPW;               // chroma samples per lane and plane
+    static constexpr int LPR = 64 / SPL;          // lanes per chroma row
+};
+
 template <typename Pix, bool FUSED, int STAGES>
-__global__ void __launch_bounds__(NT, 3) motion_tma_kernel(const __grid_constant__ TmaMaps maps,
-                                                            const TileArgs a) {
+__global__ void __launch_bounds__(Shape::NTK, Shape::MINB)
+    motion_tma_kernel(const __grid_constant__ TmaMaps maps, const TileArgs a) {
     using G = Geo<Pix>;
+    using SH = Shape;
+    constexpr int NWK = SH::NWK, NTK = SH::NTK, RPW = SH::RPW;
     using Acc = typename SseAcc<Pix>::T;
     constexpr int STAGE = FUSED ? G::STAGE_FUSED : G::STAGE_MOTION;
     extern __shared__ __align__(128) unsigned char smem_raw[];
@@ -168,7 +186,7 @@ __global__ void __launch_bounds__(NT, 3) motion_tma_kernel(const __grid_constant
     __shared__ int wcount[2];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    // each warp owns output rows 4w .. 4w+3 of the tile; its V rows are private
+    // each warp owns output rows RPW w .. RPW w + RPW-1 of the tile; its V rows are private
     uint32_t* sV = reinterpret_cast<uint32_t*>(smem + STAGES * STAGE) + warp * 4 * SVW;
     const int x0 = blockIdx.x * TW, y0 = blockIdx.y * TH;
     const bool full_tile = (x0 + TW <= a.w) && (y0 + TH <= a.h);
@@ -183,7 +201,7 @@ __global__ void __launch_bounds__(NT, 3) motion_tma_kernel(const __grid_constant
 #pragma unroll
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], NW);
+            mbar_init(&empty[s], NWK);
         }
         fence_mbar_init();
         prefetch_tmap(&maps.raw);
@@ -196,7 +214,7 @@ __global__ void __launch_bounds__(NT, 3) motion_tma_kernel(const __grid_constant
         }
         wcount[0] = wcount[1] = 0;
     }
-    for (int i = tid; i < 2 * 4 * 32; i += NT) (&wsum[0][0][0])[i] = 0;
+    for (int i = tid; i < 2 * 4 * 32; i += NTK) (&wsum[0][0][0])[i] = 0;
     __syncthreads();
 
     // this CTA's frames: chunk blockIdx.z of the launch; a chunk after the
@@ -233,12 +251,12 @@ __global__ void __launch_bounds__(NT, 3) motion_tma_kernel(const __grid_constant
         for (int l = 0; l < pre; ++l) issue(l);
     }
 
-    // this thread's outputs: rows 4w + k, columns 4q .. 4q+3 (q = lane)
+    // this thread's outputs: rows RPW w + k, columns 4q .. 4q+3 (q = lane)
     const int q = lane;
-    uint32_t bp[4][4];
+    uint32_t bp[RPW][4];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        const int y = y0 + 4 * warp + k;
+    for (int k = 0; k < RPW; ++k) {
+        const int y = y0 + RPW * warp + k;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const int x = x0 + 4 * q + i;
@@ -246,21 +264,21 @@ __global__ void __launch_bounds__(NT, 3) motion_tma_kernel(const __grid_constant
         }
     }
     // valid columns of this thread's quad in each of its rows (edge tiles)
-    int nvalid[4];
+    int nvalid[RPW];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        int nv = (y0 + 4 * warp + k < a.h) ? a.w - (x0 + 4 * q) : 0;
+    for (int k = 0; k < RPW; ++k) {
+        int nv = (y0 + RPW * warp + k < a.h) ? a.w - (x0 + 4 * q) : 0;
         nvalid[k] = nv < 0 ? 0 : (nv > 4 ? 4 : nv);
     }
     // per-thread byte offsets inside a stage (the same for every stage)
-    const int off_vsrc = ((warp * 4) * G::RAW_W + G::HX + 4 * lane) * G::S;
-    const int halo_r = (lane >> 2) & 3, halo_which = lane & 3;
+    const int off_vsrc = ((warp * RPW) * G::RAW_W + G::HX + 4 * lane) * G::S;  // half h: + 4h rows
+    const int halo_r = lane >> 2, halo_which = lane & 3;   // halo row 0..7, column
     const int halo_off = halo_which == 0 ? -2 : halo_which == 1 ? -1 : halo_which == 2 ? TW : TW + 1;
-    const int off_halo = ((warp * 4 + halo_r) * G::RAW_W + G::HX + halo_off) * G::S;
-    const int off_ref = ((4 * warp + 2) * G::RAW_W + G::HX + 4 * q) * G::S;   // row k: + k RAW_W S
-    const int off_dist = G::RAW_BYTES + ((4 * warp) * TW + 4 * q) * G::S;     // row k: + k TW S
+    const int off_halo = ((warp * RPW + halo_r) * G::RAW_W + G::HX + halo_off) * G::S;
+    const int off_ref = ((RPW * warp + 2) * G::RAW_W + G::HX + 4 * q) * G::S;   // row k: + k RAW_W S
+    const int off_dist = G::RAW_BYTES + ((RPW * warp) * TW + 4 * q) * G::S;     // row k: + k TW S
     const int off_chroma = G::RAW_BYTES + G::DIST_BYTES +
-                           ((2 * warp + (lane >> 4)) * G::CW + 4 * (lane & 15)) * G::S;
+                           ((SH::CRW * warp + lane / SH::LPR) * G::CW + SH::SPL * (lane % SH::LPR)) * G::S;
     bool timed_out = false;
     // lane j holds the warp's sums of frame 32 m + j of the current window
     uint32_t acc_s = 0;
@@ -286,7 +304,7 @@ __global__ void __launch_bounds__(NT, 3) motion_tma_kernel(const __grid_constant
         int last = 0;
         if (lane == 0) {
             __threadfence_block();
-            last = atomicAdd(&wcount[wb], 1) == NW - 1;
+            last = atomicAdd(&wcount[wb], 1) == NWK - 1;
         }
         if (__shfl_sync(0xffffffffu, last, 0)) {
             __threadfence_block();
@@ -340,86 +358,99 @@ __global__ void __launch_bounds__(NT, 3) motion_tma_kernel(const __grid_constant
                     if (tid == 0 && a.err) atomicOr(a.err, 1);
                     return false;
                 }
-                patch_mirror<Pix>(reinterpret_cast<Pix*>(st), a, x0, y0, pl, pr, pt, pb);
+                patch_mirror<Pix, NTK>(reinterpret_cast<Pix*>(st), a, x0, y0, pl, pr, pt, pb);
             }
 
-            // ---- vertical pass of the warp's 4 rows (staged row r <-> y0 - 2 + r)
-            uint32_t center[4];
-            vertical_quad(reinterpret_cast<const Pix*>(st + off_vsrc), sV + 4 + 4 * lane, rnd, sh, center);
-            if (lane < 16) {  // the two halo columns on each side, 4 rows
+            // ---- halo columns (two on each side) of the warp's rows: lane = (row, column)
+            uint32_t hv = 0;
+            {
                 const Pix* c = reinterpret_cast<const Pix*>(st + off_halo);
-                sV[halo_r * SVW + 4 + halo_off] = vtap(c[0], c[G::RAW_W], c[2 * G::RAW_W],
-                                                       c[3 * G::RAW_W], c[4 * G::RAW_W], rnd, sh);
+                hv = vtap(c[0], c[G::RAW_W], c[2 * G::RAW_W], c[3 * G::RAW_W], c[4 * G::RAW_W], rnd, sh);
             }
-            __syncwarp();
-
-            // ---- horizontal pass, SAD against B_prev, squared errors
             [[maybe_unused]] const bool do_out = l > 0 || !warm;   // not the warm-up frame
             const bool do_sad = l > 0 || use_prev;
             uint32_t sad = 0;
             [[maybe_unused]] Acc sse_y = 0, sse_u = 0, sse_v = 0;
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const uint32_t* v = sV + k * SVW + 4 * q;
-                const uint4 A = *reinterpret_cast<const uint4*>(v);
-                const uint4 Bq = *reinterpret_cast<const uint4*>(v + 4);
-                const uint4 C = *reinterpret_cast<const uint4*>(v + 8);
-                const uint32_t wv[12] = {A.x, A.y, A.z, A.w, Bq.x, Bq.y, Bq.z, Bq.w, C.x, C.y, C.z, C.w};
-                uint32_t b[4];
-                horizontal_quad(wv, b);
-                if (INTERIOR || full_tile) {
+            for (int h = 0; h < RPW / 4; ++h) {
+                if (h > 0) __syncwarp();   // the previous half has read the V rows
+                // ---- vertical pass of 4 rows (staged row r <-> y0 - 2 + r)
+                uint32_t center[4];
+                vertical_quad(reinterpret_cast<const Pix*>(st + off_vsrc + h * 4 * G::RAW_W * G::S),
+                              sV + 4 + 4 * lane, rnd, sh, center);
+                if ((halo_r >> 2) == h)
+                    sV[(halo_r & 3) * SVW + 4 + halo_off] = hv;
+                __syncwarp();
+
+                // ---- horizontal pass, SAD against B_prev, squared errors
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) sad = __sad(b[i], bp[k][i], sad);
-                } else {
-                    // an invalid sample compares with itself and adds 0
+                for (int kk = 0; kk < 4; ++kk) {
+                    const int k = 4 * h + kk;
+                    const uint32_t* v = sV + kk * SVW + 4 * q;
+                    const uint4 A = *reinterpret_cast<const uint4*>(v);
+                    const uint4 Bq = *reinterpret_cast<const uint4*>(v + 4);
+                    const uint4 C = *reinterpret_cast<const uint4*>(v + 8);
+                    const uint32_t wv[12] = {A.x, A.y, A.z, A.w, Bq.x, Bq.y, Bq.z, Bq.w, C.x, C.y, C.z, C.w};
+                    uint32_t b[4];
+                    horizontal_quad(wv, b);
+                    if (INTERIOR || full_tile) {
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) sad = __sad(b[i], i < nvalid[k] ? bp[k][i] : b[i], sad);
-                }
-#pragma unroll
-                for (int i = 0; i < 4; ++i) bp[k][i] = b[i];
-                if constexpr (FUSED) {
-                    const Pix* dp = reinterpret_cast<const Pix*>(st + off_dist + k * TW * G::S);
-                    if constexpr (sizeof(Pix) == 1) {
-                        uint32_t d = __vabsdiffu4(center[k], *reinterpret_cast<const uint32_t*>(dp));
-                        if (!INTERIOR && !full_tile)
-                            d &= nvalid[k] <= 0 ? 0u : (0xffffffffu >> (8 * (4 - nvalid[k])));
-                        sse_y = __dp4a(d, d, sse_y);
+                        for (int i = 0; i < 4; ++i) sad = __sad(b[i], bp[k][i], sad);
                     } else {
-                        uint32_t rf[4], ds[4];
-                        unpack4(reinterpret_cast<const Pix*>(st + off_ref + k * G::RAW_W * G::S), rf);
-                        unpack4(dp, ds);
+                        // an invalid sample compares with itself and adds 0
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            const long long e = (long long)rf[i] - (long long)ds[i];
-                            sse_y += (INTERIOR || i < nvalid[k]) ? (Acc)(e * e) : (Acc)0;
+                        for (int i = 0; i < 4; ++i) sad = __sad(b[i], i < nvalid[k] ? bp[k][i] : b[i], sad);
+                    }
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) bp[k][i] = b[i];
+                    if constexpr (FUSED) {
+                        const Pix* dp = reinterpret_cast<const Pix*>(st + off_dist + k * TW * G::S);
+                        if constexpr (sizeof(Pix) == 1) {
+                            uint32_t d = __vabsdiffu4(center[kk], *reinterpret_cast<const uint32_t*>(dp));
+                            if (!INTERIOR && !full_tile)
+                                d &= nvalid[k] <= 0 ? 0u : (0xffffffffu >> (8 * (4 - nvalid[k])));
+                            sse_y = __dp4a(d, d, sse_y);
+                        } else {
+                            uint32_t rf[4], ds[4];
+                            unpack4(reinterpret_cast<const Pix*>(st + off_ref + k * G::RAW_W * G::S), rf);
+                            unpack4(dp, ds);
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                const long long e = (long long)rf[i] - (long long)ds[i];
+                                sse_y += (INTERIOR || i < nvalid[k]) ? (Acc)(e * e) : (Acc)0;
+                            }
                         }
                     }
                 }
             }
             if constexpr (FUSED) {
                 // 4:2:0 chroma: 16 rows x 64 columns per plane; warp w takes rows
-                // 2w, 2w+1, 4 samples per lane; outside the picture both sides were
-                // zero-filled, so they add 0
+                // CRW w .. CRW w + CRW-1, SPL samples per lane; outside the picture
+                // both sides were zero-filled, so they add 0
                 const unsigned char* sc = st + off_chroma;
-                if constexpr (sizeof(Pix) == 1) {
-                    const uint32_t du = __vabsdiffu4(*reinterpret_cast<const uint32_t*>(sc),
-                                                     *reinterpret_cast<const uint32_t*>(sc + G::C_BYTES));
-                    const uint32_t dv = __vabsdiffu4(*reinterpret_cast<const uint32_t*>(sc + 2 * G::C_BYTES),
-                                                     *reinterpret_cast<const uint32_t*>(sc + 3 * G::C_BYTES));
-                    sse_u = __dp4a(du, du, 0u);
-                    sse_v = __dp4a(dv, dv, 0u);
-                } else {
-                    uint32_t ru[4], du[4], rv[4], dv[4];
-                    unpack4(reinterpret_cast<const Pix*>(sc), ru);
-                    unpack4(reinterpret_cast<const Pix*>(sc + G::C_BYTES), du);
-                    unpack4(reinterpret_cast<const Pix*>(sc + 2 * G::C_BYTES), rv);
-                    unpack4(reinterpret_cast<const Pix*>(sc + 3 * G::C_BYTES), dv);
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const long long eu = (long long)ru[i] - (long long)du[i];
-                        const long long ev = (long long)rv[i] - (long long)dv[i];
-                        sse_u += (Acc)(eu * eu);
-                        sse_v += (Acc)(ev * ev);
+                for (int j = 0; j < SH::SPL / 4; ++j) {
+                    const unsigned char* cj = sc + 4 * j * G::S;
+                    if constexpr (sizeof(Pix) == 1) {
+                        const uint32_t du = __vabsdiffu4(*reinterpret_cast<const uint32_t*>(cj),
+                                                         *reinterpret_cast<const uint32_t*>(cj + G::C_BYTES));
+                        const uint32_t dv = __vabsdiffu4(*reinterpret_cast<const uint32_t*>(cj + 2 * G::C_BYTES),
+                                                         *reinterpret_cast<const uint32_t*>(cj + 3 * G::C_BYTES));
+                        sse_u = __dp4a(du, du, sse_u);
+                        sse_v = __dp4a(dv, dv, sse_v);
+                    } else {
+                        uint32_t ru[4], du[4], rv[4], dv[4];
+                        unpack4(reinterpret_cast<const Pix*>(cj), ru);
+                        unpack4(reinterpret_cast<const Pix*>(cj + G::C_BYTES), du);
+                        unpack4(reinterpret_cast<const Pix*>(cj + 2 * G::C_BYTES), rv);
+                        unpack4(reinterpret_cast<const Pix*>(cj + 3 * G::C_BYTES), dv);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const long long eu = (long long)ru[i] - (long long)du[i];
+                            const long long ev = (long long)rv[i] - (long long)dv[i];
+                            sse_u += (Acc)(eu * eu);
+                            sse_v += (Acc)(ev * ev);
+                        }
                     }
                 }
             }
@@ -465,8 +496,8 @@ __global__ void __launch_bounds__(NT, 3) motion_tma_kernel(const __grid_constant
 
     if (a.store_last && cnt > 0 && f_end == a.n) {
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const int y = y0 + 4 * warp + k;
+        for (int k = 0; k < RPW; ++k) {
+            const int y = y0 + RPW * warp + k;
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const int x = x0 + 4 * q + i;
@@ -514,7 +545,7 @@ template <typename Pix, bool FUSED, int STAGES>
 cudaError_t launch_tma_one(const TmaMaps& maps, const TileArgs& a, cudaStream_t s) {
     using G = Geo<Pix>;
     constexpr int STAGE = FUSED ? G::STAGE_FUSED : G::STAGE_MOTION;
-    constexpr int SMEM = STAGES * STAGE + G::SV_BYTES + 128;
+    constexpr int SMEM = STAGES * STAGE + Shape::SV + 128;
     static unsigned long long configured = 0;  // per device bit
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -527,14 +558,16 @@ cudaError_t launch_tma_one(const TmaMaps& maps, const TileArgs& a, cudaStream_t 
         __atomic_fetch_or(&configured, bit, __ATOMIC_RELEASE);
     }
     // Size the launch by the SM count (ADR-1226): split the frames into
-    // chunks so that tiles x chunks fill whole waves of resident CTAs, each
-    // chunk after the first paying one warm-up frame.
+    // chunks so that tiles x chunks fill whole waves of resident CTAs.  A
+    // chunk after the first pays one warm-up frame and every chunk its own
+    // pipeline fill (about half a frame), so the split is chosen by
+    //   cost(c) = (n + (c - 1) + c / 2) / n / (waves / ceil(waves)).
     static int slots_per_sm[64] = {0};
     int& spm = slots_per_sm[dev & 63];
     if (spm == 0) {
         int per_sm = 0, sms = 0;
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, motion_tma_kernel<Pix, FUSED, STAGES>,
-                                                          NT, SMEM);
+                                                          Shape::NTK, SMEM);
         if (e != cudaSuccess) return e;
         e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return e;
@@ -545,18 +578,16 @@ cudaError_t launch_tma_one(const TmaMaps& maps, const TileArgs& a, cudaStream_t 
     int best_c = 1;
     double best = 1e30;
     // a launch that reads and writes the same resident plane keeps one chunk:
-    // the last chunk's store must not overtake the first chunk's read.  A
-    // grid that already fills 1.5 waves stays whole as well: every chunk pays
-    // its own pipeline fill, which costs more than the partial last wave.
+    // the last chunk's store must not overtake the first chunk's read
     const bool same_plane = a.has_prev && a.bprev == a.bprev_out;
-    const int max_c = (same_plane || tiles * 2 >= 3LL * spm) ? 1 : 8;
+    const int max_c = same_plane ? 1 : 8;
     for (int c = 1; c <= max_c && c <= a.n; ++c) {
         const int len = (a.n + c - 1) / c;
         const int cz = (a.n + len - 1) / len;
         const double units = (double)tiles * cz;
         const double waves = units / spm;
         const double fill = waves / std::ceil(waves);
-        const double work = (double)(a.n + cz - 1) / a.n;
+        const double work = (a.n + (cz - 1) + 0.5 * cz) / a.n;
         const double cost = work / fill;
         if (cost < best - 1e-9) {
             best = cost;
@@ -565,7 +596,7 @@ cudaError_t launch_tma_one(const TmaMaps& maps, const TileArgs& a, cudaStream_t 
     }
     b.chunk = (a.n + best_c - 1) / best_c;
     dim3 grid((a.w + TW - 1) / TW, (a.h + TH - 1) / TH, (a.n + b.chunk - 1) / b.chunk);
-    motion_tma_kernel<Pix, FUSED, STAGES><<<grid, NT, SMEM, s>>>(maps, b);
+    motion_tma_kernel<Pix, FUSED, STAGES><<<grid, Shape::NTK, SMEM, s>>>(maps, b);
     return cudaGetLastError();
 }
 
@@ -602,10 +633,11 @@ cudaError_t launch_motion_tma(const TileArgs& a, bool fused, cudaStream_t s, int
     if (!ok) return cudaSuccess;  // the caller falls back to the generic kernel
     *used = true;
     *launches += 1;
+    // stages per CTA: as many as keep 4 CTAs (3 for 16-bit pairs) resident
     if (S == 1)
-        return fused ? launch_tma_one<uint8_t, true, 4>(maps, a, s)
+        return fused ? launch_tma_one<uint8_t, true, 3>(maps, a, s)
                      : launch_tma_one<uint8_t, false, 4>(maps, a, s);
-    return fused ? launch_tma_one<uint16_t, true, 3>(maps, a, s)
+    return fused ? launch_tma_one<uint16_t, true, 2>(maps, a, s)
                  : launch_tma_one<uint16_t, false, 4>(maps, a, s);
 }
 

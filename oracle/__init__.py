@@ -19,7 +19,10 @@ Pins (checked by ``tests/test_oracle_pins.py`` against the mathematics, not
 against this code): constant-frame and two-constant closed forms, impulse closed
 form, row- and column-constant frames against numpy/scipy mirror-padded
 convolution, the hand-worked 6x6 example, brute-force 25-MAC per-output loop on
-tiny frames, SAD/SSE invariants and planted-mistake builds.  The PSNR dB helper
+tiny frames, SAD/SSE invariants and planted-mistake builds; moment sums against
+closed forms and numpy sums; the motion_v2 difference blur against the pinned
+reading-A blur (non-negative differences), closed forms, a floor-rounding impulse
+worked by hand and the brute-force per-output loop.  The PSNR dB helper
 ``psnr_db`` is "parity unpinned" (no page gives its formula; it is not graded).
 """
 from __future__ import annotations
@@ -72,6 +75,17 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.oracle_scores.argtypes = [P, ctypes.c_int, ctypes.c_int, ctypes.c_int, P,
                                   P, P]
     lib.oracle_scores.restype = ctypes.c_int
+    lib.oracle_moment_sums.argtypes = [P, P, ctypes.c_int, ctypes.c_int, ctypes.c_size_t,
+                                       ctypes.c_size_t, ctypes.c_int, P]
+    lib.oracle_moment_sums.restype = ctypes.c_int
+    lib.oracle_moments.argtypes = [P, ctypes.c_int, ctypes.c_int, ctypes.c_int, P]
+    lib.oracle_moments.restype = ctypes.c_int
+    lib.oracle_blur_diff.argtypes = [P, P, ctypes.c_int, ctypes.c_int, ctypes.c_size_t,
+                                     ctypes.c_int, P]
+    lib.oracle_blur_diff.restype = ctypes.c_int
+    lib.oracle_motion_v2_sequence.argtypes = [P, ctypes.c_int, ctypes.c_size_t, ctypes.c_int,
+                                              ctypes.c_int, ctypes.c_size_t, ctypes.c_int, P]
+    lib.oracle_motion_v2_sequence.restype = ctypes.c_int
     return lib
 
 
@@ -172,6 +186,76 @@ class Oracle:
         if rc != 0:
             raise ValueError("oracle_scores rejected its arguments")
         return score, motion2
+
+
+def _pair(ref: np.ndarray, dist: np.ndarray) -> tuple[np.ndarray, np.ndarray]:
+    if ref.shape != dist.shape or ref.ndim != 2:
+        raise ValueError("ref and dist must be equal-shape 2-D planes")
+    if ref.strides[1] != ref.itemsize:
+        ref = np.ascontiguousarray(ref)
+    if dist.strides[1] != dist.itemsize:
+        dist = np.ascontiguousarray(dist)
+    return ref, dist
+
+
+def _moment_sums(self, ref: np.ndarray, dist: np.ndarray, bpc: int) -> np.ndarray:
+    """uint64[4]: sum ref, sum dist, sum ref^2, sum dist^2 of one luma pair."""
+    r, d = _pair(self._frames(ref, bpc), self._frames(dist, bpc))
+    h, w = r.shape
+    out = np.zeros(4, dtype=np.uint64)
+    rc = self.lib.oracle_moment_sums(r.ctypes.data, d.ctypes.data, w, h, r.strides[0],
+                                     d.strides[0], bpc, out.ctypes.data)
+    if rc != 0:
+        raise ValueError("oracle_moment_sums rejected its arguments")
+    return out
+
+
+def _moments(self, sums: np.ndarray, w: int, h: int) -> np.ndarray:
+    """float64[n][4] moments (sums over w*h) from uint64[n][4] moment sums."""
+    s = np.ascontiguousarray(sums, dtype=np.uint64).reshape(-1, 4)
+    out = np.zeros(s.shape, dtype=np.float64)
+    rc = self.lib.oracle_moments(s.ctypes.data, s.shape[0], w, h, out.ctypes.data)
+    if rc != 0:
+        raise ValueError("oracle_moments rejected its arguments")
+    return out
+
+
+def _blur_diff(self, prev: np.ndarray, cur: np.ndarray, bpc: int) -> np.ndarray:
+    """motion_v2 blur (h x w int32) of prev - cur."""
+    p = np.ascontiguousarray(self._frames(prev, bpc))
+    c = np.ascontiguousarray(self._frames(cur, bpc))
+    if p.shape != c.shape or p.ndim != 2:
+        raise ValueError("prev and cur must be equal-shape 2-D frames")
+    h, w = p.shape
+    out = np.empty((h, w), dtype=np.int32)
+    rc = self.lib.oracle_blur_diff(p.ctypes.data, c.ctypes.data, w, h, p.strides[0], bpc,
+                                   out.ctypes.data)
+    if rc != 0:
+        raise ValueError(f"oracle_blur_diff rejected w={w} h={h} bpc={bpc}")
+    return out
+
+
+def _motion_v2_sequence(self, frames: np.ndarray, bpc: int) -> np.ndarray:
+    """frames: (n, h, w).  Returns uint64[n] motion_v2 SADs, SAD[0] = 0."""
+    f = self._frames(frames, bpc)
+    if f.ndim != 3:
+        raise ValueError("frames must be (n, h, w)")
+    f = np.ascontiguousarray(f)
+    n, h, w = f.shape
+    out = np.zeros(n, dtype=np.uint64)
+    if n == 0:
+        return out
+    rc = self.lib.oracle_motion_v2_sequence(f.ctypes.data, n, f.strides[0], w, h, f.strides[1],
+                                            bpc, out.ctypes.data)
+    if rc != 0:
+        raise ValueError(f"oracle_motion_v2_sequence rejected w={w} h={h} bpc={bpc}")
+    return out
+
+
+Oracle.moment_sums = _moment_sums
+Oracle.moments = _moments
+Oracle.blur_diff = _blur_diff
+Oracle.motion_v2_sequence = _motion_v2_sequence
 
 
 def psnr_db(sse: int, n_samples: int, bpc: int) -> float:

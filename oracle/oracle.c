@@ -32,6 +32,18 @@
  *
  * Arithmetic: every sum is exact in uint32 for sample values < 2^16
  * (65535 * 65536 + 2^15 < 2^32); SAD and SSE accumulate in uint64.
+ *
+ * Two further quantities of the same page:
+ *   - Moment sums [ADR-1392, Decision 6 and Context]: for a picture pair, the
+ *     sums of the reference and distorted luma samples and of their squares,
+ *     four exact uint64 accumulators; the moments are those sums over the
+ *     sample count (mean and mean square), in double.
+ *   - motion_v2 [ADR-1392, Decision 4]: the separable blur applied to the
+ *     signed difference prev - cur of two consecutive frames, with the same
+ *     taps, mirror and rounding constants; a right shift of a negative sum
+ *     rounds towards minus infinity (floor), and the SAD is the sum of the
+ *     absolute blurred values.  Sums need 33 bits with sign, so the
+ *     arithmetic is int64 here.
  */
 #include <stdint.h>
 #include <stdlib.h>
@@ -224,4 +236,144 @@ ORACLE_API int oracle_scores(const uint64_t* sad, int n, int w, int h,
         motion2[i] = has_next ? (score[i] < nxt ? score[i] : nxt) : score[i];
     }
     return 0;
+}
+
+/*
+ * Moment sums of one picture pair [ADR-1392, Decision 6: four accumulators,
+ * the reference and distorted sums and sums of squares; Context: exact 64-bit
+ * integer sums].  out[0] = sum ref, out[1] = sum dist, out[2] = sum ref^2,
+ * out[3] = sum dist^2.  Returns 0, or -1 on a bad argument.
+ */
+ORACLE_API int oracle_moment_sums(const void* ref, const void* dist, int w, int h,
+                                  size_t ref_pitch, size_t dist_pitch, int bpc,
+                                  uint64_t* out)
+{
+    if (!ref || !dist || !out || w <= 0 || h <= 0 || bpc < 8 || bpc > 16) return -1;
+    const unsigned char* r = (const unsigned char*)ref;
+    const unsigned char* d = (const unsigned char*)dist;
+    uint64_t s_r = 0, s_d = 0, q_r = 0, q_d = 0;
+#if defined(ORACLE_PLANT_MOMENT_SKIP_LAST_ROW)
+    h -= 1;   /* planted mistake (tests only): the last row is left out */
+#endif
+    for (int y = 0; y < h; ++y) {
+        for (int x = 0; x < w; ++x) {
+            const uint64_t a = sample_at(r, ref_pitch, bpc, y, x);
+            const uint64_t b = sample_at(d, dist_pitch, bpc, y, x);
+            s_r += a;
+            s_d += b;
+            q_r += a * a;
+#if defined(ORACLE_PLANT_MOMENT_SQUARE_OF_REF)
+            q_d += a * a;   /* planted mistake (tests only): ref squared twice */
+#else
+            q_d += b * b;
+#endif
+        }
+    }
+    out[0] = s_r;
+    out[1] = s_d;
+    out[2] = q_r;
+    out[3] = q_d;
+    return 0;
+}
+
+/*
+ * Moments from moment sums, in double: each sum over the sample count w*h
+ * (the first moments are the means, the second the mean squares).
+ */
+ORACLE_API int oracle_moments(const uint64_t* sums, int n, int w, int h, double* out)
+{
+    if (n < 0 || (n > 0 && (!sums || !out)) || w <= 0 || h <= 0) return -1;
+    const double count = (double)w * (double)h;
+    for (int i = 0; i < 4 * n; ++i) out[i] = (double)sums[i] / count;
+    return 0;
+}
+
+/* Floor of a / 2^k for a signed a (an arithmetic right shift). */
+static int64_t floor_shift(int64_t a, int k)
+{
+#if defined(ORACLE_PLANT_V2_TRUNCATE)
+    /* planted mistake (tests only): division that truncates towards zero */
+    return a / ((int64_t)1 << k);
+#else
+    const int64_t q = a / ((int64_t)1 << k);
+    return (q * ((int64_t)1 << k) > a) ? q - 1 : q;
+#endif
+}
+
+/*
+ * motion_v2 blur of the signed difference of two frames, as h rows of w int32
+ * values [ADR-1392, Decision 4: stage prev - cur, vertical pass with the CPU's
+ * rounding (>> bpc), then the 5 horizontal taps (>> 16)]:
+ *   D[y][x]  = prev[y][x] - cur[y][x]
+ *   V[y][x]  = floor((sum_k t_k * D[mirror(y+k-2, h)][x] + 2^(bpc-1)) / 2^bpc)
+ *   Bd[y][x] = floor((sum_k t_k * V[y][mirror(x+k-2, w)] + 2^15) / 2^16)
+ * Returns 0, or -1 on a bad argument or allocation failure.
+ */
+ORACLE_API int oracle_blur_diff(const void* prev, const void* cur, int w, int h,
+                                size_t pitch_bytes, int bpc, int32_t* out)
+{
+    if (!prev || !cur || !out || !args_ok(w, h, bpc)) return -1;
+    int64_t* v = (int64_t*)malloc(sizeof(int64_t) * (size_t)w * (size_t)h);
+    if (!v) return -1;
+    const unsigned char* p = (const unsigned char*)prev;
+    const unsigned char* c = (const unsigned char*)cur;
+    const int64_t vround = (int64_t)1 << (bpc - 1);
+    for (int y = 0; y < h; ++y) {
+        for (int x = 0; x < w; ++x) {
+            int64_t acc = 0;
+            for (int k = 0; k < 5; ++k) {
+                const int yy = oracle_mirror(y + k - 2, h);
+#if defined(ORACLE_PLANT_V2_CUR_MINUS_PREV)
+                /* planted mistake (tests only): the difference taken the other way */
+                const int64_t dd = (int64_t)sample_at(c, pitch_bytes, bpc, yy, x)
+                                 - (int64_t)sample_at(p, pitch_bytes, bpc, yy, x);
+#else
+                const int64_t dd = (int64_t)sample_at(p, pitch_bytes, bpc, yy, x)
+                                 - (int64_t)sample_at(c, pitch_bytes, bpc, yy, x);
+#endif
+                acc += (int64_t)oracle_taps[k] * dd;
+            }
+            v[(size_t)y * w + x] = floor_shift(acc + vround, bpc);
+        }
+    }
+    for (int y = 0; y < h; ++y) {
+        for (int x = 0; x < w; ++x) {
+            int64_t acc = 0;
+            for (int k = 0; k < 5; ++k) {
+                const int xx = oracle_mirror(x + k - 2, w);
+                acc += (int64_t)oracle_taps[k] * v[(size_t)y * w + xx];
+            }
+            out[(size_t)y * w + x] = (int32_t)floor_shift(acc + 32768, 16);
+        }
+    }
+    free(v);
+    return 0;
+}
+
+/*
+ * motion_v2 SADs over a sequence of n frames stored frame_stride bytes apart:
+ * sad_out[0] = 0 (no previous frame); sad_out[i] = sum |Bd(F_{i-1}, F_i)|.
+ */
+ORACLE_API int oracle_motion_v2_sequence(const void* frames, int n, size_t frame_stride,
+                                         int w, int h, size_t pitch_bytes, int bpc,
+                                         uint64_t* sad_out)
+{
+    if (n < 0 || (n > 0 && (!frames || !sad_out)) || !args_ok(w, h, bpc)) return -1;
+    if (n == 0) return 0;
+    const size_t npx = (size_t)w * (size_t)h;
+    int32_t* b = (int32_t*)malloc(sizeof(int32_t) * npx);
+    if (!b) return -1;
+    const unsigned char* base = (const unsigned char*)frames;
+    sad_out[0] = 0;
+    int rc = 0;
+    for (int i = 1; i < n && rc == 0; ++i) {
+        rc = oracle_blur_diff(base + (size_t)(i - 1) * frame_stride, base + (size_t)i * frame_stride,
+                              w, h, pitch_bytes, bpc, b);
+        if (rc) break;
+        uint64_t acc = 0;
+        for (size_t j = 0; j < npx; ++j) acc += (uint64_t)(b[j] < 0 ? -(int64_t)b[j] : (int64_t)b[j]);
+        sad_out[i] = acc;
+    }
+    free(b);
+    return rc;
 }
