@@ -263,7 +263,173 @@ def pin_scores(o):
     assert s[1] == (72587 / 256.0) / 36.0
 
 
+# ------------------------------------------------------------------ moment sums
+# ADR-1392 Decision 6: four accumulators per pair -- sum ref, sum dist, sum ref^2,
+# sum dist^2 -- exact 64-bit integers (Context).
+
+def pin_moment_closed_forms(o):
+    """Constant planes c1 (ref), c2 (dist): sums c N and squares c^2 N.  A column
+    ramp ref[y][x] = x (x < 2^bpc): sum = h w(w-1)/2, squares = h (w-1)w(2w-1)/6."""
+    for bpc in (8, 10, 16):
+        hi = (1 << bpc) - 1
+        for (w, h) in ((1, 1), (3, 3), (17, 5), (64, 48)):
+            n = w * h
+            for c1, c2 in ((0, hi), (hi, hi), (7, 3)):
+                r = np.full((h, w), c1, _dt(bpc))
+                d = np.full((h, w), c2, _dt(bpc))
+                assert list(o.moment_sums(r, d, bpc)) == [c1 * n, c2 * n, c1 * c1 * n, c2 * c2 * n]
+        w, h = min(200, hi + 1), 7
+        ramp = np.repeat(np.arange(w)[None, :], h, axis=0).astype(_dt(bpc))
+        zero = np.zeros((h, w), _dt(bpc))
+        s = o.moment_sums(ramp, zero, bpc)
+        assert int(s[0]) == h * w * (w - 1) // 2 and int(s[1]) == 0
+        assert int(s[2]) == h * (w - 1) * w * (2 * w - 1) // 6 and int(s[3]) == 0
+
+
+def pin_moment_numpy(o):
+    """Random planes (and a strided view) against numpy's uint64 sums."""
+    rng = np.random.default_rng(21)
+    for bpc in (8, 10, 16):
+        for (w, h) in ((3, 3), (33, 17), (129, 40)):
+            big = rng.integers(0, 1 << bpc, size=(2, h, w + 9)).astype(_dt(bpc))
+            r, d = big[0][:, 4:4 + w], big[1][:, 2:2 + w]
+            r64, d64 = r.astype(np.uint64), d.astype(np.uint64)
+            exp = [r64.sum(), d64.sum(), (r64 * r64).sum(), (d64 * d64).sum()]
+            assert [int(x) for x in o.moment_sums(r, d, bpc)] == [int(x) for x in exp], (bpc, w, h)
+
+
+def pin_moments_from_sums(o):
+    """The moments are the sums over the sample count, in double."""
+    sums = np.array([[35 * 3, 35 * 200, 35 * 9, 35 * 40000], [1, 2, 3, 4]], np.uint64)
+    m = o.moments(sums, 7, 5)
+    assert list(m[0]) == [3.0, 200.0, 9.0, 40000.0]
+    assert list(m[1]) == [1 / 35, 2 / 35, 3 / 35, 4 / 35]
+
+
+# ------------------------------------------------------------------- motion_v2
+# ADR-1392 Decision 4: stage prev - cur, vertical 5-tap pass rounded >> bpc, then
+# the horizontal taps rounded >> 16; a right shift of a negative sum floors.
+
+def pin_v2_equal_and_constant_frames(o):
+    """prev == cur blurs to 0.  Constant prev c1, cur c2: the difference d = c1-c2
+    is constant, the vertical pass gives floor((65536 d + 2^(bpc-1)) / 2^bpc) =
+    d 2^(16-bpc) exactly (also for d < 0) and the horizontal pass keeps it, so
+    SAD = |d| 2^(16-bpc) w h."""
+    rng = np.random.default_rng(22)
+    for bpc in (8, 10, 16):
+        hi = (1 << bpc) - 1
+        for (w, h) in ((3, 3), (11, 7)):
+            f = rng.integers(0, hi + 1, size=(h, w)).astype(_dt(bpc))
+            assert np.all(o.blur_diff(f, f, bpc) == 0)
+            for c1, c2 in ((0, hi), (hi, 0), (5, 9), (9, 5)):
+                p = np.full((h, w), c1, _dt(bpc))
+                c = np.full((h, w), c2, _dt(bpc))
+                d = c1 - c2
+                assert np.all(o.blur_diff(p, c, bpc) == d * (1 << (16 - bpc))), (bpc, c1, c2)
+                sad = o.motion_v2_sequence(np.stack([p, c]), bpc)
+                assert int(sad[0]) == 0 and int(sad[1]) == abs(d) * (1 << (16 - bpc)) * w * h
+
+
+def pin_v2_nonnegative_is_blur(o):
+    """Where prev >= cur everywhere the difference is a valid frame and every sum
+    is non-negative, so the difference blur equals the (separately pinned) blur
+    of the frame prev - cur."""
+    rng = np.random.default_rng(23)
+    for bpc in (8, 10, 16):
+        hi = (1 << bpc) - 1
+        for (w, h) in ((3, 3), (8, 5), (40, 19)):
+            cur = rng.integers(0, hi // 2, size=(h, w))
+            prev = cur + rng.integers(0, hi // 2, size=(h, w))
+            diff = (prev - cur).astype(_dt(bpc))
+            got = o.blur_diff(prev.astype(_dt(bpc)), cur.astype(_dt(bpc)), bpc)
+            assert np.array_equal(got.astype(np.int64), o.blur(diff, bpc).astype(np.int64)), (bpc, w, h)
+
+
+def pin_v2_floor_impulse(o):
+    """Impulse difference at an interior point, worked by hand for prev = 0 and
+    cur = 128 there (8-bit), i.e. d = -128:
+      row y0-2: -128*3571 + 128 = -456960 = -1785 * 256 exactly, so V = -1785
+                (the blur of +128 gives (457088 + 128) >> 8 = 1786: the floor of
+                a negative sum is not the negated positive result);
+      row y0-1: -128*16004 + 128 = -2048384, / 256 = -8001.5, floor -8002;
+      row y0:   -128*26386 + 128 = -3377280, / 256 = -13192.5, floor -13193;
+      centre:   -13193*26386 + 32768 = -348077730, / 65536 = -5311.24, floor -5312.
+    Every other output is 0; the 5x5 window is the outer form
+    floor((floor((d t_{2+dy} + 2^(bpc-1)) / 2^bpc) t_{2+dx} + 2^15) / 2^16).
+    The SAD of an impulse is not symmetric in time: d = +32 gives 8194 and
+    d = -32 gives 8188 (the outer form summed)."""
+    h, w, y0, x0 = 11, 13, 5, 6
+    p = np.zeros((h, w), np.uint8)
+    c = np.zeros((h, w), np.uint8)
+    c[y0, x0] = 128
+    b = o.blur_diff(p, c, 8).astype(np.int64)
+    assert b[y0, x0] == -5312
+    assert b[y0 - 2, x0] == (-1785 * 26386 + 32768) // 65536
+    for bpc, d in ((8, -128), (8, 128), (8, -255), (10, -1023), (10, 37), (16, -65535), (16, 65535)):
+        p = np.zeros((h, w), _dt(bpc))
+        c = np.zeros((h, w), _dt(bpc))
+        if d >= 0:
+            p[y0, x0] = d
+        else:
+            c[y0, x0] = -d
+        exp = np.zeros((h, w), np.int64)
+        for dy in range(-2, 3):
+            vert = (d * T[2 + dy] + (1 << (bpc - 1))) // (1 << bpc)
+            for dx in range(-2, 3):
+                exp[y0 + dy, x0 + dx] = (vert * T[2 + dx] + 32768) // 65536
+        assert np.array_equal(o.blur_diff(p, c, bpc).astype(np.int64), exp), (bpc, d)
+    imp = np.zeros((h, w), np.uint8)
+    imp[y0, x0] = 32
+    zero = np.zeros((h, w), np.uint8)
+    assert int(o.motion_v2_sequence(np.stack([imp, zero]), 8)[1]) == 8194
+    assert int(o.motion_v2_sequence(np.stack([zero, imp]), 8)[1]) == 8188
+
+
+def brute_force_blur_diff(p: np.ndarray, c: np.ndarray, bpc: int) -> np.ndarray:
+    """Per-output 25-MAC loop over the signed difference with floor division
+    (Python's // floors), the vertical value recomputed for every horizontal tap."""
+    h, w = p.shape
+    dl = (p.astype(np.int64) - c.astype(np.int64)).tolist()
+    out = np.zeros((h, w), np.int64)
+    for y in range(h):
+        for x in range(w):
+            acc = 32768
+            for j in range(5):
+                xx = _mirror_fold(x + j - 2, w)
+                col = 1 << (bpc - 1)
+                for k in range(5):
+                    col += T[k] * dl[_mirror_fold(y + k - 2, h)][xx]
+                acc += T[j] * (col // (1 << bpc))
+            out[y, x] = acc // 65536
+    return out
+
+
+def pin_v2_brute_force_tiny(o):
+    rng = np.random.default_rng(24)
+    for bpc in (8, 10, 16):
+        for h in range(3, 9):
+            for w in range(3, 9):
+                p = rng.integers(0, 1 << bpc, size=(h, w)).astype(_dt(bpc))
+                c = rng.integers(0, 1 << bpc, size=(h, w)).astype(_dt(bpc))
+                assert np.array_equal(o.blur_diff(p, c, bpc).astype(np.int64),
+                                      brute_force_blur_diff(p, c, bpc)), (bpc, w, h)
+
+
+def pin_v2_sequence(o):
+    """SAD[0] = 0 and SAD[i] = sum |blur_diff(F_{i-1}, F_i)| (numpy sum)."""
+    rng = np.random.default_rng(25)
+    for bpc in (8, 10):
+        seq = rng.integers(0, 1 << bpc, size=(5, 9, 14)).astype(_dt(bpc))
+        sad = o.motion_v2_sequence(seq, bpc)
+        assert sad[0] == 0
+        for i in range(1, 5):
+            assert int(sad[i]) == int(np.abs(o.blur_diff(seq[i - 1], seq[i], bpc).astype(np.int64)).sum())
+
+
 ALL_PINS = [pin_mirror, pin_constant_frames, pin_two_constant_sad_and_score,
             pin_impulse_interior, pin_hand_worked_6x6, pin_row_constant,
             pin_column_constant, pin_scipy_separable, pin_brute_force_tiny,
-            pin_sad_invariants, pin_sequence, pin_sse, pin_scores]
+            pin_sad_invariants, pin_sequence, pin_sse, pin_scores,
+            pin_moment_closed_forms, pin_moment_numpy, pin_moments_from_sums,
+            pin_v2_equal_and_constant_frames, pin_v2_nonnegative_is_blur,
+            pin_v2_floor_impulse, pin_v2_brute_force_tiny, pin_v2_sequence]

@@ -18,7 +18,9 @@ def test_pin_holds(oracle, pin):
 
 
 PLANTS = ["ORACLE_PLANT_MIRROR_REPEAT", "ORACLE_PLANT_NO_VROUND", "ORACLE_PLANT_VSHIFT8",
-          "ORACLE_PLANT_SWAP_MIRROR_N", "ORACLE_PLANT_NO_HROUND", "ORACLE_PLANT_HFIRST"]
+          "ORACLE_PLANT_SWAP_MIRROR_N", "ORACLE_PLANT_NO_HROUND", "ORACLE_PLANT_HFIRST",
+          "ORACLE_PLANT_MOMENT_SKIP_LAST_ROW", "ORACLE_PLANT_MOMENT_SQUARE_OF_REF",
+          "ORACLE_PLANT_V2_TRUNCATE", "ORACLE_PLANT_V2_CUR_MINUS_PREV"]
 
 
 @pytest.mark.parametrize("plant", PLANTS)
