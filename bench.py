@@ -367,10 +367,12 @@ def run_sequence_workload(args):
     for batch in batches:
         ctx = iif.MotionContext(w, h, bpc)
 
+        submit = ctx.submit_batch_v2 if args.v2 else ctx.submit_batch
+
         def step():
             ctx.reset()
             for b0 in range(0, n, batch):
-                ctx.submit_batch(d[b0:b0 + batch], sad[b0:b0 + batch], stream=stream)
+                submit(d[b0:b0 + batch], sad[b0:b0 + batch], stream=stream)
 
         for _ in range(max(args.warmup, 3)):
             step()
@@ -386,11 +388,13 @@ def run_sequence_workload(args):
         ms = e0.elapsed_time(e1) / args.steps
         launches = (iif.motion_kernel_launch_count() - l0) / args.steps
         alg = w * h * s * n
-        lines.append({"metric": "frames/s (batched motion SAD)", "value": n / (ms * 1e-3),
+        lines.append({"metric": "frames/s (batched motion%s SAD)" % ("_v2" if args.v2 else ""),
+                      "value": n / (ms * 1e-3),
                       "unit": "frames/s", "n_gpus": 1, "steps": args.steps,
                       "warmup": max(args.warmup, 3), "ms_per_step": ms, "higher_is_better": True,
                       "dtype": "u8" if bpc == 8 else "u16", "data": "synthetic",
-                      "config": {"workload": args.workload, "w": w, "h": h, "bpc": bpc,
+                      "config": {"workload": args.workload + ("_v2" if args.v2 else ""),
+                                 "w": w, "h": h, "bpc": bpc,
                                  "frames_per_step": n, "batch": batch,
                                  "launches_per_step": launches},
                       "roofline": {"bound": "hbm", "achieved": alg / (ms * 1e-3) / 1e9,
@@ -437,6 +441,50 @@ def run_sse_workload(args):
     print(json.dumps({"metric": "pairs/s (PSNR SSE of Y, U, V)", "value": n / (ms * 1e-3),
                       "unit": "frames/s", "ms_per_step": ms, "steps": args.steps,
                       "config": {"workload": "sse_yuv420_%dx%d_u8_pairs" % (args.w, args.h),
+                                 "pairs_per_step": n},
+                      "roofline": {"bound": "hbm", "achieved": alg / (ms * 1e-3) / 1e9,
+                                   "peak": peak, "unit": "GB/s",
+                                   "frac": alg / (ms * 1e-3) / 1e9 / peak,
+                                   "peak_kind": peak_kind}}), flush=True)
+    return 0
+
+
+def run_moment_workload(args):
+    """Moment sums (sum ref, sum dist, sum ref^2, sum dist^2) of the luma of the
+    4:2:0 pairs in one launch; algorithmic bytes 2 w h per pair."""
+    import torch
+
+    import integer_image_filter_gb300 as iif
+    import synth
+
+    n = args.pairs
+    batch = synth.yuv420_pairs(4, n, args.w, args.h, max_shift=2, dist_sigma=3.0)
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    ref = torch.from_numpy(batch.ref_y).to(dev)
+    dist = torch.from_numpy(batch.dist_y).to(dev)
+    out = torch.zeros((n, 4), dtype=torch.int64, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        iif.moment_sums_batch(ref, dist, 8, out, stream=stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = e0.elapsed_time(e1) / args.steps
+    peak, peak_kind = peaks()
+    alg = 2 * args.w * args.h * n
+    print(json.dumps({"metric": "pairs/s (luma moment sums)", "value": n / (ms * 1e-3),
+                      "unit": "frames/s", "ms_per_step": ms, "steps": args.steps,
+                      "config": {"workload": "moment_%dx%d_u8_pairs" % (args.w, args.h),
                                  "pairs_per_step": n},
                       "roofline": {"bound": "hbm", "achieved": alg / (ms * 1e-3) / 1e9,
                                    "peak": peak, "unit": "GB/s",
@@ -494,12 +542,17 @@ def main(argv=None):
     ap.add_argument("--workload", default=WORKLOAD,
                     help="the headline 4:2:0 workload (default) or one of the motion-only "
                          "configurations: seq_3840x2160_u10, seq_1920x1080_u8_cuts, "
-                         "seq_576x324_u8, pair_64x48_u8")
+                         "seq_576x324_u8, pair_64x48_u8; or sse_yuv420_3840x2160_u8_pairs, "
+                         "moment_3840x2160_u8_pairs (stand-alone SSE / luma moment sums)")
     ap.add_argument("--batch", type=int, default=0, help="frames per launch (sequence workloads)")
     ap.add_argument("--sweep", action="store_true", help="sweep batch sizes 1..32")
+    ap.add_argument("--v2", action="store_true",
+                    help="sequence workloads: motion_v2 (blur of prev - cur) instead of motion")
     args = ap.parse_args(argv)
     if args.workload == "sse_yuv420_3840x2160_u8_pairs" and args.impl == "ours":
         return run_sse_workload(args)
+    if args.workload == "moment_3840x2160_u8_pairs" and args.impl == "ours":
+        return run_moment_workload(args)
     if args.workload in ("seq_3840x2160_u10", "seq_1920x1080_u8_cuts") and args.impl == "ours":
         return run_sequence_workload(args)
     if args.workload in ("seq_576x324_u8", "pair_64x48_u8") and args.impl == "ours":

@@ -109,6 +109,23 @@ MOTION_API int motion_submit_batch(motion_ctx* ctx, const void* d_frames, int n,
                         size_t frame_stride_bytes, size_t pitch_bytes,
                         void* stream, uint64_t* d_sad_out);
 
+/* motion_v2 over n frames in ONE launch ("ADR-1392: CUDA motion, PSNR and
+ * moment kernels add one atomic per block, ...", Decision 4: stage prev - cur,
+ * vertical 5-tap pass with the CPU's rounding (>> bpc), then the 5 horizontal
+ * taps (>> 16)).  With the same taps and mirror rule as motion_submit_batch,
+ * each frame i gives the blur Bd of D = F_{i-1} - F_i, where a right shift
+ * of a negative sum rounds towards minus infinity, and d_sad_out[i] =
+ * sum |Bd| (device uint64[n]).  SAD_0 is against the last frame of the
+ * previous motion_v2 call on this context, or 0 at the start of a sequence
+ * (motion_reset starts one).  The context keeps the last raw frame in two
+ * planes of its own that alternate between calls; the first motion_v2 call
+ * on a context allocates them (2 w h bytes per sample).  The motion_v2
+ * sequence state is independent of motion_submit_batch's.  Frame layout,
+ * alignment handling, asynchrony and errors as motion_submit_batch. */
+MOTION_API int motion_v2_submit_batch(motion_ctx* ctx, const void* d_frames, int n,
+                                      size_t frame_stride_bytes, size_t pitch_bytes,
+                                      void* stream, uint64_t* d_sad_out);
+
 /* Fused pass over n 4:2:0 reference/distorted picture pairs in ONE launch:
  * motion SAD on the reference luma (continuing the context's sequence, as
  * motion_submit_batch) and SSE of each plane Y, U, V of every pair.
@@ -164,6 +181,30 @@ MOTION_API int psnr_sse_yuv420_batch(int w, int h, int bpc, int n,
                           const void* d_dist_u, const void* d_dist_v,
                           size_t pitch_y, size_t pitch_uv, size_t stride_y,
                           size_t stride_uv, void* stream, uint64_t* d_sse_out);
+
+/* Moment sums of n picture pairs' luma planes in ONE launch ("ADR-1392: CUDA
+ * motion, PSNR and moment kernels add one atomic per block, ...", Decision 6:
+ * four accumulators -- the reference and distorted sums and sums of squares --
+ * each added once per block; Context: exact 64-bit integer sums).
+ * d_ref / d_dist: device w x h planes, `pitch` bytes between rows and `stride`
+ * bytes between pairs (one layout for both pictures; pairs must not overlap);
+ * uint8 samples for bpc 8, little-endian uint16 for bpc 9..16.  d_out: device
+ * uint64[n][4] = {sum ref, sum dist, sum ref^2, sum dist^2}, zeroed and then
+ * written by the call.  Asynchronous on `stream` (a cudaStream_t, NULL for the
+ * legacy default stream).  w, h >= 1.  16-byte aligned pointers, pitch and
+ * stride take the vector path; any other layout is served sample by sample.
+ * Errors: MOTION_ERR_UNSUPPORTED_BITDEPTH, MOTION_ERR_INVALID_ARGUMENT (n < 0,
+ * w or h < 1, null pointers), MOTION_ERR_TOO_LARGE, MOTION_ERR_BAD_PITCH,
+ * MOTION_ERR_CUDA; nothing is launched on error.  n == 0 is a no-op. */
+MOTION_API int moment_sums_batch(int w, int h, int bpc, int n, const void* d_ref,
+                                 const void* d_dist, size_t pitch, size_t stride,
+                                 void* stream, uint64_t* d_out);
+
+/* Host, no GPU: the moments from moment sums, each sum over the sample count
+ * w*h in double -- out[i][0..3] = mean of ref, mean of dist, mean square of
+ * ref, mean square of dist (the first and second moments of each picture).
+ * sums: host uint64[n][4]; out: host double[n][4]. */
+MOTION_API int moments_from_sums(const uint64_t* sums, int n, int w, int h, double* out);
 
 /* Host helper: score_i = (SAD_i / 256) / (w h) and motion2_i =
  * min(score_i, score_{i+1}); motion2_{n-1} = score_{n-1} unless next_score

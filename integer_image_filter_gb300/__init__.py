@@ -26,7 +26,8 @@ __all__ = [
     "psnr_sse_yuv420_batch", "motion_scores_from_sad", "psnr_from_sse",
     "motion_kernel_launch_count", "motion_strerror", "MotionContext", "EXPORTED_SYMBOLS",
     "motion_set_kernel_path", "motion_device_error", "MOTION_PATH_AUTO", "MOTION_PATH_GENERIC",
-    "motion_submit_batch_noalloc", "motion_set_stall_injection",
+    "motion_submit_batch_noalloc", "motion_set_stall_injection", "moment_sums_batch",
+    "moments_from_sums", "motion_v2_submit_batch",
 ]
 
 EXPORTED_SYMBOLS = (
@@ -35,7 +36,8 @@ EXPORTED_SYMBOLS = (
     "psnr_sse", "psnr_sse_yuv420_batch", "motion_scores_from_sad", "psnr_from_sse",
     "motion_kernel_launch_count", "motion_strerror", "motion_last_cuda_error",
     "motion_set_kernel_path", "motion_device_error", "motion_submit_batch_noalloc",
-    "motion_set_stall_injection",
+    "motion_set_stall_injection", "moment_sums_batch", "moments_from_sums",
+    "motion_v2_submit_batch",
 )
 
 _LIB: ctypes.CDLL | None = None
@@ -75,6 +77,9 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
         "motion_device_error": ([P, ctypes.POINTER(I)], I),
         "motion_submit_batch_noalloc": ([P, I, I, I, I, Z, Z, I, P, P], I),
         "motion_set_stall_injection": ([P, I], I),
+        "moment_sums_batch": ([I, I, I, I, P, P, Z, Z, P, P], I),
+        "moments_from_sums": ([P, I, I, I, P], I),
+        "motion_v2_submit_batch": ([P, P, I, Z, Z, P, P], I),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -199,6 +204,20 @@ def motion_submit_batch(ctx: int, frames, sad_out, n: int | None = None,
            "motion_submit_batch")
 
 
+def motion_v2_submit_batch(ctx: int, frames, sad_out, n: int | None = None,
+                           frame_stride: int | None = None, pitch_bytes: int | None = None,
+                           stream=None) -> None:
+    if n is None:
+        n = int(frames.shape[0])
+    if pitch_bytes is None or frame_stride is None:
+        p, s = _layout(frames)
+        pitch_bytes = p if pitch_bytes is None else pitch_bytes
+        frame_stride = s if frame_stride is None else frame_stride
+    _check(load_library().motion_v2_submit_batch(ctx, _addr(frames), n, frame_stride,
+                                                 pitch_bytes, _stream(stream), _addr(sad_out)),
+           "motion_v2_submit_batch")
+
+
 @dataclass
 class Yuv420Layout:
     pitch_y: int
@@ -284,6 +303,32 @@ def motion_scores_from_sad(sad, w: int, h: int, next_score: float | None = None)
         s.ctypes.data, n, w, h, ctypes.addressof(nxt) if nxt is not None else None,
         score.ctypes.data, motion2.ctypes.data), "motion_scores_from_sad")
     return score, motion2
+
+
+def moment_sums_batch(ref, dist, bpc: int, out, w: int | None = None, h: int | None = None,
+                      n: int | None = None, pitch: int | None = None, stride: int | None = None,
+                      stream=None) -> None:
+    """Moment sums of n luma pairs ((n, h, w) or (h, w) device tensors sharing one
+    layout) into the device uint64/int64 tensor out[n][4]."""
+    if h is None or w is None:
+        h, w = int(ref.shape[-2]), int(ref.shape[-1])
+    if n is None:
+        n = int(ref.shape[0]) if len(ref.shape) == 3 else 1
+    if pitch is None or stride is None:
+        p, st = _layout(ref)
+        pitch = p if pitch is None else pitch
+        stride = st if stride is None else stride
+    _check(load_library().moment_sums_batch(w, h, bpc, n, _addr(ref), _addr(dist), pitch, stride,
+                                            _stream(stream), _addr(out)), "moment_sums_batch")
+
+
+def moments_from_sums(sums, w: int, h: int) -> np.ndarray:
+    """float64[n][4] moments (each sum over w*h) from uint64[n][4] moment sums."""
+    s = np.ascontiguousarray(np.asarray(sums, dtype=np.uint64)).reshape(-1, 4)
+    out = np.zeros(s.shape, np.float64)
+    _check(load_library().moments_from_sums(s.ctypes.data, s.shape[0], w, h, out.ctypes.data),
+           "moments_from_sums")
+    return out
 
 
 def psnr_from_sse(sse: int, n_samples: int, bpc: int):
@@ -379,6 +424,9 @@ class MotionContext:
 
     def submit_batch(self, frames, sad_out, stream=None) -> None:
         motion_submit_batch(self.handle, frames, sad_out, stream=stream)
+
+    def submit_batch_v2(self, frames, sad_out, stream=None) -> None:
+        motion_v2_submit_batch(self.handle, frames, sad_out, stream=stream)
 
     def yuv420_batch(self, ref_y, ref_u, ref_v, dist_y, dist_u, dist_v, sad_out, sse_out,
                      stream=None) -> None:

@@ -13,7 +13,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "_lib")
 LIB_NAME = "libmotion_gb300.so"
-SOURCES = ["motion_capi.cu", "motion_tile.cu", "motion_tma.cu", "psnr_sse.cu", "motion_noalloc.cu"]
+SOURCES = ["motion_capi.cu", "motion_tile.cu", "motion_tma.cu", "psnr_sse.cu", "motion_noalloc.cu",
+           "moment.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -87,6 +87,12 @@ struct motion_ctx {
     // uploads are queued without waiting for this chunk's kernel
     unsigned long long* h_res = nullptr;
     size_t h_res_pairs = 0;
+    // motion_v2: the last raw frame of the sequence, two planes that alternate
+    // (allocated by the first motion_v2 call), rows raw_pitch bytes apart
+    uint8_t* d_raw[2] = {nullptr, nullptr};
+    size_t raw_pitch = 0;
+    int raw_cur = 0;
+    int v2_has_prev = 0;
 };
 
 namespace {
@@ -240,6 +246,8 @@ int motion_destroy(motion_ctx* c) {
     free_staging(c);
     if (c->d_bprev[0]) cudaFree(c->d_bprev[0]);
     if (c->d_bprev[1]) cudaFree(c->d_bprev[1]);
+    if (c->d_raw[0]) cudaFree(c->d_raw[0]);
+    if (c->d_raw[1]) cudaFree(c->d_raw[1]);
     if (c->d_slot) cudaFree(c->d_slot);
     if (c->d_err) cudaFree(c->d_err);
     if (c->h_slot) cudaFreeHost(c->h_slot);
@@ -251,6 +259,7 @@ int motion_destroy(motion_ctx* c) {
 int motion_reset(motion_ctx* c) {
     if (!c) return MOTION_ERR_INVALID_ARGUMENT;
     c->has_prev = 0;
+    c->v2_has_prev = 0;
     return MOTION_OK;
 }
 
@@ -271,6 +280,45 @@ int motion_submit_batch(motion_ctx* c, const void* d_frames, int n, size_t frame
     a.aligned16 = aligned16(d_frames, pitch, frame_stride, n);
     a.sad_out = (unsigned long long*)d_sad_out;
     return launch_motion(c, a, false, s);
+}
+
+int motion_v2_submit_batch(motion_ctx* c, const void* d_frames, int n, size_t frame_stride,
+                           size_t pitch, void* stream, uint64_t* d_sad_out) {
+    if (!c || n < 0) return MOTION_ERR_INVALID_ARGUMENT;
+    if (n == 0) return MOTION_OK;
+    if (!d_sad_out) return MOTION_ERR_INVALID_ARGUMENT;
+    int rc = check_layout(d_frames, pitch, frame_stride, n, c->w, c->bpc);
+    if (rc) return rc;
+    if ((rc = ctx_device_ok(c))) return rc;
+    const size_t s_bytes = (size_t)sample_bytes(c->bpc);
+    if (!c->d_raw[0]) {
+        c->raw_pitch = ((size_t)c->w * s_bytes + 15) & ~(size_t)15;
+        for (int k = 0; k < 2; ++k)
+            MG_CUDA(cudaMalloc(&c->d_raw[k], c->raw_pitch * (size_t)c->h));
+    }
+    cudaStream_t s = (cudaStream_t)stream;
+    MG_CUDA(cudaMemsetAsync(d_sad_out, 0, sizeof(uint64_t) * (size_t)n, s));
+    mg::TileArgs a = motion_args(c, n);
+    a.ref_y = (const uint8_t*)d_frames;
+    a.pitch_y = (long long)pitch;
+    a.stride_y = (long long)frame_stride;
+    a.aligned16 = aligned16(d_frames, pitch, frame_stride, n);
+    a.sad_out = (unsigned long long*)d_sad_out;
+    a.has_prev = c->v2_has_prev;
+    a.bprev = a.bprev_out = nullptr;
+    a.raw_prev = c->d_raw[c->raw_cur];
+    a.raw_out = c->d_raw[c->raw_cur ^ 1];
+    a.raw_pitch = (long long)c->raw_pitch;
+    int launched = 0;
+    bool used = false;
+    cudaError_t e = cudaSuccess;
+    if (!c->force_generic) e = mg::launch_motion_v2_tma(a, s, &launched, &used);
+    if (e == cudaSuccess && !used) e = mg::launch_motion_v2_tile(a, s, &launched);
+    g_launches += (uint64_t)launched;
+    if (e != cudaSuccess) return cuda_fail(e);
+    c->v2_has_prev = 1;
+    c->raw_cur ^= 1;   // the plane just written holds the last frame
+    return MOTION_OK;
 }
 
 int motion_submit(motion_ctx* c, const void* d_frame, size_t pitch, void* stream,
@@ -487,6 +535,49 @@ int psnr_sse_yuv420_batch(int w, int h, int bpc, int n, const void* ry, const vo
     cudaError_t e = mg::launch_sse(a, s, sms, &launched);
     g_launches += (uint64_t)launched;
     if (e != cudaSuccess) return cuda_fail(e);
+    return MOTION_OK;
+}
+
+int moment_sums_batch(int w, int h, int bpc, int n, const void* d_ref, const void* d_dist,
+                      size_t pitch, size_t stride, void* stream, uint64_t* d_out) {
+    if (bpc < 8 || bpc > 16) return MOTION_ERR_UNSUPPORTED_BITDEPTH;
+    if (w < 1 || h < 1 || n < 0) return MOTION_ERR_INVALID_ARGUMENT;
+    if (w > MOTION_MAX_DIM || h > MOTION_MAX_DIM) return MOTION_ERR_TOO_LARGE;
+    if (n == 0) return MOTION_OK;
+    if (!d_out) return MOTION_ERR_INVALID_ARGUMENT;
+    int rc;
+    if ((rc = check_layout(d_ref, pitch, stride, n, w, bpc))) return rc;
+    if ((rc = check_layout(d_dist, pitch, stride, n, w, bpc))) return rc;
+    if (n > 1 && stride < pitch * (size_t)(h - 1) + (size_t)w * (size_t)sample_bytes(bpc))
+        return MOTION_ERR_BAD_PITCH;
+    cudaStream_t s = (cudaStream_t)stream;
+    MG_CUDA(cudaMemsetAsync(d_out, 0, sizeof(uint64_t) * 4 * (size_t)n, s));
+    int dev = 0, sms = 0;
+    MG_CUDA(cudaGetDevice(&dev));
+    MG_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+    mg::MomentArgs a;
+    std::memset(&a, 0, sizeof(a));
+    a.ref = (const uint8_t*)d_ref;
+    a.dist = (const uint8_t*)d_dist;
+    a.pitch = (long long)pitch;
+    a.stride = (long long)stride;
+    a.w = w;
+    a.h = h;
+    a.bpc = bpc;
+    a.n = n;
+    a.out = (unsigned long long*)d_out;
+    int launched = 0;
+    cudaError_t e = mg::launch_moment(a, s, sms, &launched);
+    g_launches += (uint64_t)launched;
+    if (e != cudaSuccess) return cuda_fail(e);
+    return MOTION_OK;
+}
+
+int moments_from_sums(const uint64_t* sums, int n, int w, int h, double* out) {
+    if (n < 0 || w <= 0 || h <= 0) return MOTION_ERR_INVALID_ARGUMENT;
+    if (n > 0 && (!sums || !out)) return MOTION_ERR_INVALID_ARGUMENT;
+    const double count = (double)w * (double)h;
+    for (int i = 0; i < 4 * n; ++i) out[i] = (double)sums[i] / count;
     return MOTION_OK;
 }
 

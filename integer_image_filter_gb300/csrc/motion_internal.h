@@ -35,6 +35,11 @@ struct TileArgs {
     int chunk;                    // TMA kernel: frames per CTA (grid.z = ceil(n / chunk))
     long long wait_cycles;        // bound of every mbarrier wait (0: about one second)
     int tx_extra;                 // test hook: bytes a stage expects beyond its boxes (0)
+    // motion_v2 (blur of prev - cur): the last raw frame of the previous call
+    // (read when has_prev) and the plane that receives this call's last frame
+    const uint8_t* raw_prev;      // w x h samples, raw_pitch bytes per row
+    uint8_t* raw_out;
+    long long raw_pitch;
 };
 
 // Tensor maps of one TMA launch (64-byte aligned, passed as a grid constant).
@@ -42,6 +47,7 @@ struct TmaMaps {
     CUtensorMap raw;              // reference luma, box (TW + 2 HX) x (TH + 4) x 1
     CUtensorMap dist;             // distorted luma, box TW x TH x 1
     CUtensorMap ru, du, rv, dv;   // chroma planes, box TW/2 x TH/2 x 1
+    CUtensorMap prev;             // motion_v2: the previous call's last raw frame, box as raw
 };
 
 // Arguments of one batched SSE launch over n pairs x (1 or 3) planes.
@@ -64,7 +70,21 @@ cudaError_t launch_motion_tile(const TileArgs& a, bool fused, cudaStream_t s,
 // suit TMA (nothing launched; the caller falls back to launch_motion_tile).
 cudaError_t launch_motion_tma(const TileArgs& a, bool fused, cudaStream_t s, int* launches,
                               bool* used);
+// motion_v2 (the blur of prev - cur, floor rounding, SAD of |blur|): TMA
+// kernel when the layout allows (*used), else the generic kernel.
+cudaError_t launch_motion_v2_tma(const TileArgs& a, cudaStream_t s, int* launches, bool* used);
+cudaError_t launch_motion_v2_tile(const TileArgs& a, cudaStream_t s, int* launches);
 cudaError_t launch_sse(const SseArgs& a, cudaStream_t s, int sm_count, int* launches);
+
+// Moment sums of n luma pairs (sum ref, sum dist, sum ref^2, sum dist^2).
+struct MomentArgs {
+    const uint8_t* ref;
+    const uint8_t* dist;
+    long long pitch, stride;        // shared by both pictures
+    int w, h, bpc, n;
+    unsigned long long* out;        // [n][4], zeroed by the caller
+};
+cudaError_t launch_moment(const MomentArgs& a, cudaStream_t s, int sm_count, int* launches);
 
 // Adds to the library-wide kernel launch count (motion_kernel_launch_count).
 void note_launches(int n);

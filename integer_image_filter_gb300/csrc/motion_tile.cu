@@ -24,19 +24,21 @@
 
 namespace mg {
 
+// Stage frame f (luma fy with row pitch `pitch`; fused: the distorted luma
+// and chroma of pair f) for the tile at (x0, y0).
 template <typename Pix, bool FUSED>
 __device__ __forceinline__ void load_stage(const TileArgs& a, int f, unsigned char* st,
-                                           int x0, int y0, bool fast) {
+                                           int x0, int y0, bool fast, const uint8_t* fy,
+                                           long long pitch) {
     using G = Geo<Pix>;
     constexpr int S = G::S;
     const int tid = threadIdx.x;
-    const uint8_t* fy = a.ref_y + (long long)f * a.stride_y;
     if (fast) {
         constexpr int CHR = G::RAW_W * S / 16;
-        const uint8_t* g0 = fy + (long long)(y0 - 2) * a.pitch_y + (long long)(x0 - G::HX) * S;
+        const uint8_t* g0 = fy + (long long)(y0 - 2) * pitch + (long long)(x0 - G::HX) * S;
         for (int c = tid; c < G::RAW_ROWS * CHR; c += NT) {
             const int r = c / CHR, k = c - r * CHR;
-            cp_async16(st + (r * G::RAW_W) * S + k * 16, g0 + (long long)r * a.pitch_y + k * 16);
+            cp_async16(st + (r * G::RAW_W) * S + k * 16, g0 + (long long)r * pitch + k * 16);
         }
         if constexpr (FUSED) {
             unsigned char* sd = st + G::RAW_BYTES;
@@ -68,7 +70,7 @@ __device__ __forceinline__ void load_stage(const TileArgs& a, int f, unsigned ch
     for (int e = tid; e < G::RAW_ROWS * G::RAW_W; e += NT) {
         const int r = e / G::RAW_W, c = e - r * G::RAW_W;
         const int yy = mirror_clamp(y0 - 2 + r, a.h), xx = mirror_clamp(x0 - G::HX + c, a.w);
-        raw[e] = *reinterpret_cast<const Pix*>(fy + (long long)yy * a.pitch_y + (long long)xx * S);
+        raw[e] = *reinterpret_cast<const Pix*>(fy + (long long)yy * pitch + (long long)xx * S);
     }
     if constexpr (FUSED) {
         Pix* sd = reinterpret_cast<Pix*>(st + G::RAW_BYTES);
@@ -80,7 +82,7 @@ __device__ __forceinline__ void load_stage(const TileArgs& a, int f, unsigned ch
             // reference sample, so the squared error there is zero
             const bool in = (y < a.h) && (x < a.w);
             const uint8_t* src = in ? fd + (long long)y * a.pitch_y + (long long)x * S
-                                    : fy + (long long)mirror_clamp(y, a.h) * a.pitch_y +
+                                    : fy + (long long)mirror_clamp(y, a.h) * pitch +
                                           (long long)mirror_clamp(x, a.w) * S;
             sd[e] = *reinterpret_cast<const Pix*>(src);
         }
@@ -100,8 +102,11 @@ __device__ __forceinline__ void load_stage(const TileArgs& a, int f, unsigned ch
     }
 }
 
-template <typename Pix, bool FUSED>
+// V2: motion_v2, the blur of prev - cur (unrounded vertical sums of the
+// previous frame kept per thread, floor shifts, SAD of |blur|); FUSED false.
+template <typename Pix, bool FUSED, bool V2>
 __global__ void __launch_bounds__(NT) motion_tile_kernel(const TileArgs a) {
+    static_assert(!(FUSED && V2), "motion_v2 has no fused form");
     using G = Geo<Pix>;
     using Acc = typename SseAcc<Pix>::T;
     constexpr int STAGE = FUSED ? G::STAGE_FUSED : G::STAGE_MOTION;
@@ -112,8 +117,24 @@ __global__ void __launch_bounds__(NT) motion_tile_kernel(const TileArgs a) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int x0 = blockIdx.x * TW, y0 = blockIdx.y * TH;
     const bool full = (x0 + TW <= a.w) && (y0 + TH <= a.h);
-    const bool fast = a.aligned16 && (x0 - G::HX >= 0) && (x0 + TW + G::HX <= a.w) &&
-                      (y0 - 2 >= 0) && (y0 + TH + 2 <= a.h);
+    const bool inner = (x0 - G::HX >= 0) && (x0 + TW + G::HX <= a.w) && (y0 - 2 >= 0) &&
+                       (y0 + TH + 2 <= a.h);
+    const bool fast = a.aligned16 && inner;
+    const bool fast_prev = inner && (((uintptr_t)a.raw_prev | (uintptr_t)a.raw_pitch) % 16 == 0);
+    // motion_v2 continuing an earlier call first re-derives the vertical sums
+    // of that call's last raw frame (local frame 0, no output)
+    const bool warm = V2 && a.has_prev;
+    const int cnt = a.n + (warm ? 1 : 0);
+    auto stage = [&](int l, unsigned char* st) {
+        const int f = l - (warm ? 1 : 0);
+        if (f < 0)
+            load_stage<Pix, FUSED>(a, 0, st, x0, y0, fast_prev, a.raw_prev, a.raw_pitch);
+        else
+            load_stage<Pix, FUSED>(a, f, st, x0, y0, fast, a.ref_y + (long long)f * a.stride_y,
+                                   a.pitch_y);
+    };
+    [[maybe_unused]] uint32_t xp[4][4] = {};   // motion_v2: this thread's vertical sums, previous frame
+    [[maybe_unused]] uint32_t hxp = 0;          // and of its halo value
     const uint32_t rnd = 1u << (a.bpc - 1);
     const int sh = a.bpc;
 
@@ -130,11 +151,12 @@ __global__ void __launch_bounds__(NT) motion_tile_kernel(const TileArgs a) {
         }
     }
 
-    load_stage<Pix, FUSED>(a, 0, smem, x0, y0, fast);
+    stage(0, smem);
     cp_async_commit();
-    for (int f = 0; f < a.n; ++f) {
-        unsigned char* st = smem + (f & 1) * STAGE;
-        if (f + 1 < a.n) load_stage<Pix, FUSED>(a, f + 1, smem + ((f + 1) & 1) * STAGE, x0, y0, fast);
+    for (int l = 0; l < cnt; ++l) {
+        const int f = l - (warm ? 1 : 0);   // frame index of the output (-1: warm-up)
+        unsigned char* st = smem + (l & 1) * STAGE;
+        if (l + 1 < cnt) stage(l + 1, smem + ((l + 1) & 1) * STAGE);
         cp_async_commit();
         cp_async_wait<1>();
         __syncthreads();
@@ -149,10 +171,23 @@ __global__ void __launch_bounds__(NT) motion_tile_kernel(const TileArgs a) {
 #pragma unroll
             for (int r = 0; r < 4; ++r) {
                 uint4 o;
-                o.x = vtap(p[r][0], p[r + 1][0], p[r + 2][0], p[r + 3][0], p[r + 4][0], rnd, sh);
-                o.y = vtap(p[r][1], p[r + 1][1], p[r + 2][1], p[r + 3][1], p[r + 4][1], rnd, sh);
-                o.z = vtap(p[r][2], p[r + 1][2], p[r + 2][2], p[r + 3][2], p[r + 4][2], rnd, sh);
-                o.w = vtap(p[r][3], p[r + 1][3], p[r + 2][3], p[r + 3][3], p[r + 4][3], rnd, sh);
+                if constexpr (V2) {
+                    uint32_t x[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        x[i] = vsum(p[r][i], p[r + 1][i], p[r + 2][i], p[r + 3][i], p[r + 4][i]);
+                    o.x = (uint32_t)vdiff<Pix>(xp[r][0], x[0], rnd, sh);
+                    o.y = (uint32_t)vdiff<Pix>(xp[r][1], x[1], rnd, sh);
+                    o.z = (uint32_t)vdiff<Pix>(xp[r][2], x[2], rnd, sh);
+                    o.w = (uint32_t)vdiff<Pix>(xp[r][3], x[3], rnd, sh);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) xp[r][i] = x[i];
+                } else {
+                    o.x = vtap(p[r][0], p[r + 1][0], p[r + 2][0], p[r + 3][0], p[r + 4][0], rnd, sh);
+                    o.y = vtap(p[r][1], p[r + 1][1], p[r + 2][1], p[r + 3][1], p[r + 4][1], rnd, sh);
+                    o.z = vtap(p[r][2], p[r + 1][2], p[r + 2][2], p[r + 3][2], p[r + 4][2], rnd, sh);
+                    o.w = vtap(p[r][3], p[r + 1][3], p[r + 2][3], p[r + 3][3], p[r + 4][3], rnd, sh);
+                }
                 *reinterpret_cast<uint4*>(sV + (warp * 4 + r) * SVW + 4 + 4 * lane) = o;
             }
             // the two halo columns on each side of the tile
@@ -160,14 +195,21 @@ __global__ void __launch_bounds__(NT) motion_tile_kernel(const TileArgs a) {
                 const int r = tid >> 2, which = tid & 3;
                 const int off = which == 0 ? -2 : which == 1 ? -1 : which == 2 ? TW : TW + 1;
                 const Pix* s = raw + r * G::RAW_W + G::HX + off;
-                sV[r * SVW + 4 + off] = vtap(s[0], s[G::RAW_W], s[2 * G::RAW_W], s[3 * G::RAW_W],
-                                             s[4 * G::RAW_W], rnd, sh);
+                if constexpr (V2) {
+                    const uint32_t x = vsum(s[0], s[G::RAW_W], s[2 * G::RAW_W], s[3 * G::RAW_W],
+                                            s[4 * G::RAW_W]);
+                    sV[r * SVW + 4 + off] = (uint32_t)vdiff<Pix>(hxp, x, rnd, sh);
+                    hxp = x;
+                } else {
+                    sV[r * SVW + 4 + off] = vtap(s[0], s[G::RAW_W], s[2 * G::RAW_W], s[3 * G::RAW_W],
+                                                 s[4 * G::RAW_W], rnd, sh);
+                }
             }
         }
         __syncthreads();
 
         // ---- horizontal pass, SAD against B_prev, SSE of the luma
-        const bool do_sad = (f > 0) || a.has_prev;
+        const bool do_sad = V2 ? l > 0 : (f > 0) || a.has_prev;
         uint32_t sad = 0;
         Acc sse_y = 0, sse_u = 0, sse_v = 0;
 #pragma unroll
@@ -177,6 +219,18 @@ __global__ void __launch_bounds__(NT) motion_tile_kernel(const TileArgs a) {
             const uint4 A = *reinterpret_cast<const uint4*>(v);
             const uint4 Bq = *reinterpret_cast<const uint4*>(v + 4);
             const uint4 C = *reinterpret_cast<const uint4*>(v + 8);
+            if constexpr (V2) {
+                const int wi[12] = {(int)A.x, (int)A.y, (int)A.z, (int)A.w, (int)Bq.x, (int)Bq.y,
+                                    (int)Bq.z, (int)Bq.w, (int)C.x, (int)C.y, (int)C.z, (int)C.w};
+                int bd[4];
+                horizontal_quad_signed(wi, bd);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const bool ok = full || ((y0 + r < a.h) && (x0 + 4 * q + i < a.w));
+                    sad = __sad(ok ? bd[i] : 0, 0, sad);
+                }
+                continue;
+            }
             const uint32_t wv[12] = {A.x, A.y, A.z, A.w, Bq.x, Bq.y, Bq.z, Bq.w, C.x, C.y, C.z, C.w};
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
@@ -260,6 +314,23 @@ __global__ void __launch_bounds__(NT) motion_tile_kernel(const TileArgs a) {
         }
     }
 
+    if (V2 && a.store_last && a.n > 0) {
+        // keep the last raw frame for the next call (the last stage; border
+        // tiles staged it with the mirror applied, so take in-frame samples only)
+        const Pix* raw = reinterpret_cast<const Pix*>(smem + ((cnt - 1) & 1) * STAGE);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int r = rbase + 8 * k, y = y0 + r;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int x = x0 + 4 * q + i;
+                if (y < a.h && x < a.w)
+                    reinterpret_cast<Pix*>(a.raw_out + (long long)y * a.raw_pitch)[x] =
+                        raw[(r + 2) * G::RAW_W + G::HX + 4 * q + i];
+            }
+        }
+        return;
+    }
     if (a.store_last && a.n > 0) {
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
@@ -273,7 +344,7 @@ __global__ void __launch_bounds__(NT) motion_tile_kernel(const TileArgs a) {
     }
 }
 
-template <typename Pix, bool FUSED>
+template <typename Pix, bool FUSED, bool V2 = false>
 static cudaError_t launch_one(const TileArgs& a, cudaStream_t s) {
     using G = Geo<Pix>;
     constexpr int STAGE = FUSED ? G::STAGE_FUSED : G::STAGE_MOTION;
@@ -285,13 +356,13 @@ static cudaError_t launch_one(const TileArgs& a, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     const unsigned long long bit = 1ull << (dev & 63);
     if (!(__atomic_load_n(&configured, __ATOMIC_ACQUIRE) & bit)) {
-        e = cudaFuncSetAttribute(motion_tile_kernel<Pix, FUSED>,
+        e = cudaFuncSetAttribute(motion_tile_kernel<Pix, FUSED, V2>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
         if (e != cudaSuccess) return e;
         __atomic_fetch_or(&configured, bit, __ATOMIC_RELEASE);
     }
     dim3 grid((a.w + TW - 1) / TW, (a.h + TH - 1) / TH);
-    motion_tile_kernel<Pix, FUSED><<<grid, NT, SMEM, s>>>(a);
+    motion_tile_kernel<Pix, FUSED, V2><<<grid, NT, SMEM, s>>>(a);
     return cudaGetLastError();
 }
 
@@ -300,6 +371,13 @@ cudaError_t launch_motion_tile(const TileArgs& a, bool fused, cudaStream_t s, in
     *launches += 1;
     if (a.bpc == 8) return fused ? launch_one<uint8_t, true>(a, s) : launch_one<uint8_t, false>(a, s);
     return fused ? launch_one<uint16_t, true>(a, s) : launch_one<uint16_t, false>(a, s);
+}
+
+cudaError_t launch_motion_v2_tile(const TileArgs& a, cudaStream_t s, int* launches) {
+    if (a.n <= 0) return cudaSuccess;
+    *launches += 1;
+    if (a.bpc == 8) return launch_one<uint8_t, false, true>(a, s);
+    return launch_one<uint16_t, false, true>(a, s);
 }
 
 }  // namespace mg

@@ -148,6 +148,40 @@ __device__ __forceinline__ void horizontal_quad(const uint32_t (&wv)[12], uint32
     }
 }
 
+// Unrounded vertical sums of 4 rows x 4 columns (8 staged rows from src).
+__device__ __forceinline__ void vertical_sums(const uint8_t* src, uint32_t (&x)[4][4]) {
+    constexpr int RW = Geo<uint8_t>::RAW_W;
+    uint32_t wv[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) wv[i] = *reinterpret_cast<const uint32_t*>(src + i * RW);
+    uint32_t lo[7], hi[7];
+#pragma unroll
+    for (int i = 0; i < 7; ++i) {
+        lo[i] = __byte_perm(wv[i], wv[i + 1], 0x5140);
+        hi[i] = __byte_perm(wv[i], wv[i + 1], 0x7362);
+    }
+    constexpr uint32_t T01 = kT0 | (kT1 << 16);
+    constexpr uint32_t T23 = kT2 | (kT1 << 16);
+    constexpr uint32_t T_4 = kT0 << 16;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        x[j][0] = __dp2a_lo(T01, lo[j], __dp2a_lo(T23, lo[j + 2], __dp2a_lo(T_4, lo[j + 3], 0u)));
+        x[j][1] = __dp2a_hi(T01, lo[j], __dp2a_hi(T23, lo[j + 2], __dp2a_hi(T_4, lo[j + 3], 0u)));
+        x[j][2] = __dp2a_lo(T01, hi[j], __dp2a_lo(T23, hi[j + 2], __dp2a_lo(T_4, hi[j + 3], 0u)));
+        x[j][3] = __dp2a_hi(T01, hi[j], __dp2a_hi(T23, hi[j + 2], __dp2a_hi(T_4, hi[j + 3], 0u)));
+    }
+}
+__device__ __forceinline__ void vertical_sums(const uint16_t* src, uint32_t (&x)[4][4]) {
+    constexpr int RW = Geo<uint16_t>::RAW_W;
+    uint32_t p[8][4];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) unpack4(src + i * RW, p[i]);
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            x[j][i] = vsum(p[j][i], p[j + 1][i], p[j + 2][i], p[j + 3][i], p[j + 4][i]);
+}
 // Thread layout: each warp owns RPW = 8 output rows of the tile and runs them
 // in two halves of 4 rows through its own 4-row V buffer; 4 warps cover the
 // 32 rows.  Eight rows per warp halve the per-frame cost of stage waits,
@@ -164,9 +198,11 @@ struct Shape {
     static constexpr int LPR = 64 / SPL;          // lanes per chroma row
 };
 
-template <typename Pix, bool FUSED, int STAGES>
+// V2: motion_v2, the blur of prev - cur (see vsum / vdiff); FUSED is false then.
+template <typename Pix, bool FUSED, int STAGES, bool V2>
 __global__ void __launch_bounds__(Shape::NTK, Shape::MINB)
     motion_tma_kernel(const __grid_constant__ TmaMaps maps, const TileArgs a) {
+    static_assert(!(FUSED && V2), "motion_v2 has no fused form");
     using G = Geo<Pix>;
     using SH = Shape;
     constexpr int NWK = SH::NWK, NTK = SH::NTK, RPW = SH::RPW;
@@ -205,6 +241,7 @@ __global__ void __launch_bounds__(Shape::NTK, Shape::MINB)
         }
         fence_mbar_init();
         prefetch_tmap(&maps.raw);
+        if (V2 && a.has_prev) prefetch_tmap(&maps.prev);
         if constexpr (FUSED) {
             prefetch_tmap(&maps.dist);
             prefetch_tmap(&maps.ru);
@@ -218,14 +255,17 @@ __global__ void __launch_bounds__(Shape::NTK, Shape::MINB)
     __syncthreads();
 
     // this CTA's frames: chunk blockIdx.z of the launch; a chunk after the
-    // first starts one frame early to rebuild B_prev (no outputs for it)
+    // first starts one frame early to rebuild B_prev (no outputs for it).
+    // motion_v2 continuing an earlier call starts from that call's last raw
+    // frame (the prev map) in the same way.
     const int chunk = a.chunk > 0 ? a.chunk : a.n;
     const int f_begin = blockIdx.z * chunk;
     const int f_end = min(a.n, f_begin + chunk);
-    const bool warm = blockIdx.z > 0;
+    const bool warm_prev = V2 && blockIdx.z == 0 && a.has_prev;
+    const bool warm = blockIdx.z > 0 || warm_prev;
     const int first = f_begin - (warm ? 1 : 0);
     const int cnt = f_end - first;
-    const bool use_prev = !warm && a.has_prev;
+    const bool use_prev = !V2 && !warm && a.has_prev;
 
     int issued = 0;  // thread 0: frames issued so far
     auto issue = [&](int l) {  // thread 0 only; l = frame index within the chunk
@@ -236,7 +276,10 @@ __global__ void __launch_bounds__(Shape::NTK, Shape::MINB)
         const bool luma_only = warm && l == 0;
         fence_proxy_async();
         mbar_arrive_expect_tx(&full[s], (luma_only ? G::RAW_BYTES : STAGE) + a.tx_extra);
-        tma_load_3d(st, &maps.raw, x0 - G::HX, y0 - 2, f, &full[s]);
+        if (V2 && warm_prev && l == 0)
+            tma_load_3d(st, &maps.prev, x0 - G::HX, y0 - 2, 0, &full[s]);
+        else
+            tma_load_3d(st, &maps.raw, x0 - G::HX, y0 - 2, f, &full[s]);
         if (FUSED && !luma_only) {
             tma_load_3d(st + G::RAW_BYTES, &maps.dist, x0, y0, f, &full[s]);
             unsigned char* sc = st + G::RAW_BYTES + G::DIST_BYTES;
@@ -251,8 +294,11 @@ __global__ void __launch_bounds__(Shape::NTK, Shape::MINB)
         for (int l = 0; l < pre; ++l) issue(l);
     }
 
-    // this thread's outputs: rows RPW w + k, columns 4q .. 4q+3 (q = lane)
+    // this thread's outputs: rows RPW w + k, columns 4q .. 4q+3 (q = lane).
+    // bp holds B of the previous frame -- for motion_v2 the previous frame's
+    // unrounded vertical sums X, and hxp that of the thread's halo value
     const int q = lane;
+    [[maybe_unused]] uint32_t hxp = 0;
     uint32_t bp[RPW][4];
 #pragma unroll
     for (int k = 0; k < RPW; ++k) {
@@ -290,7 +336,7 @@ __global__ void __launch_bounds__(Shape::NTK, Shape::MINB)
     // them.  Warps are at most STAGES frames apart, so two windows suffice.
     auto flush_window = [&](int l) {
         const int jl = (l & ~31) + lane;   // this lane's frame
-        const bool v = jl <= l;
+        const bool v = jl <= l && first + jl >= 0;   // (a warm-up frame may be frame -1)
         const int wb = (l >> 5) & 1;
         if (v) {
             atomicAdd(&wsum[wb][0][lane], (Win)acc_s);
@@ -365,7 +411,13 @@ __global__ void __launch_bounds__(Shape::NTK, Shape::MINB)
             uint32_t hv = 0;
             {
                 const Pix* c = reinterpret_cast<const Pix*>(st + off_halo);
-                hv = vtap(c[0], c[G::RAW_W], c[2 * G::RAW_W], c[3 * G::RAW_W], c[4 * G::RAW_W], rnd, sh);
+                if constexpr (V2) {
+                    const uint32_t x = vsum(c[0], c[G::RAW_W], c[2 * G::RAW_W], c[3 * G::RAW_W], c[4 * G::RAW_W]);
+                    hv = (uint32_t)vdiff<Pix>(hxp, x, rnd, sh);
+                    hxp = x;
+                } else {
+                    hv = vtap(c[0], c[G::RAW_W], c[2 * G::RAW_W], c[3 * G::RAW_W], c[4 * G::RAW_W], rnd, sh);
+                }
             }
             [[maybe_unused]] const bool do_out = l > 0 || !warm;   // not the warm-up frame
             const bool do_sad = l > 0 || use_prev;
@@ -375,9 +427,26 @@ __global__ void __launch_bounds__(Shape::NTK, Shape::MINB)
             for (int h = 0; h < RPW / 4; ++h) {
                 if (h > 0) __syncwarp();   // the previous half has read the V rows
                 // ---- vertical pass of 4 rows (staged row r <-> y0 - 2 + r)
-                uint32_t center[4];
-                vertical_quad(reinterpret_cast<const Pix*>(st + off_vsrc + h * 4 * G::RAW_W * G::S),
-                              sV + 4 + 4 * lane, rnd, sh, center);
+                [[maybe_unused]] uint32_t center[4];
+                if constexpr (V2) {
+                    // V of prev - cur from this frame's sums and the previous frame's
+                    uint32_t x[4][4];
+                    vertical_sums(reinterpret_cast<const Pix*>(st + off_vsrc + h * 4 * G::RAW_W * G::S), x);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        uint4 o;
+                        o.x = (uint32_t)vdiff<Pix>(bp[4 * h + j][0], x[j][0], rnd, sh);
+                        o.y = (uint32_t)vdiff<Pix>(bp[4 * h + j][1], x[j][1], rnd, sh);
+                        o.z = (uint32_t)vdiff<Pix>(bp[4 * h + j][2], x[j][2], rnd, sh);
+                        o.w = (uint32_t)vdiff<Pix>(bp[4 * h + j][3], x[j][3], rnd, sh);
+                        *reinterpret_cast<uint4*>(sV + 4 + 4 * lane + j * SVW) = o;
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) bp[4 * h + j][i] = x[j][i];
+                    }
+                } else {
+                    vertical_quad(reinterpret_cast<const Pix*>(st + off_vsrc + h * 4 * G::RAW_W * G::S),
+                                  sV + 4 + 4 * lane, rnd, sh, center);
+                }
                 if ((halo_r >> 2) == h)
                     sV[(halo_r & 3) * SVW + 4 + halo_off] = hv;
                 __syncwarp();
@@ -390,6 +459,17 @@ __global__ void __launch_bounds__(Shape::NTK, Shape::MINB)
                     const uint4 A = *reinterpret_cast<const uint4*>(v);
                     const uint4 Bq = *reinterpret_cast<const uint4*>(v + 4);
                     const uint4 C = *reinterpret_cast<const uint4*>(v + 8);
+                    if constexpr (V2) {
+                        // SAD of |blur(prev - cur)|; invalid samples add 0
+                        const int wi[12] = {(int)A.x, (int)A.y, (int)A.z, (int)A.w, (int)Bq.x, (int)Bq.y,
+                                            (int)Bq.z, (int)Bq.w, (int)C.x, (int)C.y, (int)C.z, (int)C.w};
+                        int bd[4];
+                        horizontal_quad_signed(wi, bd);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            sad = __sad((INTERIOR || full_tile || i < nvalid[k]) ? bd[i] : 0, 0, sad);
+                        continue;
+                    }
                     const uint32_t wv[12] = {A.x, A.y, A.z, A.w, Bq.x, Bq.y, Bq.z, Bq.w, C.x, C.y, C.z, C.w};
                     uint32_t b[4];
                     horizontal_quad(wv, b);
@@ -494,6 +574,24 @@ __global__ void __launch_bounds__(Shape::NTK, Shape::MINB)
     }
     if (!alive) return;
 
+    if (V2 && a.store_last && cnt > 0 && f_end == a.n) {
+        // motion_v2 keeps the last raw frame for the next call: the tile's
+        // samples from the last frame's stage (no stage is refilled after it;
+        // a border patch only wrote outside the frame)
+        const Pix* raw = reinterpret_cast<const Pix*>(smem + ((cnt - 1) % STAGES) * STAGE);
+#pragma unroll
+        for (int k = 0; k < RPW; ++k) {
+            const int y = y0 + RPW * warp + k;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int x = x0 + 4 * q + i;
+                if (y < a.h && x < a.w)
+                    reinterpret_cast<Pix*>(a.raw_out + (long long)y * a.raw_pitch)[x] =
+                        raw[(RPW * warp + k + 2) * G::RAW_W + G::HX + 4 * q + i];
+            }
+        }
+        return;
+    }
     if (a.store_last && cnt > 0 && f_end == a.n) {
 #pragma unroll
         for (int k = 0; k < RPW; ++k) {
@@ -541,7 +639,7 @@ bool encode(CUtensorMap* m, int bytes_per_sample, const void* base, int w, int h
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <typename Pix, bool FUSED, int STAGES>
+template <typename Pix, bool FUSED, int STAGES, bool V2 = false>
 cudaError_t launch_tma_one(const TmaMaps& maps, const TileArgs& a, cudaStream_t s) {
     using G = Geo<Pix>;
     constexpr int STAGE = FUSED ? G::STAGE_FUSED : G::STAGE_MOTION;
@@ -552,7 +650,7 @@ cudaError_t launch_tma_one(const TmaMaps& maps, const TileArgs& a, cudaStream_t 
     if (e != cudaSuccess) return e;
     const unsigned long long bit = 1ull << (dev & 63);
     if (!(__atomic_load_n(&configured, __ATOMIC_ACQUIRE) & bit)) {
-        e = cudaFuncSetAttribute(motion_tma_kernel<Pix, FUSED, STAGES>,
+        e = cudaFuncSetAttribute(motion_tma_kernel<Pix, FUSED, STAGES, V2>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
         if (e != cudaSuccess) return e;
         __atomic_fetch_or(&configured, bit, __ATOMIC_RELEASE);
@@ -566,7 +664,7 @@ cudaError_t launch_tma_one(const TmaMaps& maps, const TileArgs& a, cudaStream_t 
     int& spm = slots_per_sm[dev & 63];
     if (spm == 0) {
         int per_sm = 0, sms = 0;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, motion_tma_kernel<Pix, FUSED, STAGES>,
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, motion_tma_kernel<Pix, FUSED, STAGES, V2>,
                                                           Shape::NTK, SMEM);
         if (e != cudaSuccess) return e;
         e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -579,7 +677,7 @@ cudaError_t launch_tma_one(const TmaMaps& maps, const TileArgs& a, cudaStream_t 
     double best = 1e30;
     // a launch that reads and writes the same resident plane keeps one chunk:
     // the last chunk's store must not overtake the first chunk's read
-    const bool same_plane = a.has_prev && a.bprev == a.bprev_out;
+    const bool same_plane = !V2 && a.has_prev && a.bprev == a.bprev_out;
     const int max_c = same_plane ? 1 : 8;
     for (int c = 1; c <= max_c && c <= a.n; ++c) {
         const int len = (a.n + c - 1) / c;
@@ -596,7 +694,7 @@ cudaError_t launch_tma_one(const TmaMaps& maps, const TileArgs& a, cudaStream_t 
     }
     b.chunk = (a.n + best_c - 1) / best_c;
     dim3 grid((a.w + TW - 1) / TW, (a.h + TH - 1) / TH, (a.n + b.chunk - 1) / b.chunk);
-    motion_tma_kernel<Pix, FUSED, STAGES><<<grid, Shape::NTK, SMEM, s>>>(maps, b);
+    motion_tma_kernel<Pix, FUSED, STAGES, V2><<<grid, Shape::NTK, SMEM, s>>>(maps, b);
     return cudaGetLastError();
 }
 
@@ -639,6 +737,25 @@ cudaError_t launch_motion_tma(const TileArgs& a, bool fused, cudaStream_t s, int
                      : launch_tma_one<uint8_t, false, 4>(maps, a, s);
     return fused ? launch_tma_one<uint16_t, true, 2>(maps, a, s)
                  : launch_tma_one<uint16_t, false, 4>(maps, a, s);
+}
+
+cudaError_t launch_motion_v2_tma(const TileArgs& a, cudaStream_t s, int* launches, bool* used) {
+    *used = false;
+    if (a.n <= 0) return cudaSuccess;
+    if (!tma_usable(a, false)) return cudaSuccess;
+    if (a.has_prev && (a.raw_pitch % 16 || ((uintptr_t)a.raw_prev & 15))) return cudaSuccess;
+    const int S = a.bpc == 8 ? 1 : 2;
+    TmaMaps maps;
+    std::memset(&maps, 0, sizeof(maps));
+    const int rawW = TW + 2 * (16 / S), rawH = TH + 4;
+    bool ok = encode(&maps.raw, S, a.ref_y, a.w, a.h, a.n, a.pitch_y, a.stride_y, rawW, rawH);
+    if (a.has_prev)
+        ok = ok && encode(&maps.prev, S, a.raw_prev, a.w, a.h, 1, a.raw_pitch, 0, rawW, rawH);
+    if (!ok) return cudaSuccess;  // the caller falls back to the generic kernel
+    *used = true;
+    *launches += 1;
+    if (S == 1) return launch_tma_one<uint8_t, false, 4, true>(maps, a, s);
+    return launch_tma_one<uint16_t, false, 4, true>(maps, a, s);
 }
 
 }  // namespace mg

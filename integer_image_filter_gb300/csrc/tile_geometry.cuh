@@ -53,4 +53,39 @@ __device__ __forceinline__ uint32_t vtap(uint32_t a, uint32_t b, uint32_t c, uin
     return (kT0 * (a + e) + kT1 * (b + d) + kT2 * c + rnd) >> sh;
 }
 
+// motion_v2 helpers.  The blur of prev - cur is linear up to its roundings, so
+// the vertical sum of the difference is the difference of the unrounded
+// vertical sums X = t0 (a + e) + t1 (b + d) + t2 c of the two frames (exact:
+// X < 2^32 for samples < 2^16); it is then rounded with a floor shift.
+__device__ __forceinline__ uint32_t vsum(uint32_t a, uint32_t b, uint32_t c, uint32_t d,
+                                         uint32_t e) {
+    return kT0 * (a + e) + kT1 * (b + d) + kT2 * c;
+}
+// floor((xp - x + rnd) / 2^sh): 32-bit for 8-bit samples (|xp - x| < 2^24),
+// 64-bit above (33 bits with sign).
+template <typename Pix>
+__device__ __forceinline__ int vdiff(uint32_t xp, uint32_t x, uint32_t rnd, int sh) {
+    if constexpr (sizeof(Pix) == 1)
+        return ((int)xp - (int)x + (int)rnd) >> sh;
+    else
+        return (int)(((long long)xp - (long long)x + (long long)rnd) >> sh);
+}
+// The horizontal pass on signed V: the same window sums as horizontal_quad,
+// the products and the rounding in 64 bits (|sum| < 2^32 + 2^15 needs 33
+// bits with sign), floor shift >> 16.
+__device__ __forceinline__ void horizontal_quad_signed(const int (&wv)[12], int (&b)[4]) {
+    int w3 = wv[3] + wv[4] + wv[5];
+    int w5 = w3 + wv[2] + wv[6];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        if (i > 0) {
+            w3 = w3 + wv[5 + i] - wv[2 + i];
+            w5 = w5 + wv[6 + i] - wv[1 + i];
+        }
+        const long long t = (long long)kT0 * w5 + (long long)(kT1 - kT0) * w3 +
+                            (long long)(kT2 - kT1) * wv[4 + i] + 32768LL;
+        b[i] = (int)(t >> 16);
+    }
+}
+
 }  // namespace mg
