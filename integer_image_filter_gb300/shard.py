@@ -6,7 +6,9 @@ one-frame halo), so its first SAD is against frame s_r - 1 exactly as in the
 unsharded sequence.  The only cross-rank value is the score of the first frame
 of the next shard, which the last frame of each shard needs for motion2
 (motion2_i = min(score_i, score_{i+1})); it is exchanged once on the host.
-Independent sequences (or picture pairs) need no exchange at all.
+Independent sequences (or picture pairs) need no exchange at all.  motion_v2
+(the blur of prev - cur) needs exactly the same one-frame halo, so the same
+shards serve it; the moment sums are per pair and split by pairs.
 """
 from __future__ import annotations
 

@@ -24,8 +24,8 @@ def iif():
     return m
 
 
-@pytest.mark.parametrize("fused", [False, True])
-def test_stage_wait_times_out_and_context_recovers(iif, oracle, fused):
+@pytest.mark.parametrize("mode", ["motion", "fused", "motion_v2"])
+def test_stage_wait_times_out_and_context_recovers(iif, oracle, mode):
     import torch
     w, h, n = 640, 160, 3                     # 16-byte rows: the TMA kernel; interior and border tiles
     b = synth.yuv420_pairs(31, n, w, h)
@@ -34,20 +34,24 @@ def test_stage_wait_times_out_and_context_recovers(iif, oracle, fused):
     with iif.MotionContext(w, h, 8) as ctx:
         assert ctx.device_error() == 0
         iif.motion_set_stall_injection(ctx.handle, True)
-        if fused:
-            ctx.yuv420_batch(*planes, sad, sse)
-        else:
-            ctx.submit_batch(planes[0], sad)
+        run(ctx, mode, planes, sad, sse)
         torch.cuda.synchronize()               # the launch ends: the waits are bounded
         flags = ctx.device_error()
         assert flags & 1, flags
         assert ctx.device_error() == 0          # read and cleared
         iif.motion_set_stall_injection(ctx.handle, False)
         ctx.reset()
-        if fused:
-            ctx.yuv420_batch(*planes, sad, sse)
-        else:
-            ctx.submit_batch(planes[0], sad)
+        run(ctx, mode, planes, sad, sse)
         torch.cuda.synchronize()
         assert ctx.device_error() == 0
-    assert np.array_equal(to_u64(sad), oracle.motion_sad_sequence(b.ref_y, 8))
+    seq = oracle.motion_v2_sequence if mode == "motion_v2" else oracle.motion_sad_sequence
+    assert np.array_equal(to_u64(sad), seq(b.ref_y, 8))
+
+
+def run(ctx, mode, planes, sad, sse):
+    if mode == "fused":
+        ctx.yuv420_batch(*planes, sad, sse)
+    elif mode == "motion_v2":
+        ctx.submit_batch_v2(planes[0], sad)
+    else:
+        ctx.submit_batch(planes[0], sad)

@@ -58,7 +58,7 @@ def test_10bit_4k_consecutive_frames(iif, oracle):
     assert np.array_equal(got, oracle_moments(oracle, f[:-1], f[1:], 10))
 
 
-@pytest.mark.parametrize("bpc", [8, 10, 12, 16])
+@pytest.mark.parametrize("bpc", [8, 9, 10, 12, 15, 16])
 @pytest.mark.parametrize("wh", [(1, 1), (3, 3), (17, 5), (64, 48), (1000, 3), (1921, 1081)])
 def test_depths_and_sizes(iif, oracle, bpc, wh):
     w, h = wh

@@ -155,3 +155,22 @@ def test_constant_frames_closed_form_large(iif):
             torch.cuda.synchronize()
         exp = abs(c1 - c2) * (1 << (16 - bpc)) * w * h
         assert [int(x) for x in out.cpu()] == [0, exp, exp, exp], bpc
+
+
+@pytest.mark.parametrize("bpc", [9, 12, 15])
+def test_other_depths(iif, oracle, bpc):
+    rng = np.random.default_rng(bpc)
+    w, h = 200, 70
+    frames = rng.integers(0, 1 << bpc, size=(6, h, w)).astype(np.uint16)
+    want = oracle.motion_v2_sequence(frames, bpc)
+    assert np.array_equal(run_v2(iif, padded_dev(frames), w, h, bpc, 4), want)
+    assert np.array_equal(run_v2(iif, to_dev(frames), w, h, bpc, 6), want)
+
+
+def test_long_batch_many_chunks(iif, oracle):
+    """200 frames of a small frame in one launch: few tiles, so the launch is
+    split into frame chunks, each re-deriving its warm-up frame's sums."""
+    frames = synth.smooth_sequence(77, 200, 130, 36, 2)
+    want = oracle.motion_v2_sequence(frames, 8)
+    assert np.array_equal(run_v2(iif, padded_dev(frames), 130, 36, 8, 200), want)
+    assert np.array_equal(run_v2(iif, padded_dev(frames), 130, 36, 8, 37), want)

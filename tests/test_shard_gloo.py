@@ -30,7 +30,7 @@ def test_shards_cover_each_frame_once(n, world):
     assert got == list(range(n))
 
 
-def _worker(rank, world, port, frames, want_score, want_m2, result_q):
+def _worker(rank, world, port, frames, want_score, want_m2, result_q, variant="motion"):
     import torch.distributed as dist
 
     import oracle
@@ -45,7 +45,8 @@ def _worker(rank, world, port, frames, want_score, want_m2, result_q):
         o = oracle.Oracle()
         n, h, w = frames.shape
         sh = shard_frames(n, world, rank)
-        sad = o.motion_sad_sequence(frames[sh.read_from:sh.end], 8)
+        seq = o.motion_v2_sequence if variant == "motion_v2" else o.motion_sad_sequence
+        sad = seq(np.ascontiguousarray(frames[sh.read_from:sh.end]), 8)
         if sh.drop_first:
             sad = sad[1:]
         score, m2 = stitch_motion2(sad, sh, w, h)
@@ -56,18 +57,20 @@ def _worker(rank, world, port, frames, want_score, want_m2, result_q):
         dist.destroy_process_group()
 
 
-def test_sharded_sequence_matches_unsharded():
+@pytest.mark.parametrize("variant", ["motion", "motion_v2"])
+def test_sharded_sequence_matches_unsharded(variant):
     import oracle
     import synth
     frames = synth.smooth_sequence(21, 9, 64, 40, 2)
     o = oracle.Oracle()
-    sad = o.motion_sad_sequence(frames, 8)
+    sad = (o.motion_v2_sequence if variant == "motion_v2" else o.motion_sad_sequence)(frames, 8)
     want_score, want_m2 = o.scores(sad, 64, 40)
     world = 2
     ctx = mp.get_context("spawn")
     q = ctx.Queue()
     port = _free_port()
-    procs = [ctx.Process(target=_worker, args=(r, world, port, frames, want_score, want_m2, q))
+    procs = [ctx.Process(target=_worker, args=(r, world, port, frames, want_score, want_m2, q,
+                                               variant))
              for r in range(world)]
     for p in procs:
         p.start()
