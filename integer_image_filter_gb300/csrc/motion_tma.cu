@@ -12,8 +12,10 @@
 //    box with its 2-row and 16-byte halo -- and, fused, the distorted luma
 //    tile and the four chroma tiles -- completing on that stage's mbarrier.
 //    Out-of-frame parts of a box arrive zero-filled; tiles on the frame border
-//    then write the mirrored halo in shared memory (i<0 -> -i, i>=n -> 2n-i-2),
-//    so no tile takes a sample-by-sample path.
+//    read rows through a per-CTA table of mirrored rows (i<0 -> -i,
+//    i>=n -> 2n-i-2) and mirror the V columns of their own rows, so no tile
+//    takes a sample-by-sample path and no block barrier is left in the frame
+//    loop.
 //  * Separable blur: the vertical 5-tap pass once per sample (rounded >> bpc)
 //    into a shared V tile, then the horizontal 5-tap pass (rounded >> 16)
 //    ("ADR-1392: CUDA motion, PSNR and moment kernels add one atomic per
@@ -23,8 +25,7 @@
 //    warps add their lanes into the block's window sums in shared memory and
 //    the last warp adds each accumulator of each frame to its 64-bit output
 //    with ONE atomic (same page, Decision 1; integer sums are
-//    order-independent, so the result is exact -- Context).  No block-wide
-//    barrier is left in the frame loop of interior tiles.
+//    order-independent, so the result is exact -- Context).
 //  * Every mbarrier wait is bounded: on time-out a warp raises the device
 //    error word and leaves instead of spinning; thread 0 waits (bounded) for
 //    the copies it issued before the block exits.
@@ -40,56 +41,18 @@ namespace mg {
 
 constexpr long long kWaitCycles = 1LL << 31;  // default wait bound: about one second
 
-// Mirror the halo of a staged luma box in place for tiles on the frame border.
-template <typename Pix, int NTK>
-__device__ __forceinline__ void patch_mirror(Pix* raw, const TileArgs& a, int x0, int y0,
-                                             bool pl, bool pr, bool pt, bool pb) {
-    using G = Geo<Pix>;
-    const int tid = threadIdx.x;
-    // columns first (every staged row), then whole rows (so corners follow)
-    if (pl || pr) {
-        const int cw0 = a.w - x0 + G::HX;  // staged column of x = w
-        for (int i = tid; i < 4 * G::RAW_ROWS; i += NTK) {
-            const int r = i >> 2, which = i & 3;
-            Pix* row = raw + r * G::RAW_W;
-            if (which < 2) {
-                if (pl) row[G::HX - 1 - which] = row[G::HX + 1 + which];    // x=-1,-2 <- 1,2
-            } else if (pr) {
-                const int k = which - 2;                                      // x=w+k <- w-2-k
-                row[cw0 + k] = row[cw0 - 2 - k];
-            }
-        }
-        __syncthreads();
-    }
-    if (pt || pb) {
-        const int rh = a.h - y0 + 2;      // staged row of y = h
-        for (int i = tid; i < 4 * G::RAW_W; i += NTK) {
-            const int which = i / G::RAW_W, c = i - which * G::RAW_W;
-            if (which < 2) {
-                if (pt) raw[(1 - which) * G::RAW_W + c] = raw[(3 + which) * G::RAW_W + c];  // y=-1,-2 <- 1,2
-            } else if (pb) {
-                const int k = which - 2;                                   // y=h+k <- h-2-k
-                if (rh + k < G::RAW_ROWS) raw[(rh + k) * G::RAW_W + c] = raw[(rh - 2 - k) * G::RAW_W + c];
-            }
-        }
-        __syncthreads();
-    }
-    // these generic writes precede a later TMA refill of the same stage
-    fence_proxy_async();
-}
-
-// The vertical 5-tap pass for one warp: 4 output rows (8 staged rows from
-// src feed them) x 128 columns, lane = quad of 4 columns; result V (uint32) into
+// The vertical 5-tap pass for one warp: 4 output rows (8 staged rows, at
+// element offsets ro(0..7) from the lane's column src, feed them) x 128 columns, lane = quad of 4 columns; result V (uint32) into
 // the warp's own rows of sV, and the 4 centre-row words (the reference luma
 // of the warp's output rows) for the squared error.  8-bit samples use
 // byte-pair dot products: rows are interleaved two at a time so that one dp2a
 // applies two taps to two rows of one column (exact: sums stay below 2^24).
-__device__ __forceinline__ void vertical_quad(const uint8_t* src, uint32_t* dst, uint32_t rnd,
-                                              int sh, uint32_t (&center)[4]) {
-    constexpr int RW = Geo<uint8_t>::RAW_W;
+template <typename RowOff>
+__device__ __forceinline__ void vertical_quad(const uint8_t* src, RowOff ro, uint32_t* dst,
+                                              uint32_t rnd, int sh, uint32_t (&center)[4]) {
     uint32_t wv[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) wv[i] = *reinterpret_cast<const uint32_t*>(src + i * RW);
+    for (int i = 0; i < 8; ++i) wv[i] = *reinterpret_cast<const uint32_t*>(src + ro(i));
 #pragma unroll
     for (int i = 0; i < 4; ++i) center[i] = wv[i + 2];
     uint32_t lo[7], hi[7];  // rows (i, i+1): columns 0,1 in lo, columns 2,3 in hi
@@ -111,12 +74,12 @@ __device__ __forceinline__ void vertical_quad(const uint8_t* src, uint32_t* dst,
         *reinterpret_cast<uint4*>(dst + j * SVW) = o;
     }
 }
-__device__ __forceinline__ void vertical_quad(const uint16_t* src, uint32_t* dst, uint32_t rnd,
-                                              int sh, uint32_t (&center)[4]) {
-    constexpr int RW = Geo<uint16_t>::RAW_W;
+template <typename RowOff>
+__device__ __forceinline__ void vertical_quad(const uint16_t* src, RowOff ro, uint32_t* dst,
+                                              uint32_t rnd, int sh, uint32_t (&center)[4]) {
     uint32_t p[8][4];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) unpack4(src + i * RW, p[i]);
+    for (int i = 0; i < 8; ++i) unpack4(src + ro(i), p[i]);
 #pragma unroll
     for (int i = 0; i < 4; ++i) center[i] = 0;  // 16-bit SSE reloads its samples
 #pragma unroll
@@ -149,11 +112,11 @@ __device__ __forceinline__ void horizontal_quad(const uint32_t (&wv)[12], uint32
 }
 
 // Unrounded vertical sums of 4 rows x 4 columns (8 staged rows from src).
-__device__ __forceinline__ void vertical_sums(const uint8_t* src, uint32_t (&x)[4][4]) {
-    constexpr int RW = Geo<uint8_t>::RAW_W;
+template <typename RowOff>
+__device__ __forceinline__ void vertical_sums(const uint8_t* src, RowOff ro, uint32_t (&x)[4][4]) {
     uint32_t wv[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) wv[i] = *reinterpret_cast<const uint32_t*>(src + i * RW);
+    for (int i = 0; i < 8; ++i) wv[i] = *reinterpret_cast<const uint32_t*>(src + ro(i));
     uint32_t lo[7], hi[7];
 #pragma unroll
     for (int i = 0; i < 7; ++i) {
@@ -171,11 +134,11 @@ __device__ __forceinline__ void vertical_sums(const uint8_t* src, uint32_t (&x)[
         x[j][3] = __dp2a_hi(T01, hi[j], __dp2a_hi(T23, hi[j + 2], __dp2a_hi(T_4, hi[j + 3], 0u)));
     }
 }
-__device__ __forceinline__ void vertical_sums(const uint16_t* src, uint32_t (&x)[4][4]) {
-    constexpr int RW = Geo<uint16_t>::RAW_W;
+template <typename RowOff>
+__device__ __forceinline__ void vertical_sums(const uint16_t* src, RowOff ro, uint32_t (&x)[4][4]) {
     uint32_t p[8][4];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) unpack4(src + i * RW, p[i]);
+    for (int i = 0; i < 8; ++i) unpack4(src + ro(i), p[i]);
 #pragma unroll
     for (int j = 0; j < 4; ++j)
 #pragma unroll
@@ -220,6 +183,9 @@ __global__ void __launch_bounds__(Shape::NTK, Shape::MINB)
     using Win = typename std::conditional<sizeof(Pix) == 1, uint32_t, unsigned long long>::type;
     __shared__ __align__(16) Win wsum[2][4][32];
     __shared__ int wcount[2];
+    // border tiles: element offset of the staged row that holds each staged
+    // row after the mirror rule (frame-invariant, filled once)
+    __shared__ int rowsrc[Geo<Pix>::RAW_ROWS];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     // each warp owns output rows RPW w .. RPW w + RPW-1 of the tile; its V rows are private
@@ -252,6 +218,16 @@ __global__ void __launch_bounds__(Shape::NTK, Shape::MINB)
         wcount[0] = wcount[1] = 0;
     }
     for (int i = tid; i < 2 * 4 * 32; i += NTK) (&wsum[0][0][0])[i] = 0;
+    if (tid < G::RAW_ROWS) {
+        // mirror on read: the boxes arrive zero-filled outside the frame; a row
+        // y0 - 2 + r outside [0, h) is read from its mirror, clamped into the
+        // box for rows that only feed outputs outside the frame
+        int y = y0 - 2 + tid;
+        y = y < 0 ? -y : (y >= a.h ? 2 * a.h - 2 - y : y);
+        int rr = y - (y0 - 2);
+        rr = rr < 0 ? 0 : (rr > G::RAW_ROWS - 1 ? G::RAW_ROWS - 1 : rr);
+        rowsrc[tid] = rr * G::RAW_W;
+    }
     __syncthreads();
 
     // this CTA's frames: chunk blockIdx.z of the launch; a chunk after the
@@ -317,10 +293,13 @@ __global__ void __launch_bounds__(Shape::NTK, Shape::MINB)
         nvalid[k] = nv < 0 ? 0 : (nv > 4 ? 4 : nv);
     }
     // per-thread byte offsets inside a stage (the same for every stage)
-    const int off_vsrc = ((warp * RPW) * G::RAW_W + G::HX + 4 * lane) * G::S;  // half h: + 4h rows
+    const int off_vcol = (G::HX + 4 * lane) * G::S;   // this lane's columns in staged row 0
     const int halo_r = lane >> 2, halo_which = lane & 3;   // halo row 0..7, column
     const int halo_off = halo_which == 0 ? -2 : halo_which == 1 ? -1 : halo_which == 2 ? TW : TW + 1;
-    const int off_halo = ((warp * RPW + halo_r) * G::RAW_W + G::HX + halo_off) * G::S;
+    const int off_hcol = (G::HX + halo_off) * G::S;   // the halo lane's column in staged row 0
+    // only warps whose rows reach above row 0 or below row h - 1 read rows
+    // through rowsrc
+    const bool wmirror = (pt && RPW * warp < 2) || (pb && RPW * warp + RPW + 3 >= a.h - y0 + 2);
     const int off_ref = ((RPW * warp + 2) * G::RAW_W + G::HX + 4 * q) * G::S;   // row k: + k RAW_W S
     const int off_dist = G::RAW_BYTES + ((RPW * warp) * TW + 4 * q) * G::S;     // row k: + k TW S
     const int off_chroma = G::RAW_BYTES + G::DIST_BYTES +
@@ -371,9 +350,9 @@ __global__ void __launch_bounds__(Shape::NTK, Shape::MINB)
         }
     };
 
-    // The frame loop, compiled twice: for interior tiles (no mirror patch, no
-    // masks, no block barrier) and for tiles on the frame border.  A runtime
-    // test per frame costs the interior tiles several percent.
+    // The frame loop, compiled twice: for interior tiles (no mirrored reads,
+    // no masks) and for tiles on the frame border.  A runtime test per frame
+    // costs the interior tiles several percent.
     auto frames = [&](auto interior_tag) -> bool {
         constexpr bool INTERIOR = decltype(interior_tag)::value;
         for (int l = 0; l < cnt; ++l) {
@@ -391,32 +370,28 @@ __global__ void __launch_bounds__(Shape::NTK, Shape::MINB)
                 else
                     timed_out = true;
             }
-            if (INTERIOR || !edge) {
-                // a stage that never landed: this warp records it and leaves (the
-                // others then run out of stages and leave too)
-                if (__any_sync(0xffffffffu, !ok)) {
-                    if (lane == 0 && a.err) atomicOr(a.err, 1);
-                    return false;
-                }
-            } else {
-                // border tiles write the mirrored halo together (block barriers)
-                if (!__syncthreads_and(ok)) {
-                    if (tid == 0 && a.err) atomicOr(a.err, 1);
-                    return false;
-                }
-                patch_mirror<Pix, NTK>(reinterpret_cast<Pix*>(st), a, x0, y0, pl, pr, pt, pb);
+            // a stage that never landed: this warp records it and leaves (the
+            // others then run out of stages and leave too)
+            if (__any_sync(0xffffffffu, !ok)) {
+                if (lane == 0 && a.err) atomicOr(a.err, 1);
+                return false;
             }
+            const bool remap = !INTERIOR && wmirror;   // warp-uniform
 
             // ---- halo columns (two on each side) of the warp's rows: lane = (row, column)
             uint32_t hv = 0;
             {
-                const Pix* c = reinterpret_cast<const Pix*>(st + off_halo);
+                const Pix* c = reinterpret_cast<const Pix*>(st + off_hcol);
+                const int hr = RPW * warp + halo_r;
+                uint32_t t[5];
+#pragma unroll
+                for (int k = 0; k < 5; ++k) t[k] = c[remap ? rowsrc[hr + k] : (hr + k) * G::RAW_W];
                 if constexpr (V2) {
-                    const uint32_t x = vsum(c[0], c[G::RAW_W], c[2 * G::RAW_W], c[3 * G::RAW_W], c[4 * G::RAW_W]);
+                    const uint32_t x = vsum(t[0], t[1], t[2], t[3], t[4]);
                     hv = (uint32_t)vdiff<Pix>(hxp, x, rnd, sh);
                     hxp = x;
                 } else {
-                    hv = vtap(c[0], c[G::RAW_W], c[2 * G::RAW_W], c[3 * G::RAW_W], c[4 * G::RAW_W], rnd, sh);
+                    hv = vtap(t[0], t[1], t[2], t[3], t[4], rnd, sh);
                 }
             }
             [[maybe_unused]] const bool do_out = l > 0 || !warm;   // not the warm-up frame
@@ -431,7 +406,12 @@ __global__ void __launch_bounds__(Shape::NTK, Shape::MINB)
                 if constexpr (V2) {
                     // V of prev - cur from this frame's sums and the previous frame's
                     uint32_t x[4][4];
-                    vertical_sums(reinterpret_cast<const Pix*>(st + off_vsrc + h * 4 * G::RAW_W * G::S), x);
+                    const Pix* colv = reinterpret_cast<const Pix*>(st + off_vcol);
+                    const int r0 = RPW * warp + 4 * h;
+                    if (remap)
+                        vertical_sums(colv, [&](int i) { return rowsrc[r0 + i]; }, x);
+                    else
+                        vertical_sums(colv, [=](int i) { return (r0 + i) * G::RAW_W; }, x);
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
                         uint4 o;
@@ -444,12 +424,36 @@ __global__ void __launch_bounds__(Shape::NTK, Shape::MINB)
                         for (int i = 0; i < 4; ++i) bp[4 * h + j][i] = x[j][i];
                     }
                 } else {
-                    vertical_quad(reinterpret_cast<const Pix*>(st + off_vsrc + h * 4 * G::RAW_W * G::S),
-                                  sV + 4 + 4 * lane, rnd, sh, center);
+                    const Pix* colv = reinterpret_cast<const Pix*>(st + off_vcol);
+                    const int r0 = RPW * warp + 4 * h;
+                    if (remap)
+                        vertical_quad(colv, [&](int i) { return rowsrc[r0 + i]; },
+                                      sV + 4 + 4 * lane, rnd, sh, center);
+                    else
+                        vertical_quad(colv, [=](int i) { return (r0 + i) * G::RAW_W; },
+                                      sV + 4 + 4 * lane, rnd, sh, center);
                 }
                 if ((halo_r >> 2) == h)
                     sV[(halo_r & 3) * SVW + 4 + halo_off] = hv;
                 __syncwarp();
+                if (!INTERIOR && (pl || pr)) {
+                    // the column mirror on V (the vertical pass works per column):
+                    // x = -1, -2 <- 1, 2 on the left edge, x = w + k <- w - 2 - k on
+                    // the right edge, in this warp's 4 V rows; no source is a target
+                    if (lane < 16) {
+                        const int row = lane >> 2, which = lane & 3;
+                        int dc = -3, sc = 0;
+                        if (which < 2) {
+                            if (pl) { dc = -1 - which; sc = 1 + which; }
+                        } else if (pr) {
+                            const int k = which - 2;
+                            dc = a.w - x0 + k;
+                            sc = a.w - x0 - 2 - k;
+                        }
+                        if (dc >= -2 && dc <= TW + 1) sV[row * SVW + 4 + dc] = sV[row * SVW + 4 + sc];
+                    }
+                    __syncwarp();
+                }
 
                 // ---- horizontal pass, SAD against B_prev, squared errors
 #pragma unroll
@@ -576,8 +580,7 @@ __global__ void __launch_bounds__(Shape::NTK, Shape::MINB)
 
     if (V2 && a.store_last && cnt > 0 && f_end == a.n) {
         // motion_v2 keeps the last raw frame for the next call: the tile's
-        // samples from the last frame's stage (no stage is refilled after it;
-        // a border patch only wrote outside the frame)
+        // samples from the last frame's stage (no stage is refilled after it)
         const Pix* raw = reinterpret_cast<const Pix*>(smem + ((cnt - 1) % STAGES) * STAGE);
 #pragma unroll
         for (int k = 0; k < RPW; ++k) {
