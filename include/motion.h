@@ -160,9 +160,10 @@ MOTION_API int motion_psnr_yuv420_batch_host(motion_ctx* ctx, int n,
 
 /* Allocate the two device staging sets, result buffers and streams used by
  * motion_psnr_yuv420_batch_host, for chunks of `pairs_per_chunk` pairs whose
- * planes are stride_y / stride_uv bytes apart (0 picks about 64 MB of pictures
- * per chunk; a stride of 0 means tightly packed rows).  Kept until destroy;
- * a later call with a larger need reallocates. */
+ * planes are stride_y / stride_uv bytes apart (0 picks about 256 MB of
+ * pictures per chunk, 1 to 64 pairs, so the two sets take about 512 MB of
+ * device memory; a stride of 0 means tightly packed rows).  Kept until
+ * destroy; a later call with a larger need reallocates. */
 MOTION_API int motion_reserve_host_staging(motion_ctx* ctx, int pairs_per_chunk,
                                 size_t stride_y, size_t stride_uv);
 

@@ -360,9 +360,10 @@ int motion_reserve_host_staging(motion_ctx* c, int pairs_per_chunk, size_t strid
     if (stride_y == 0) stride_y = (size_t)c->w * s * (size_t)c->h;
     if (stride_uv == 0) stride_uv = (size_t)c->cw * s * (size_t)c->ch;
     if (pairs_per_chunk == 0) {
-        // about 64 MB of pictures per chunk, at least one pair
+        // about 256 MB of pictures per chunk (copies of that size run at the
+        // host link's rate; 64 MB chunks lost ~4 %), at least one pair
         const size_t pair_bytes = 2 * (stride_y + 2 * stride_uv);
-        pairs_per_chunk = (int)((size_t)64 << 20) / (int)(pair_bytes ? pair_bytes : 1);
+        pairs_per_chunk = (int)(((size_t)256 << 20) / (pair_bytes ? pair_bytes : 1));
         if (pairs_per_chunk < 1) pairs_per_chunk = 1;
         if (pairs_per_chunk > 64) pairs_per_chunk = 64;
     }
