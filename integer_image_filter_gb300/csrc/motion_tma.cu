@@ -658,11 +658,15 @@ cudaError_t launch_tma_one(const TmaMaps& maps, const TileArgs& a, cudaStream_t 
         if (e != cudaSuccess) return e;
         __atomic_fetch_or(&configured, bit, __ATOMIC_RELEASE);
     }
-    // Size the launch by the SM count (ADR-1226): split the frames into
-    // chunks so that tiles x chunks fill whole waves of resident CTAs.  A
-    // chunk after the first pays one warm-up frame and every chunk its own
-    // pipeline fill (about half a frame), so the split is chosen by
-    //   cost(c) = (n + (c - 1) + c / 2) / n / (waves / ceil(waves)).
+    // Size the launch by the SM count (ADR-1226): split the frames into c
+    // chunks run by separate CTAs.  A chunk after the first pays one warm-up
+    // frame and every chunk its own pipeline fill (about half a frame); the
+    // idle part of the last wave and, under 2.5 waves, the pipeline fills that
+    // other CTAs cannot cover are paid too.  Chunks keep at least 5 frames.
+    //   cost(c) = (n + (c - 1) + c / 2) / n / eff,
+    //   eff = (waves / ceil(waves)) * min(1, waves / 2.5), waves = tiles c / slots.
+    // (Measured: 1080p x 32 frames is fastest at 3-5 chunks, x 8 at one; 4K
+    // x 32 or 50 at two.)
     static int slots_per_sm[64] = {0};
     int& spm = slots_per_sm[dev & 63];
     if (spm == 0) {
@@ -684,12 +688,13 @@ cudaError_t launch_tma_one(const TmaMaps& maps, const TileArgs& a, cudaStream_t 
     const int max_c = same_plane ? 1 : 8;
     for (int c = 1; c <= max_c && c <= a.n; ++c) {
         const int len = (a.n + c - 1) / c;
+        if (c > 1 && len < 5) break;
         const int cz = (a.n + len - 1) / len;
         const double units = (double)tiles * cz;
         const double waves = units / spm;
-        const double fill = waves / std::ceil(waves);
+        const double eff = waves / std::ceil(waves) * (waves < 2.5 ? waves / 2.5 : 1.0);
         const double work = (a.n + (cz - 1) + 0.5 * cz) / a.n;
-        const double cost = work / fill;
+        const double cost = work / eff;
         if (cost < best - 1e-9) {
             best = cost;
             best_c = cz;

@@ -157,8 +157,8 @@ def test_tiny_and_ragged_frames(iif, oracle, bpc):
 
 @pytest.mark.parametrize("bpc", [8, 10, 16])
 def test_tma_and_generic_paths_on_aligned_layouts(iif, oracle, bpc):
-    """16-byte-aligned pitches: the TMA kernel (mirror halo written in shared
-    memory on border tiles) and the generic kernel both equal the oracle."""
+    """16-byte-aligned pitches: the TMA kernel (mirrored reads on border tiles)
+    and the generic kernel (mirror applied at load) both equal the oracle."""
     rng = np.random.default_rng(100 + bpc)
     for (w, h) in SIZES:
         frames = synth.uniform_frames(int(rng.integers(1 << 30)), 4, w, h, bpc)
@@ -284,6 +284,16 @@ def test_symmetry_and_identity_on_gpu(iif):
 
 
 # --------------------------------------------------------------- sequence state
+def test_long_batches_many_chunks(iif, oracle):
+    """200 frames of a small frame per launch: the launch splits the frames
+    into chunks (each after the first re-blurs a warm-up frame), continuing
+    the sequence across launches of 37 frames as well."""
+    frames = synth.smooth_sequence(78, 200, 130, 36, 2)
+    want = oracle.motion_sad_sequence(frames, 8)
+    for batch in (200, 37):
+        assert np.array_equal(run_batches(iif, frames, 8, batch, padded=True), want), batch
+
+
 def test_batch_continuity_and_reset(iif, oracle):
     import torch
     frames = synth.make("seq_576x324_u8", n=16)
