@@ -20,6 +20,7 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import re
 import os
 import statistics
 import subprocess
@@ -67,12 +68,21 @@ def peaks():
 KERNEL_SOURCES = ("motion_tma.cu", "tile_geometry.cuh", "motion_common.cuh", "motion_internal.h")
 
 
+def _code_tokens(text: str) -> bytes:
+    """The source without comments and with whitespace runs collapsed, so that
+    a comment or layout edit does not count as a kernel change (string
+    literals in these sources hold no comment markers)."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split()).encode()
+
+
 def kernel_source_hash() -> str:
     csrc = os.path.join(ROOT, "integer_image_filter_gb300", "csrc")
     h = hashlib.sha256()
     for f in KERNEL_SOURCES:
-        with open(os.path.join(csrc, f), "rb") as fh:
-            h.update(f.encode() + b"\0" + fh.read())
+        with open(os.path.join(csrc, f), encoding="utf-8") as fh:
+            h.update(f.encode() + b"\0" + _code_tokens(fh.read()))
     return h.hexdigest()[:16]
 
 

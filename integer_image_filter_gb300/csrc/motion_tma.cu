@@ -41,12 +41,13 @@ namespace mg {
 
 constexpr long long kWaitCycles = 1LL << 31;  // default wait bound: about one second
 
-// The vertical 5-tap pass for one warp: 4 output rows (8 staged rows, at
-// element offsets ro(0..7) from the lane's column src, feed them) x 128 columns, lane = quad of 4 columns; result V (uint32) into
-// the warp's own rows of sV, and the 4 centre-row words (the reference luma
-// of the warp's output rows) for the squared error.  8-bit samples use
-// byte-pair dot products: rows are interleaved two at a time so that one dp2a
-// applies two taps to two rows of one column (exact: sums stay below 2^24).
+// The vertical 5-tap pass for one warp: 4 output rows x 128 columns, fed by 8
+// staged rows at element offsets ro(0..7) from the lane's column src (lane =
+// quad of 4 columns); result V (uint32) into the warp's own rows of sV, and
+// the 4 centre-row words (the reference luma of the warp's output rows) for
+// the squared error.  8-bit samples use byte-pair dot products: rows are
+// interleaved two at a time so that one dp2a applies two taps to two rows of
+// one column (exact: sums stay below 2^24).
 template <typename RowOff>
 __device__ __forceinline__ void vertical_quad(const uint8_t* src, RowOff ro, uint32_t* dst,
                                               uint32_t rnd, int sh, uint32_t (&center)[4]) {
