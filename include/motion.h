@@ -228,6 +228,18 @@ MOTION_API int psnr_from_sse(uint64_t sse, uint64_t n_samples, int bpc, double* 
 #define MOTION_PATH_GENERIC 1
 MOTION_API int motion_set_kernel_path(motion_ctx* ctx, int path);
 
+/* Diagnostic, host only, no GPU: the number of frame chunks (1..8) a batched
+ * launch of n frames of w x h splits into on a device where `resident_ctas`
+ * motion CTAs run at once (4 per SM on GB300: 608).  The launch sizing
+ * follows "ADR-1226: Size the CUDA AIM CM launch by SM count, not by a fixed
+ * rows-per-thread": chunks after the first re-blur one warm-up frame, and
+ * the count balances that work against the idle part of the last wave.
+ * *chunks_out (host int) receives the count.  Errors:
+ * MOTION_ERR_INVALID_ARGUMENT (w, h < 1, n < 0, resident_ctas < 1, NULL
+ * chunks_out).  A launch that continues a sequence in place (the
+ * allocation-free entry point) always uses one chunk. */
+MOTION_API int motion_plan_chunks(int w, int h, int n, int resident_ctas, int* chunks_out);
+
 /* Test hook for the kernels' bounded waits (no counterpart in the paper):
  * while on, TMA launches on this context expect 16 bytes per stage more than
  * their boxes deliver, so no stage wait can complete, and bound every wait at

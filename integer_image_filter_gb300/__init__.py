@@ -27,7 +27,7 @@ __all__ = [
     "motion_kernel_launch_count", "motion_strerror", "MotionContext", "EXPORTED_SYMBOLS",
     "motion_set_kernel_path", "motion_device_error", "MOTION_PATH_AUTO", "MOTION_PATH_GENERIC",
     "motion_submit_batch_noalloc", "motion_set_stall_injection", "moment_sums_batch",
-    "moments_from_sums", "motion_v2_submit_batch",
+    "moments_from_sums", "motion_v2_submit_batch", "motion_plan_chunks",
 ]
 
 EXPORTED_SYMBOLS = (
@@ -37,7 +37,7 @@ EXPORTED_SYMBOLS = (
     "motion_kernel_launch_count", "motion_strerror", "motion_last_cuda_error",
     "motion_set_kernel_path", "motion_device_error", "motion_submit_batch_noalloc",
     "motion_set_stall_injection", "moment_sums_batch", "moments_from_sums",
-    "motion_v2_submit_batch",
+    "motion_v2_submit_batch", "motion_plan_chunks",
 )
 
 _LIB: ctypes.CDLL | None = None
@@ -80,6 +80,7 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
         "moment_sums_batch": ([I, I, I, I, P, P, Z, Z, P, P], I),
         "moments_from_sums": ([P, I, I, I, P], I),
         "motion_v2_submit_batch": ([P, P, I, Z, Z, P, P], I),
+        "motion_plan_chunks": ([I, I, I, I, ctypes.POINTER(I)], I),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -329,6 +330,14 @@ def moments_from_sums(sums, w: int, h: int) -> np.ndarray:
     _check(load_library().moments_from_sums(s.ctypes.data, s.shape[0], w, h, out.ctypes.data),
            "moments_from_sums")
     return out
+
+
+def motion_plan_chunks(w: int, h: int, n: int, resident_ctas: int) -> int:
+    """Frame chunks of a batched launch (host only; see include/motion.h)."""
+    c = ctypes.c_int()
+    _check(load_library().motion_plan_chunks(w, h, n, resident_ctas, ctypes.byref(c)),
+           "motion_plan_chunks")
+    return int(c.value)
 
 
 def psnr_from_sse(sse: int, n_samples: int, bpc: int):

@@ -615,6 +615,15 @@ int motion_set_kernel_path(motion_ctx* c, int path) {
     return MOTION_OK;
 }
 
+int motion_plan_chunks(int w, int h, int n, int resident_ctas, int* chunks_out) {
+    if (w < 1 || h < 1 || n < 0 || resident_ctas < 1 || !chunks_out)
+        return MOTION_ERR_INVALID_ARGUMENT;
+    const long long tiles = (long long)((w + mg::kTileW - 1) / mg::kTileW) *
+                            ((h + mg::kTileH - 1) / mg::kTileH);
+    *chunks_out = mg::plan_frame_chunks(tiles, resident_ctas, n, 8);
+    return MOTION_OK;
+}
+
 int motion_set_stall_injection(motion_ctx* c, int on) {
     if (!c) return MOTION_ERR_INVALID_ARGUMENT;
     c->stall_injection = on ? 1 : 0;

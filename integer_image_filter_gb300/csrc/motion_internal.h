@@ -74,6 +74,11 @@ cudaError_t launch_motion_tma(const TileArgs& a, bool fused, cudaStream_t s, int
 // kernel when the layout allows (*used), else the generic kernel.
 cudaError_t launch_motion_v2_tma(const TileArgs& a, cudaStream_t s, int* launches, bool* used);
 cudaError_t launch_motion_v2_tile(const TileArgs& a, cudaStream_t s, int* launches);
+// The output tile of the motion kernels (the TMA kernel's TW x TH).
+constexpr int kTileW = 128, kTileH = 32;
+// Chunks of a TMA launch (host only): n frames over `tiles` tiles with
+// `slots` CTAs resident on the device at once; 1 <= result <= max_c.
+int plan_frame_chunks(long long tiles, long long slots, int n, int max_c);
 cudaError_t launch_sse(const SseArgs& a, cudaStream_t s, int sm_count, int* launches);
 
 // Moment sums of n luma pairs (sum ref, sum dist, sum ref^2, sum dist^2).

@@ -610,6 +610,36 @@ __global__ void __launch_bounds__(Shape::NTK, Shape::MINB)
 }
 
 // ------------------------------------------------------------------ host side
+// Frame chunks of a launch, sized by the SM count (ADR-1226): n frames over
+// `tiles` tiles run as c chunks of CTAs, `slots` CTAs resident at once.  A
+// chunk after the first pays one warm-up frame and every chunk its own
+// pipeline fill (about half a frame); the idle part of the last wave and,
+// under 2.5 waves, the pipeline fills that other CTAs cannot cover are paid
+// too.  Chunks keep at least 5 frames; c <= max_c.
+//   cost(c) = (n + (c - 1) + c / 2) / n / eff,
+//   eff = (waves / ceil(waves)) * min(1, waves / 2.5), waves = tiles c / slots.
+// Fitted to forced-chunk timings on GB300: 1080p x 32 frames is fastest at
+// 3-5 chunks, x 16 at 3, x 8 at one; 4K x 32 or x 50 at two.
+int plan_frame_chunks(long long tiles, long long slots, int n, int max_c) {
+    if (n <= 1 || tiles <= 0 || slots <= 0) return 1;
+    int best_c = 1;
+    double best = 1e30;
+    for (int c = 1; c <= max_c && c <= n; ++c) {
+        const int len = (n + c - 1) / c;
+        if (c > 1 && len < 5) break;
+        const int cz = (n + len - 1) / len;
+        const double waves = (double)tiles * cz / (double)slots;
+        const double eff = waves / std::ceil(waves) * (waves < 2.5 ? waves / 2.5 : 1.0);
+        const double work = (n + (cz - 1) + 0.5 * cz) / (double)n;
+        const double cost = work / eff;
+        if (cost < best - 1e-9) {
+            best = cost;
+            best_c = cz;
+        }
+    }
+    return best_c;
+}
+
 namespace {
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -659,15 +689,7 @@ cudaError_t launch_tma_one(const TmaMaps& maps, const TileArgs& a, cudaStream_t 
         if (e != cudaSuccess) return e;
         __atomic_fetch_or(&configured, bit, __ATOMIC_RELEASE);
     }
-    // Size the launch by the SM count (ADR-1226): split the frames into c
-    // chunks run by separate CTAs.  A chunk after the first pays one warm-up
-    // frame and every chunk its own pipeline fill (about half a frame); the
-    // idle part of the last wave and, under 2.5 waves, the pipeline fills that
-    // other CTAs cannot cover are paid too.  Chunks keep at least 5 frames.
-    //   cost(c) = (n + (c - 1) + c / 2) / n / eff,
-    //   eff = (waves / ceil(waves)) * min(1, waves / 2.5), waves = tiles c / slots.
-    // (Measured: 1080p x 32 frames is fastest at 3-5 chunks, x 8 at one; 4K
-    // x 32 or 50 at two.)
+    // Size the launch by the SM count (ADR-1226): plan_frame_chunks.
     static int slots_per_sm[64] = {0};
     int& spm = slots_per_sm[dev & 63];
     if (spm == 0) {
@@ -681,26 +703,10 @@ cudaError_t launch_tma_one(const TmaMaps& maps, const TileArgs& a, cudaStream_t 
     }
     TileArgs b = a;
     const long long tiles = (long long)((a.w + TW - 1) / TW) * ((a.h + TH - 1) / TH);
-    int best_c = 1;
-    double best = 1e30;
     // a launch that reads and writes the same resident plane keeps one chunk:
     // the last chunk's store must not overtake the first chunk's read
     const bool same_plane = !V2 && a.has_prev && a.bprev == a.bprev_out;
-    const int max_c = same_plane ? 1 : 8;
-    for (int c = 1; c <= max_c && c <= a.n; ++c) {
-        const int len = (a.n + c - 1) / c;
-        if (c > 1 && len < 5) break;
-        const int cz = (a.n + len - 1) / len;
-        const double units = (double)tiles * cz;
-        const double waves = units / spm;
-        const double eff = waves / std::ceil(waves) * (waves < 2.5 ? waves / 2.5 : 1.0);
-        const double work = (a.n + (cz - 1) + 0.5 * cz) / a.n;
-        const double cost = work / eff;
-        if (cost < best - 1e-9) {
-            best = cost;
-            best_c = cz;
-        }
-    }
+    const int best_c = plan_frame_chunks(tiles, spm, a.n, same_plane ? 1 : 8);
     b.chunk = (a.n + best_c - 1) / best_c;
     dim3 grid((a.w + TW - 1) / TW, (a.h + TH - 1) / TH, (a.n + b.chunk - 1) / b.chunk);
     motion_tma_kernel<Pix, FUSED, STAGES, V2><<<grid, Shape::NTK, SMEM, s>>>(maps, b);

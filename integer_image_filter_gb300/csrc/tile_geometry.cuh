@@ -3,11 +3,12 @@
 #pragma once
 
 #include "motion_common.cuh"
+#include "motion_internal.h"
 
 namespace mg {
 
-constexpr int TW = 128;            // output tile width, samples
-constexpr int TH = 32;             // output tile height, rows
+constexpr int TW = kTileW;         // output tile width, samples (128)
+constexpr int TH = kTileH;         // output tile height, rows (32)
 constexpr int NT = 256;            // threads per CTA
 constexpr int NW = NT / 32;
 constexpr int SVW = TW + 8;        // V tile row pitch (uint32); col j <-> x = x0 - 4 + j

@@ -108,6 +108,32 @@ def test_psnr_helper(lib):
         assert abs(db - oracle.psnr_db(sse, n, bpc)) <= 1e-12 * abs(db)
 
 
+def test_frame_chunk_plan(lib):
+    """Launch sizing by SM count: the chunk counts that forced-chunk timings
+    on a GB300 (608 resident CTAs) found fastest, and the invariants of the
+    plan (1..8 chunks, at least 5 frames per chunk, one chunk for one frame)."""
+    import integer_image_filter_gb300 as iif
+    plan = iif.motion_plan_chunks
+    assert plan(3840, 2160, 50, 608) == 2      # fused 4K 4:2:0 pairs
+    assert plan(3840, 2160, 32, 608) == 2      # 10-bit 4K, batch 32
+    assert plan(1920, 1080, 32, 608) in (3, 4, 5)
+    assert plan(1920, 1080, 16, 608) == 3
+    assert plan(1920, 1080, 8, 608) == 1
+    assert plan(576, 324, 48, 608) == 8        # 55 tiles: as many chunks as allowed
+    for (w, h) in ((64, 48), (576, 324), (1920, 1080), (3840, 2160), (8192, 4320)):
+        for n in (0, 1, 2, 5, 9, 10, 31, 64, 300):
+            for slots in (1, 152, 608, 1216):
+                c = plan(w, h, n, slots)
+                assert 1 <= c <= 8
+                assert c == 1 or -(-n // c) >= 5, (w, h, n, slots, c)
+                if n <= 1:
+                    assert c == 1
+    with pytest.raises(iif.MotionError):
+        plan(0, 10, 4, 608)
+    with pytest.raises(iif.MotionError):
+        plan(10, 10, 4, 0)
+
+
 # ---------------------------------------------------------------- source contracts
 def _kernel_sources():
     return {f: open(os.path.join(CSRC, f)).read() for f in os.listdir(CSRC)
