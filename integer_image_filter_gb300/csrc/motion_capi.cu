@@ -291,10 +291,23 @@ int motion_v2_submit_batch(motion_ctx* c, const void* d_frames, int n, size_t fr
     if (rc) return rc;
     if ((rc = ctx_device_ok(c))) return rc;
     const size_t s_bytes = (size_t)sample_bytes(c->bpc);
-    if (!c->d_raw[0]) {
-        c->raw_pitch = ((size_t)c->w * s_bytes + 15) & ~(size_t)15;
-        for (int k = 0; k < 2; ++k)
-            MG_CUDA(cudaMalloc(&c->d_raw[k], c->raw_pitch * (size_t)c->h));
+    if (!c->d_raw[0] || !c->d_raw[1]) {
+        // both planes or neither: a failed second allocation leaves no half state
+        const size_t pitch_r = ((size_t)c->w * s_bytes + 15) & ~(size_t)15;
+        uint8_t* p[2] = {nullptr, nullptr};
+        cudaError_t e = cudaMalloc(&p[0], pitch_r * (size_t)c->h);
+        if (e == cudaSuccess) e = cudaMalloc(&p[1], pitch_r * (size_t)c->h);
+        if (e != cudaSuccess) {
+            if (p[0]) cudaFree(p[0]);
+            return cuda_fail(e);
+        }
+        if (c->d_raw[0]) cudaFree(c->d_raw[0]);
+        if (c->d_raw[1]) cudaFree(c->d_raw[1]);
+        c->d_raw[0] = p[0];
+        c->d_raw[1] = p[1];
+        c->raw_pitch = pitch_r;
+        c->raw_cur = 0;
+        c->v2_has_prev = 0;
     }
     cudaStream_t s = (cudaStream_t)stream;
     MG_CUDA(cudaMemsetAsync(d_sad_out, 0, sizeof(uint64_t) * (size_t)n, s));
