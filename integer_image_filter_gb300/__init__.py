@@ -152,6 +152,46 @@ def _itemsize(t) -> int:
     return int(t.element_size()) if hasattr(t, "element_size") else int(t.itemsize)
 
 
+# The C ABI takes plain pointers and cannot see how much memory is behind them;
+# these checks keep a short array from turning into an out-of-bounds access.
+def _span(t):
+    """Bytes from t's first element to the end of what it may address (the
+    tensor's storage, or a contiguous array's own data), or None if unknown."""
+    if t is None or isinstance(t, int):
+        return None
+    if hasattr(t, "untyped_storage"):
+        return int(t.untyped_storage().nbytes()) - int(t.storage_offset()) * _itemsize(t)
+    if isinstance(t, np.ndarray) and t.flags["C_CONTIGUOUS"]:
+        return int(t.nbytes)
+    return None
+
+
+def _need(t, nbytes: int, what: str) -> None:
+    span = _span(t)
+    if span is not None and nbytes > 0 and span < nbytes:
+        raise ValueError(f"{what} holds {span} bytes from its first element; {nbytes} are needed")
+
+
+def _need_out(t, count: int, what: str) -> None:
+    """An output the library writes as `count` contiguous 64-bit integers."""
+    if t is None or isinstance(t, int) or count <= 0:
+        return
+    if _itemsize(t) != 8:
+        raise TypeError(f"{what} must hold 64-bit integers")
+    contiguous = t.is_contiguous() if hasattr(t, "is_contiguous") else bool(t.flags["C_CONTIGUOUS"])
+    if not contiguous:
+        raise ValueError(f"{what} must be contiguous")
+    _need(t, 8 * count, what)
+
+
+def _plane_bytes(n: int, w: int, h: int, bpc: int, pitch: int, stride: int) -> int:
+    """Bytes a batch of n planes of w x h samples addresses from its first
+    sample (0, i.e. no check, for arguments the library itself rejects)."""
+    if n <= 0 or w <= 0 or h <= 0 or not 8 <= bpc <= 16 or pitch < w * (1 if bpc == 8 else 2):
+        return 0
+    return (n - 1) * stride + (h - 1) * pitch + w * (1 if bpc == 8 else 2)
+
+
 def _layout(t):
     """(pitch_bytes, frame_stride_bytes) of a (h, w) or (n, h, w) array/tensor
     whose last dimension is contiguous."""
@@ -200,6 +240,7 @@ def motion_submit_batch(ctx: int, frames, sad_out, n: int | None = None,
         p, s = _layout(frames)
         pitch_bytes = p if pitch_bytes is None else pitch_bytes
         frame_stride = s if frame_stride is None else frame_stride
+    _need_out(sad_out, n, "sad_out")
     _check(load_library().motion_submit_batch(ctx, _addr(frames), n, frame_stride, pitch_bytes,
                                               _stream(stream), _addr(sad_out)),
            "motion_submit_batch")
@@ -214,6 +255,7 @@ def motion_v2_submit_batch(ctx: int, frames, sad_out, n: int | None = None,
         p, s = _layout(frames)
         pitch_bytes = p if pitch_bytes is None else pitch_bytes
         frame_stride = s if frame_stride is None else frame_stride
+    _need_out(sad_out, n, "sad_out")
     _check(load_library().motion_v2_submit_batch(ctx, _addr(frames), n, frame_stride,
                                                  pitch_bytes, _stream(stream), _addr(sad_out)),
            "motion_v2_submit_batch")
@@ -239,6 +281,8 @@ def motion_psnr_yuv420_batch(ctx: int, ref_y, ref_u, ref_v, dist_y, dist_u, dist
     if n is None:
         n = int(ref_y.shape[0])
     lay = layout or _yuv_layout(ref_y, ref_u)
+    _need_out(sad_out, n, "sad_out")
+    _need_out(sse_out, 3 * n, "sse_out")
     _check(load_library().motion_psnr_yuv420_batch(
         ctx, n, _addr(ref_y), _addr(ref_u), _addr(ref_v), _addr(dist_y), _addr(dist_u),
         _addr(dist_v), lay.pitch_y, lay.pitch_uv, lay.stride_y, lay.stride_uv, _stream(stream),
@@ -257,6 +301,8 @@ def motion_psnr_yuv420_batch_host(ctx: int, ref_y, ref_u, ref_v, dist_y, dist_u,
         sad_out = np.zeros(n, np.uint64)
     if sse_out is None:
         sse_out = np.zeros((n, 3), np.uint64)
+    _need_out(sad_out, n, "sad_out")
+    _need_out(sse_out, 3 * n, "sse_out")
     _check(load_library().motion_psnr_yuv420_batch_host(
         ctx, n, _host_addr(ref_y), _host_addr(ref_u), _host_addr(ref_v), _host_addr(dist_y),
         _host_addr(dist_u), _host_addr(dist_v), lay.pitch_y, lay.pitch_uv, lay.stride_y,
@@ -278,6 +324,9 @@ def psnr_sse(ref, dist, bpc: int, sse_out, w: int | None = None, h: int | None =
         ref_pitch, _ = _layout(ref)
     if dist_pitch is None:
         dist_pitch, _ = _layout(dist)
+    _need(ref, _plane_bytes(1, w, h, bpc, ref_pitch, 0), "ref")
+    _need(dist, _plane_bytes(1, w, h, bpc, dist_pitch, 0), "dist")
+    _need_out(sse_out, 1, "sse_out")
     _check(load_library().psnr_sse(_addr(ref), _addr(dist), ref_pitch, dist_pitch, w, h, bpc,
                                    _stream(stream), _addr(sse_out)), "psnr_sse")
 
@@ -288,6 +337,12 @@ def psnr_sse_yuv420_batch(w: int, h: int, bpc: int, ref_y, ref_u, ref_v, dist_y,
     if n is None:
         n = int(ref_y.shape[0])
     lay = layout or _yuv_layout(ref_y, ref_u)
+    cw, ch = (w + 1) // 2, (h + 1) // 2
+    for t, what in ((ref_y, "ref_y"), (dist_y, "dist_y")):
+        _need(t, _plane_bytes(n, w, h, bpc, lay.pitch_y, lay.stride_y), what)
+    for t, what in ((ref_u, "ref_u"), (ref_v, "ref_v"), (dist_u, "dist_u"), (dist_v, "dist_v")):
+        _need(t, _plane_bytes(n, cw, ch, bpc, lay.pitch_uv, lay.stride_uv), what)
+    _need_out(sse_out, 3 * n, "sse_out")
     _check(load_library().psnr_sse_yuv420_batch(
         w, h, bpc, n, _addr(ref_y), _addr(ref_u), _addr(ref_v), _addr(dist_y), _addr(dist_u),
         _addr(dist_v), lay.pitch_y, lay.pitch_uv, lay.stride_y, lay.stride_uv, _stream(stream),
@@ -319,6 +374,9 @@ def moment_sums_batch(ref, dist, bpc: int, out, w: int | None = None, h: int | N
         p, st = _layout(ref)
         pitch = p if pitch is None else pitch
         stride = st if stride is None else stride
+    _need(ref, _plane_bytes(n, w, h, bpc, pitch, stride), "ref")
+    _need(dist, _plane_bytes(n, w, h, bpc, pitch, stride), "dist")
+    _need_out(out, 4 * n, "out")
     _check(load_library().moment_sums_batch(w, h, bpc, n, _addr(ref), _addr(dist), pitch, stride,
                                             _stream(stream), _addr(out)), "moment_sums_batch")
 
@@ -363,6 +421,8 @@ def motion_submit_batch_noalloc(frames, sad_out, w: int | None = None, h: int | 
         p, s = _layout(frames)
         pitch_bytes = p if pitch_bytes is None else pitch_bytes
         frame_stride = s if frame_stride is None else frame_stride
+    _need(frames, _plane_bytes(n, w, h, bpc, pitch_bytes, frame_stride), "frames")
+    _need_out(sad_out, n, "sad_out")
     _check(load_library().motion_submit_batch_noalloc(
         _addr(frames), n, w, h, bpc, frame_stride, pitch_bytes, 1 if continue_sequence else 0,
         _stream(stream), _addr(sad_out)), "motion_submit_batch_noalloc")
@@ -428,21 +488,41 @@ class MotionContext:
     def device_error(self) -> int:
         return motion_device_error(self.handle)
 
+    def _frames_fit(self, frames, n: int) -> None:
+        if hasattr(frames, "shape") and len(frames.shape) in (2, 3):
+            pitch, stride = _layout(frames)
+            _need(frames, _plane_bytes(n, self.w, self.h, self.bpc, pitch, stride), "frames")
+
+    def _yuv_fit(self, planes, n: int) -> None:
+        if all(hasattr(t, "shape") for t in planes):
+            lay = _yuv_layout(planes[0], planes[1])
+            cw, ch = (self.w + 1) // 2, (self.h + 1) // 2
+            for i, t in enumerate(planes):
+                luma = i in (0, 3)
+                _need(t, _plane_bytes(n, self.w if luma else cw, self.h if luma else ch, self.bpc,
+                                      lay.pitch_y if luma else lay.pitch_uv,
+                                      lay.stride_y if luma else lay.stride_uv), "picture plane")
+
     def submit(self, frame, stream=None):
+        self._frames_fit(frame, 1)
         return motion_submit(self.handle, frame, stream=stream)
 
     def submit_batch(self, frames, sad_out, stream=None) -> None:
+        self._frames_fit(frames, int(frames.shape[0]))
         motion_submit_batch(self.handle, frames, sad_out, stream=stream)
 
     def submit_batch_v2(self, frames, sad_out, stream=None) -> None:
+        self._frames_fit(frames, int(frames.shape[0]))
         motion_v2_submit_batch(self.handle, frames, sad_out, stream=stream)
 
     def yuv420_batch(self, ref_y, ref_u, ref_v, dist_y, dist_u, dist_v, sad_out, sse_out,
                      stream=None) -> None:
+        self._yuv_fit((ref_y, ref_u, ref_v, dist_y, dist_u, dist_v), int(ref_y.shape[0]))
         motion_psnr_yuv420_batch(self.handle, ref_y, ref_u, ref_v, dist_y, dist_u, dist_v,
                                  sad_out, sse_out, stream=stream)
 
     def yuv420_batch_host(self, ref_y, ref_u, ref_v, dist_y, dist_u, dist_v, sad_out=None,
                           sse_out=None):
+        self._yuv_fit((ref_y, ref_u, ref_v, dist_y, dist_u, dist_v), int(ref_y.shape[0]))
         return motion_psnr_yuv420_batch_host(self.handle, ref_y, ref_u, ref_v, dist_y, dist_u,
                                              dist_v, sad_out, sse_out)

@@ -108,6 +108,35 @@ def test_psnr_helper(lib):
         assert abs(db - oracle.psnr_db(sse, n, bpc)) <= 1e-12 * abs(db)
 
 
+def test_binding_refuses_short_buffers(lib):
+    """The binding checks every buffer it can measure before the library sees a
+    pointer: outputs must be contiguous 64-bit arrays of the right length and
+    inputs must reach their last sample (raised on the host, no GPU needed)."""
+    import torch
+
+    import integer_image_filter_gb300 as iif
+    f = torch.zeros((2, 8, 8), dtype=torch.uint8)
+    short = "are needed"
+    with pytest.raises(ValueError, match=short):             # out: 4 of 8 values
+        iif.moment_sums_batch(f, f, 8, torch.zeros((1, 4), dtype=torch.int64))
+    with pytest.raises(TypeError, match="64-bit"):           # 32-bit output
+        iif.moment_sums_batch(f, f, 8, torch.zeros((2, 4), dtype=torch.int32))
+    with pytest.raises(ValueError, match="contiguous"):      # non-contiguous output
+        iif.moment_sums_batch(f, f, 8, torch.zeros((4, 4), dtype=torch.int64)[::2])
+    with pytest.raises(ValueError, match=short):             # pitch runs past the frames
+        iif.moment_sums_batch(f, f, 8, torch.zeros((2, 4), dtype=torch.int64), pitch=16,
+                              stride=64)
+    with pytest.raises(ValueError, match=short):
+        iif.motion_submit_batch_noalloc(f, torch.zeros(1, dtype=torch.int64))
+    y, c = torch.zeros((3, 8, 8), dtype=torch.uint8), torch.zeros((3, 4, 4), dtype=torch.uint8)
+    c2 = torch.zeros((2, 4, 4), dtype=torch.uint8)           # chroma of 2 pairs only
+    with pytest.raises(ValueError, match=short):
+        iif.psnr_sse_yuv420_batch(8, 8, 8, y, c, c2, y, c, c, torch.zeros((3, 3), dtype=torch.int64))
+    with pytest.raises(ValueError, match=short):
+        iif.motion_psnr_yuv420_batch_host(0, y.numpy(), c.numpy(), c.numpy(), y.numpy(),
+                                          c.numpy(), c.numpy(), np.zeros(2, np.uint64))
+
+
 def test_frame_chunk_plan(lib):
     """Launch sizing by SM count: the chunk counts that forced-chunk timings
     on a GB300 (608 resident CTAs) found fastest, and the invariants of the
