@@ -240,6 +240,18 @@ MOTION_API int motion_set_kernel_path(motion_ctx* ctx, int path);
  * allocation-free entry point) always uses one chunk. */
 MOTION_API int motion_plan_chunks(int w, int h, int n, int resident_ctas, int* chunks_out);
 
+/* Diagnostic, host only, no GPU: the output tile and frame chunk that block
+ * `block` of a batched TMA launch of w x h frames in `chunks` chunks works on
+ * (blocks counted x fastest, then y, then chunk, over ceil(w/128) x
+ * ceil(h/32) x chunks blocks).  The tiles on the frame border come first for
+ * every chunk, then the interior tiles -- those that read no mirrored sample
+ * of the "Gaussian blur with mirror boundaries" -- so that after the first
+ * wave an SM runs one kind of frame loop at a time.  tile_out (host int[3]) receives
+ * {tile column, tile row, chunk}.  Errors: MOTION_ERR_INVALID_ARGUMENT (w, h
+ * outside 1..32768, chunks outside 1..8, block outside the launch, NULL
+ * tile_out). */
+MOTION_API int motion_tile_order(int w, int h, int chunks, long long block, int* tile_out);
+
 /* Test hook for the kernels' bounded waits (no counterpart in the paper):
  * while on, TMA launches on this context expect 16 bytes per stage more than
  * their boxes deliver, so no stage wait can complete, and bound every wait at

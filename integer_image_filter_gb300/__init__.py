@@ -27,7 +27,7 @@ __all__ = [
     "motion_kernel_launch_count", "motion_strerror", "MotionContext", "EXPORTED_SYMBOLS",
     "motion_set_kernel_path", "motion_device_error", "MOTION_PATH_AUTO", "MOTION_PATH_GENERIC",
     "motion_submit_batch_noalloc", "motion_set_stall_injection", "moment_sums_batch",
-    "moments_from_sums", "motion_v2_submit_batch", "motion_plan_chunks",
+    "moments_from_sums", "motion_v2_submit_batch", "motion_plan_chunks", "motion_tile_order",
 ]
 
 EXPORTED_SYMBOLS = (
@@ -37,7 +37,7 @@ EXPORTED_SYMBOLS = (
     "motion_kernel_launch_count", "motion_strerror", "motion_last_cuda_error",
     "motion_set_kernel_path", "motion_device_error", "motion_submit_batch_noalloc",
     "motion_set_stall_injection", "moment_sums_batch", "moments_from_sums",
-    "motion_v2_submit_batch", "motion_plan_chunks",
+    "motion_v2_submit_batch", "motion_plan_chunks", "motion_tile_order",
 )
 
 _LIB: ctypes.CDLL | None = None
@@ -81,6 +81,7 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
         "moments_from_sums": ([P, I, I, I, P], I),
         "motion_v2_submit_batch": ([P, P, I, Z, Z, P, P], I),
         "motion_plan_chunks": ([I, I, I, I, ctypes.POINTER(I)], I),
+        "motion_tile_order": ([I, I, I, ctypes.c_longlong, ctypes.POINTER(I)], I),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -388,6 +389,13 @@ def moments_from_sums(sums, w: int, h: int) -> np.ndarray:
     _check(load_library().moments_from_sums(s.ctypes.data, s.shape[0], w, h, out.ctypes.data),
            "moments_from_sums")
     return out
+
+
+def motion_tile_order(w: int, h: int, chunks: int, block: int) -> tuple[int, int, int]:
+    """(tile column, tile row, chunk) of one block of a batched launch (host only)."""
+    t = (ctypes.c_int * 3)()
+    _check(load_library().motion_tile_order(w, h, chunks, block, t), "motion_tile_order")
+    return int(t[0]), int(t[1]), int(t[2])
 
 
 def motion_plan_chunks(w: int, h: int, n: int, resident_ctas: int) -> int:

@@ -637,6 +637,15 @@ int motion_plan_chunks(int w, int h, int n, int resident_ctas, int* chunks_out) 
     return MOTION_OK;
 }
 
+int motion_tile_order(int w, int h, int chunks, long long block, int* tile_out) {
+    if (w < 1 || h < 1 || w > 32768 || h > 32768 || chunks < 1 || chunks > 8 || !tile_out)
+        return MOTION_ERR_INVALID_ARGUMENT;
+    const int gx = (w + mg::kTileW - 1) / mg::kTileW, gy = (h + mg::kTileH - 1) / mg::kTileH;
+    if (block < 0 || block >= (long long)gx * gy * chunks) return MOTION_ERR_INVALID_ARGUMENT;
+    mg::tile_of_block(w, h, gx, gy, chunks, (int)block, &tile_out[0], &tile_out[1], &tile_out[2]);
+    return MOTION_OK;
+}
+
 int motion_set_stall_injection(motion_ctx* c, int on) {
     if (!c) return MOTION_ERR_INVALID_ARGUMENT;
     c->stall_injection = on ? 1 : 0;

@@ -76,6 +76,41 @@ cudaError_t launch_motion_v2_tma(const TileArgs& a, cudaStream_t s, int* launche
 cudaError_t launch_motion_v2_tile(const TileArgs& a, cudaStream_t s, int* launches);
 // The output tile of the motion kernels (the TMA kernel's TW x TH).
 constexpr int kTileW = 128, kTileH = 32;
+// The tile and frame chunk of block `lin` (x fastest, then y, then chunk) of a
+// TMA launch over gx x gy tiles and gz chunks: the tiles on the frame border
+// of every chunk first, then the interior tiles (those that read no mirrored
+// sample: x0 > 0, y0 > 0, x0 + TW + 2 <= w and y0 + TH + 2 <= h).  The two
+// kinds run different copies of the frame loop, and an SM that runs both at
+// once misses in its instruction cache; in this order only the first wave
+// mixes them, and the last wave is made of the faster interior tiles.  A
+// bijection of [0, gx gy gz).
+__host__ __device__ inline void tile_of_block(int w, int h, int gx, int gy, int gz, int lin,
+                                              int* tx, int* ty, int* cz) {
+    const int nix = w >= kTileW + 2 ? (w - kTileW - 2) / kTileW : 0;   // interior columns 1..nix
+    const int niy = h >= kTileH + 2 ? (h - kTileH - 2) / kTileH : 0;   // interior rows 1..niy
+    const int ni = nix * niy, nb = gx * gy - ni;
+    if (lin >= nb * gz) {
+        const int idx = lin - nb * gz;
+        *cz = idx / ni;
+        const int r = idx - *cz * ni;
+        *ty = 1 + r / nix;
+        *tx = 1 + r % nix;
+        return;
+    }
+    *cz = lin / nb;
+    const int r = lin - *cz * nb;
+    const int nbr = (gy - niy) * gx;   // whole border rows: row 0 and rows after niy
+    if (r < nbr) {
+        const int k = r / gx;
+        *tx = r % gx;
+        *ty = k == 0 ? 0 : niy + k;
+    } else {                           // rows 1..niy: column 0 and columns after nix
+        const int rr = r - nbr, per = gx - nix;
+        *ty = 1 + rr / per;
+        const int c = rr % per;
+        *tx = c == 0 ? 0 : nix + c;
+    }
+}
 // Chunks of a TMA launch (host only): n frames over `tiles` tiles with
 // `slots` CTAs resident on the device at once; 1 <= result <= max_c.
 int plan_frame_chunks(long long tiles, long long slots, int n, int max_c);

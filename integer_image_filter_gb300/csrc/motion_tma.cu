@@ -16,6 +16,10 @@
 //    i>=n -> 2n-i-2) and mirror the V columns of their own rows, so no tile
 //    takes a sample-by-sample path and no block barrier is left in the frame
 //    loop.
+//  * Blocks take the border tiles of every chunk first and the interior tiles
+//    after them (tile_of_block): the two kinds run different copies of the
+//    frame loop, and an SM that runs both at once misses in its instruction
+//    cache.
 //  * Separable blur: the vertical 5-tap pass once per sample (rounded >> bpc)
 //    into a shared V tile, then the horizontal 5-tap pass (rounded >> 16)
 //    ("ADR-1392: CUDA motion, PSNR and moment kernels add one atomic per
@@ -191,7 +195,11 @@ __global__ void __launch_bounds__(Shape::NTK, Shape::MINB)
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     // each warp owns output rows RPW w .. RPW w + RPW-1 of the tile; its V rows are private
     uint32_t* sV = reinterpret_cast<uint32_t*>(smem + STAGES * STAGE) + warp * 4 * SVW;
-    const int x0 = blockIdx.x * TW, y0 = blockIdx.y * TH;
+    // border tiles of every chunk first, interior tiles after them (tile_of_block)
+    int tx, ty, cz;
+    tile_of_block(a.w, a.h, gridDim.x, gridDim.y, gridDim.z,
+                  blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z), &tx, &ty, &cz);
+    const int x0 = tx * TW, y0 = ty * TH;
     const bool full_tile = (x0 + TW <= a.w) && (y0 + TH <= a.h);
     const bool pl = x0 == 0, pt = y0 == 0;
     const bool pr = x0 + TW + 2 > a.w, pb = y0 + TH + 2 > a.h;
@@ -231,15 +239,15 @@ __global__ void __launch_bounds__(Shape::NTK, Shape::MINB)
     }
     __syncthreads();
 
-    // this CTA's frames: chunk blockIdx.z of the launch; a chunk after the
+    // this CTA's frames: chunk cz of the launch; a chunk after the
     // first starts one frame early to rebuild B_prev (no outputs for it).
     // motion_v2 continuing an earlier call starts from that call's last raw
     // frame (the prev map) in the same way.
     const int chunk = a.chunk > 0 ? a.chunk : a.n;
-    const int f_begin = blockIdx.z * chunk;
+    const int f_begin = cz * chunk;
     const int f_end = min(a.n, f_begin + chunk);
-    const bool warm_prev = V2 && blockIdx.z == 0 && a.has_prev;
-    const bool warm = blockIdx.z > 0 || warm_prev;
+    const bool warm_prev = V2 && cz == 0 && a.has_prev;
+    const bool warm = cz > 0 || warm_prev;
     const int first = f_begin - (warm ? 1 : 0);
     const int cnt = f_end - first;
     const bool use_prev = !V2 && !warm && a.has_prev;

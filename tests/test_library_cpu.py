@@ -163,6 +163,32 @@ def test_frame_chunk_plan(lib):
         plan(10, 10, 4, 0)
 
 
+def test_tile_order(lib):
+    """Block order of a batched launch: every (tile, chunk) exactly once, the
+    frame-border tiles first, the tiles that read no mirrored sample last."""
+    import integer_image_filter_gb300 as iif
+    order = iif.motion_tile_order
+    for (w, h, chunks) in ((3840, 2160, 2), (1920, 1080, 3), (576, 324, 8), (64, 48, 1),
+                           (129, 33, 2), (130, 34, 1), (258, 66, 3), (390, 98, 4), (1, 1, 1),
+                           (32768, 40, 2), (40, 32768, 1), (8192, 4320, 1)):
+        gx, gy = -(-w // 128), -(-h // 32)
+        seen = set()
+        kinds = []
+        for b in range(gx * gy * chunks):
+            tx, ty, cz = order(w, h, chunks, b)
+            assert 0 <= tx < gx and 0 <= ty < gy and 0 <= cz < chunks
+            seen.add((tx, ty, cz))
+            x0, y0 = 128 * tx, 32 * ty
+            kinds.append(x0 > 0 and y0 > 0 and x0 + 130 <= w and y0 + 34 <= h)
+        assert len(seen) == gx * gy * chunks, (w, h, chunks)
+        n_border = len(kinds) - sum(kinds)
+        assert not any(kinds[:n_border]) and all(kinds[n_border:]), (w, h, chunks)
+    for bad in ((0, 10, 1, 0), (10, 10, 0, 0), (10, 10, 9, 0), (10, 10, 1, 1), (10, 10, 1, -1),
+                (32769, 10, 1, 0)):
+        with pytest.raises(iif.MotionError):
+            order(*bad)
+
+
 # ---------------------------------------------------------------- source contracts
 def _kernel_sources():
     return {f: open(os.path.join(CSRC, f)).read() for f in os.listdir(CSRC)
