@@ -46,6 +46,29 @@ def algorithmic_bytes_per_pair(w: int, h: int, bpc: int) -> int:
     return 2 * (w * h + 2 * cw * ch) * s
 
 
+# The integer-arithmetic co-bound.  Algorithmic operations of the definition:
+# per luma pixel 10 multiply-adds for the two 5-tap passes, one absolute
+# difference and one add for the SAD (motion_v2: one subtract more for
+# prev - cur); per sample one subtract and one multiply-add for the squared
+# error.  Peak: two integer pipes of 64 lanes per SM (multiply / dot product,
+# and add / logic / permute; each measured at 64 lane-operations per clock per
+# SM on GB300) at the maximum SM clock.
+MOTION_OPS_PER_PIXEL = 12
+SSE_OPS_PER_SAMPLE = 2
+INT_LANES_PER_SM_CLOCK = 128
+
+
+def alu_co_bound(ops_per_launch: float, launch_ms: float, sm_max_mhz) -> dict:
+    import torch
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    mhz = float(sm_max_mhz) if sm_max_mhz else 2070.0
+    peak = sms * INT_LANES_PER_SM_CLOCK * mhz * 1e6 / 1e12
+    achieved = ops_per_launch / (launch_ms * 1e-3) / 1e12
+    return {"achieved": achieved, "peak": peak, "unit": "Tops/s", "frac": achieved / peak,
+            "ops_per_launch": ops_per_launch,
+            "peak_basis": f"{sms} SMs x {INT_LANES_PER_SM_CLOCK} integer lanes x {mhz:.0f} MHz"}
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -310,7 +333,10 @@ def run_gpu(args):
 
     peak, peak_kind = peaks()
     bytes_per_launch = algorithmic_bytes_per_pair(args.w, args.h, 8) * n
+    ops_per_launch = n * (MOTION_OPS_PER_PIXEL * args.w * args.h +
+                          SSE_OPS_PER_SAMPLE * (args.w * args.h + 2 * ((args.w + 1) // 2) * ((args.h + 1) // 2)))
     kern_ms = statistics.mean(step_ms)
+    clk = clocks.summary()
     achieved = bytes_per_launch / (kern_ms * 1e-3) / 1e9
     value = ws * n * args.steps / (total_ms * 1e-3)
     cpu = None
@@ -335,12 +361,13 @@ def run_gpu(args):
                      "traffic": recorded_traffic("motion_tma_kernel<uint8_t, fused>", WORKLOAD),
                      "kernel": "motion_tma_kernel<uint8_t, fused>",
                      "algorithmic_bytes_per_launch": bytes_per_launch,
-                     "kernel_ms": kern_ms},
+                     "kernel_ms": kern_ms,
+                     "alu": alu_co_bound(ops_per_launch, kern_ms, (clk or {}).get("sm_max_mhz"))},
         "cpu_baseline": cpu,
         "e2e": {"value": ws * n * e2e_steps / e2e_s, "unit": "frames/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches,
-        "clocks": clocks.summary(),
+        "clocks": clk,
     }
     print(json.dumps(line), flush=True)
     ctx.close()
@@ -398,6 +425,7 @@ def run_sequence_workload(args):
         ms = e0.elapsed_time(e1) / args.steps
         launches = (iif.motion_kernel_launch_count() - l0) / args.steps
         alg = w * h * s * n
+        ops = (MOTION_OPS_PER_PIXEL + (1 if args.v2 else 0)) * w * h * n
         lines.append({"metric": "frames/s (batched motion%s SAD)" % ("_v2" if args.v2 else ""),
                       "value": n / (ms * 1e-3),
                       "unit": "frames/s", "n_gpus": 1, "steps": args.steps,
@@ -410,7 +438,8 @@ def run_sequence_workload(args):
                       "roofline": {"bound": "hbm", "achieved": alg / (ms * 1e-3) / 1e9,
                                    "peak": peak, "unit": "GB/s",
                                    "frac": alg / (ms * 1e-3) / 1e9 / peak, "peak_kind": peak_kind,
-                                   "algorithmic_bytes_per_step": alg}})
+                                   "algorithmic_bytes_per_step": alg,
+                                   "alu": alu_co_bound(ops, ms, None)}})
         ctx.close()
     for ln in lines:
         print(json.dumps(ln), flush=True)
