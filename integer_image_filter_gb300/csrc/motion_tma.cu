@@ -621,13 +621,16 @@ __global__ void __launch_bounds__(Shape::NTK, Shape::MINB)
 // Frame chunks of a launch, sized by the SM count (ADR-1226): n frames over
 // `tiles` tiles run as c chunks of CTAs, `slots` CTAs resident at once.  A
 // chunk after the first pays one warm-up frame and every chunk its own
-// pipeline fill (about half a frame); the idle part of the last wave and,
-// under 2.5 waves, the pipeline fills that other CTAs cannot cover are paid
-// too.  Chunks keep at least 5 frames; c <= max_c.
-//   cost(c) = (n + (c - 1) + c / 2) / n / eff,
-//   eff = (waves / ceil(waves)) * min(1, waves / 2.5), waves = tiles c / slots.
-// Fitted to forced-chunk timings on GB300: 1080p x 32 frames is fastest at
-// 3-5 chunks, x 16 at 3, x 8 at one; 4K x 32 or x 50 at two.
+// pipeline fill (about half a frame); a launch under one wave leaves SMs idle,
+// and the last, partial wave of a longer one costs a quarter of its idle
+// share (the SMs it leaves short of CTAs run the ones they hold faster: the
+// kernel is bound by instruction issue).  Chunks keep at least 5 frames;
+// c <= max_c.
+//   cost(c) = (n + (c - 1) + c / 2) / n / eff, waves = tiles c / slots,
+//   eff = min(1, waves) / (1 + (ceil(waves) / waves - 1) / 4).
+// Fitted to forced-chunk timings on GB300 with the border-first block order:
+// 1080p x 16 frames is fastest at 1-2 chunks, x 32 at 2; 4K x 16 at one,
+// x 32 at 1-2, x 50 4:2:0 pairs at 2.
 int plan_frame_chunks(long long tiles, long long slots, int n, int max_c) {
     if (n <= 1 || tiles <= 0 || slots <= 0) return 1;
     int best_c = 1;
@@ -637,7 +640,8 @@ int plan_frame_chunks(long long tiles, long long slots, int n, int max_c) {
         if (c > 1 && len < 5) break;
         const int cz = (n + len - 1) / len;
         const double waves = (double)tiles * cz / (double)slots;
-        const double eff = waves / std::ceil(waves) * (waves < 2.5 ? waves / 2.5 : 1.0);
+        const double q = std::ceil(waves) / waves;
+        const double eff = (waves < 1.0 ? waves : 1.0) / (1.0 + 0.25 * (q - 1.0));
         const double work = (n + (cz - 1) + 0.5 * cz) / (double)n;
         const double cost = work / eff;
         if (cost < best - 1e-9) {
