@@ -88,7 +88,8 @@ def peaks():
 
 # the sources that make up the fused TMA kernel; its recorded DRAM traffic is
 # only reported while they are unchanged since the capture
-KERNEL_SOURCES = ("motion_tma.cu", "tile_geometry.cuh", "motion_common.cuh", "motion_internal.h")
+KERNEL_SOURCES = ("motion_tma.cu", "tile_geometry.cuh", "motion_common.cuh", "motion_internal.h",
+                  "bounds_check.cuh")
 
 
 def _code_tokens(text: str) -> bytes:

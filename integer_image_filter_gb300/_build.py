@@ -1,5 +1,11 @@
 """Build libmotion_gb300.so in-tree with nvcc for sm_103a (one -gencode, the
-translation units compiled in parallel, then linked into one shared object)."""
+translation units compiled in parallel, then linked into one shared object).
+
+``build(checked=True)`` builds the bounds-checked variant,
+libmotion_gb300_checked.so (MG_BOUNDS_CHECK=1: every shared- and global-memory
+access of the motion kernels is checked against its buffer, a failed check
+skips the access and sets bit 1 of the device error word); the tests run it
+on small cases, as the stand-in for a memory checker."""
 from __future__ import annotations
 
 import os
@@ -13,6 +19,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "_lib")
 LIB_NAME = "libmotion_gb300.so"
+CHECKED_LIB_NAME = "libmotion_gb300_checked.so"
 SOURCES = ["motion_capi.cu", "motion_tile.cu", "motion_tma.cu", "psnr_sse.cu", "motion_noalloc.cu",
            "moment.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -25,8 +32,8 @@ def nvcc() -> str:
     raise RuntimeError("nvcc not found: the CUDA library cannot be built")
 
 
-def lib_path() -> str:
-    return os.path.join(OUT_DIR, LIB_NAME)
+def lib_path(checked: bool = False) -> str:
+    return os.path.join(OUT_DIR, CHECKED_LIB_NAME if checked else LIB_NAME)
 
 
 def _newest_source_mtime() -> float:
@@ -36,16 +43,19 @@ def _newest_source_mtime() -> float:
     return max(os.path.getmtime(f) for f in files)
 
 
-def up_to_date() -> bool:
-    p = lib_path()
+def up_to_date(checked: bool = False) -> bool:
+    p = lib_path(checked)
     return os.path.exists(p) and os.path.getmtime(p) >= _newest_source_mtime()
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags: tuple[str, ...] = ()) -> str:
-    if not force and up_to_date():
-        return lib_path()
+def build(force: bool = False, verbose: bool = False, extra_flags: tuple[str, ...] = (),
+          checked: bool = False) -> str:
+    if not force and up_to_date(checked):
+        return lib_path(checked)
     os.makedirs(OUT_DIR, exist_ok=True)
-    obj_dir = os.path.join(OUT_DIR, "obj")
+    obj_dir = os.path.join(OUT_DIR, "obj_checked" if checked else "obj")
+    if checked:
+        extra_flags = tuple(extra_flags) + ("-DMG_BOUNDS_CHECK=1",)
     os.makedirs(obj_dir, exist_ok=True)
     cc = nvcc()
     common = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-fvisibility=hidden",
@@ -65,13 +75,13 @@ def build(force: bool = False, verbose: bool = False, extra_flags: tuple[str, ..
 
     with ThreadPoolExecutor(len(SOURCES)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
-    tmp = lib_path() + ".tmp"
+    tmp = lib_path(checked) + ".tmp"
     cmd = [cc] + ARCH + ["-shared", "-o", tmp] + objs + ["-Xcompiler", "-fPIC"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, lib_path())
-    return lib_path()
+    os.replace(tmp, lib_path(checked))
+    return lib_path(checked)
 
 
 if __name__ == "__main__":

@@ -24,6 +24,13 @@
 
 namespace mg {
 
+// A 16-byte asynchronous copy whose source and destination must stay inside
+// their buffers (checked build; otherwise the plain copy).
+__device__ __forceinline__ void cp_async16_in(void* dst, const void* src, [[maybe_unused]] Span d,
+                                              [[maybe_unused]] Span s) {
+    if (MG_OK(dst, 16, d.p, d.n) && MG_OK(src, 16, s.p, s.n)) cp_async16(dst, src);
+}
+
 // Stage frame f (luma fy with row pitch `pitch`; fused: the distorted luma
 // and chroma of pair f) for the tile at (x0, y0).
 template <typename Pix, bool FUSED>
@@ -33,21 +40,27 @@ __device__ __forceinline__ void load_stage(const TileArgs& a, int f, unsigned ch
     using G = Geo<Pix>;
     constexpr int S = G::S;
     const int tid = threadIdx.x;
+    // the buffers every access below must stay in: the frame fy, the caller's
+    // distorted luma and chroma planes, and this stage's regions
+    [[maybe_unused]] const Span fy_span{fy, (size_t)plane_span(1, 0, a.h, pitch, a.w, S)};
+    [[maybe_unused]] const Span box{st, (size_t)G::RAW_BYTES};
     if (fast) {
         constexpr int CHR = G::RAW_W * S / 16;
         const uint8_t* g0 = fy + (long long)(y0 - 2) * pitch + (long long)(x0 - G::HX) * S;
         for (int c = tid; c < G::RAW_ROWS * CHR; c += NT) {
             const int r = c / CHR, k = c - r * CHR;
-            cp_async16(st + (r * G::RAW_W) * S + k * 16, g0 + (long long)r * pitch + k * 16);
+            cp_async16_in(st + (r * G::RAW_W) * S + k * 16, g0 + (long long)r * pitch + k * 16, box, fy_span);
         }
         if constexpr (FUSED) {
             unsigned char* sd = st + G::RAW_BYTES;
             constexpr int CHD = TW * S / 16;
             const uint8_t* d0 = a.dist_y + (long long)f * a.stride_y + (long long)y0 * a.pitch_y +
                                 (long long)x0 * S;
+            const Span dist_span{a.dist_y, (size_t)plane_span(a.n, a.stride_y, a.h, a.pitch_y, a.w, S)};
             for (int c = tid; c < TH * CHD; c += NT) {
                 const int r = c / CHD, k = c - r * CHD;
-                cp_async16(sd + r * TW * S + k * 16, d0 + (long long)r * a.pitch_y + k * 16);
+                cp_async16_in(sd + r * TW * S + k * 16, d0 + (long long)r * a.pitch_y + k * 16,
+                              Span{sd, (size_t)G::DIST_BYTES}, dist_span);
             }
             constexpr int CHC = G::CW * S / 16;
             const long long coff = (long long)f * a.stride_uv + (long long)(y0 / 2) * a.pitch_uv +
@@ -59,8 +72,10 @@ __device__ __forceinline__ void load_stage(const TileArgs& a, int f, unsigned ch
                 const int r = rem / CHC, k = rem - r * CHC;
                 // constant-index plane selection (ADR-1392 Decision 3)
                 const uint8_t* base = p == 0 ? a.ref_u : p == 1 ? a.dist_u : p == 2 ? a.ref_v : a.dist_v;
-                cp_async16(sc + p * G::C_BYTES + r * G::CW * S + k * 16,
-                           base + coff + (long long)r * a.pitch_uv + k * 16);
+                cp_async16_in(sc + p * G::C_BYTES + r * G::CW * S + k * 16,
+                              base + coff + (long long)r * a.pitch_uv + k * 16,
+                              Span{sc + p * G::C_BYTES, (size_t)G::C_BYTES},
+                              Span{base, (size_t)plane_span(a.n, a.stride_uv, a.ch, a.pitch_uv, a.cw, S)});
             }
         }
         return;
@@ -70,7 +85,9 @@ __device__ __forceinline__ void load_stage(const TileArgs& a, int f, unsigned ch
     for (int e = tid; e < G::RAW_ROWS * G::RAW_W; e += NT) {
         const int r = e / G::RAW_W, c = e - r * G::RAW_W;
         const int yy = mirror_clamp(y0 - 2 + r, a.h), xx = mirror_clamp(x0 - G::HX + c, a.w);
-        raw[e] = *reinterpret_cast<const Pix*>(fy + (long long)yy * pitch + (long long)xx * S);
+        MG_ST(&raw[e], MG_LD(reinterpret_cast<const Pix*>(fy + (long long)yy * pitch + (long long)xx * S),
+                             fy_span.p, fy_span.n),
+              box.p, box.n);
     }
     if constexpr (FUSED) {
         Pix* sd = reinterpret_cast<Pix*>(st + G::RAW_BYTES);
@@ -84,7 +101,10 @@ __device__ __forceinline__ void load_stage(const TileArgs& a, int f, unsigned ch
             const uint8_t* src = in ? fd + (long long)y * a.pitch_y + (long long)x * S
                                     : fy + (long long)mirror_clamp(y, a.h) * pitch +
                                           (long long)mirror_clamp(x, a.w) * S;
-            sd[e] = *reinterpret_cast<const Pix*>(src);
+            [[maybe_unused]] const Span src_span =
+                in ? Span{fd, (size_t)plane_span(1, 0, a.h, a.pitch_y, a.w, S)} : fy_span;
+            MG_ST(&sd[e], MG_LD(reinterpret_cast<const Pix*>(src), src_span.p, src_span.n), st + G::RAW_BYTES,
+                  G::DIST_BYTES);
         }
         Pix* sc = reinterpret_cast<Pix*>(st + G::RAW_BYTES + G::DIST_BYTES);
         const long long foff = (long long)f * a.stride_uv;
@@ -96,8 +116,9 @@ __device__ __forceinline__ void load_stage(const TileArgs& a, int f, unsigned ch
             const uint8_t* base = p == 0 ? a.ref_u : p == 1 ? a.dist_u : p == 2 ? a.ref_v : a.dist_v;
             Pix v = 0;
             if (y < a.ch && x < a.cw)
-                v = *reinterpret_cast<const Pix*>(base + foff + (long long)y * a.pitch_uv + (long long)x * S);
-            sc[e] = v;
+                v = MG_LD(reinterpret_cast<const Pix*>(base + foff + (long long)y * a.pitch_uv + (long long)x * S),
+                          base, plane_span(a.n, a.stride_uv, a.ch, a.pitch_uv, a.cw, S));
+            MG_ST(&sc[e], v, st + G::RAW_BYTES + G::DIST_BYTES, 4 * G::C_BYTES);
         }
     }
 }
@@ -112,7 +133,12 @@ __global__ void __launch_bounds__(NT) motion_tile_kernel(const TileArgs a) {
     constexpr int STAGE = FUSED ? G::STAGE_FUSED : G::STAGE_MOTION;
     extern __shared__ __align__(16) unsigned char smem[];
     uint32_t* sV = reinterpret_cast<uint32_t*>(smem + 2 * STAGE);
+    [[maybe_unused]] const Span vtile{sV, (size_t)G::SV_BYTES};
     __shared__ unsigned long long red[NW][4];
+#if MG_BOUNDS_CHECK
+    MG_BC_BEGIN(a.err);
+    __syncthreads();
+#endif
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int x0 = blockIdx.x * TW, y0 = blockIdx.y * TH;
@@ -147,7 +173,10 @@ __global__ void __launch_bounds__(NT) motion_tile_kernel(const TileArgs a) {
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const int x = x0 + 4 * q + i;
-            bp[k][i] = (a.has_prev && y < a.h && x < a.w) ? a.bprev[(long long)y * a.bprev_pitch + x] : 0u;
+            bp[k][i] = (a.has_prev && y < a.h && x < a.w)
+                           ? MG_LD(a.bprev + (long long)y * a.bprev_pitch + x, a.bprev,
+                                   (size_t)a.h * a.bprev_pitch * sizeof(uint16_t))
+                           : 0u;
         }
     }
 
@@ -162,12 +191,13 @@ __global__ void __launch_bounds__(NT) motion_tile_kernel(const TileArgs a) {
         __syncthreads();
 
         const Pix* raw = reinterpret_cast<const Pix*>(st);
+        [[maybe_unused]] const Span box{st, (size_t)G::RAW_BYTES};
         // ---- vertical pass: 32 quads x 8 runs of 4 rows; raw row r <-> y0 - 2 + r
         {
             const Pix* src = raw + (warp * 4) * G::RAW_W + G::HX + 4 * lane;
             uint32_t p[8][4];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) unpack4(src + i * G::RAW_W, p[i]);
+            for (int i = 0; i < 8; ++i) unpack4_in(src + i * G::RAW_W, box.p, box.n, p[i]);
 #pragma unroll
             for (int r = 0; r < 4; ++r) {
                 uint4 o;
@@ -188,21 +218,22 @@ __global__ void __launch_bounds__(NT) motion_tile_kernel(const TileArgs a) {
                     o.z = vtap(p[r][2], p[r + 1][2], p[r + 2][2], p[r + 3][2], p[r + 4][2], rnd, sh);
                     o.w = vtap(p[r][3], p[r + 1][3], p[r + 2][3], p[r + 3][3], p[r + 4][3], rnd, sh);
                 }
-                *reinterpret_cast<uint4*>(sV + (warp * 4 + r) * SVW + 4 + 4 * lane) = o;
+                MG_ST(reinterpret_cast<uint4*>(sV + (warp * 4 + r) * SVW + 4 + 4 * lane), o, vtile.p, vtile.n);
             }
             // the two halo columns on each side of the tile
             if (tid < 4 * TH) {
                 const int r = tid >> 2, which = tid & 3;
                 const int off = which == 0 ? -2 : which == 1 ? -1 : which == 2 ? TW : TW + 1;
                 const Pix* s = raw + r * G::RAW_W + G::HX + off;
+                uint32_t t[5];
+#pragma unroll
+                for (int k = 0; k < 5; ++k) t[k] = MG_LD(s + k * G::RAW_W, box.p, box.n);
                 if constexpr (V2) {
-                    const uint32_t x = vsum(s[0], s[G::RAW_W], s[2 * G::RAW_W], s[3 * G::RAW_W],
-                                            s[4 * G::RAW_W]);
-                    sV[r * SVW + 4 + off] = (uint32_t)vdiff<Pix>(hxp, x, rnd, sh);
+                    const uint32_t x = vsum(t[0], t[1], t[2], t[3], t[4]);
+                    MG_ST(&sV[r * SVW + 4 + off], (uint32_t)vdiff<Pix>(hxp, x, rnd, sh), vtile.p, vtile.n);
                     hxp = x;
                 } else {
-                    sV[r * SVW + 4 + off] = vtap(s[0], s[G::RAW_W], s[2 * G::RAW_W], s[3 * G::RAW_W],
-                                                 s[4 * G::RAW_W], rnd, sh);
+                    MG_ST(&sV[r * SVW + 4 + off], vtap(t[0], t[1], t[2], t[3], t[4], rnd, sh), vtile.p, vtile.n);
                 }
             }
         }
@@ -216,9 +247,9 @@ __global__ void __launch_bounds__(NT) motion_tile_kernel(const TileArgs a) {
         for (int k = 0; k < 4; ++k) {
             const int r = rbase + 8 * k;
             const uint32_t* v = sV + r * SVW + 4 * q;
-            const uint4 A = *reinterpret_cast<const uint4*>(v);
-            const uint4 Bq = *reinterpret_cast<const uint4*>(v + 4);
-            const uint4 C = *reinterpret_cast<const uint4*>(v + 8);
+            const uint4 A = MG_LD(reinterpret_cast<const uint4*>(v), vtile.p, vtile.n);
+            const uint4 Bq = MG_LD(reinterpret_cast<const uint4*>(v + 4), vtile.p, vtile.n);
+            const uint4 C = MG_LD(reinterpret_cast<const uint4*>(v + 8), vtile.p, vtile.n);
             if constexpr (V2) {
                 const int wi[12] = {(int)A.x, (int)A.y, (int)A.z, (int)A.w, (int)Bq.x, (int)Bq.y,
                                     (int)Bq.z, (int)Bq.w, (int)C.x, (int)C.y, (int)C.z, (int)C.w};
@@ -246,8 +277,9 @@ __global__ void __launch_bounds__(NT) motion_tile_kernel(const TileArgs a) {
             }
             if constexpr (FUSED) {
                 uint32_t rf[4], ds[4];
-                unpack4(raw + (r + 2) * G::RAW_W + G::HX + 4 * q, rf);
-                unpack4(reinterpret_cast<const Pix*>(st + G::RAW_BYTES) + r * TW + 4 * q, ds);
+                unpack4_in(raw + (r + 2) * G::RAW_W + G::HX + 4 * q, box.p, box.n, rf);
+                unpack4_in(reinterpret_cast<const Pix*>(st + G::RAW_BYTES) + r * TW + 4 * q, st + G::RAW_BYTES,
+                           G::DIST_BYTES, ds);
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const int e = (int)rf[i] - (int)ds[i];
@@ -260,10 +292,10 @@ __global__ void __launch_bounds__(NT) motion_tile_kernel(const TileArgs a) {
             constexpr int CE = G::CH * G::CW;
             const int off = (tid >> 4) * G::CW + 4 * (tid & 15);
             uint32_t ru[4], du[4], rv[4], dv[4];
-            unpack4(sc + off, ru);
-            unpack4(sc + CE + off, du);
-            unpack4(sc + 2 * CE + off, rv);
-            unpack4(sc + 3 * CE + off, dv);
+            unpack4_in(sc + off, sc, G::C_BYTES, ru);
+            unpack4_in(sc + CE + off, sc + CE, G::C_BYTES, du);
+            unpack4_in(sc + 2 * CE + off, sc + 2 * CE, G::C_BYTES, rv);
+            unpack4_in(sc + 3 * CE + off, sc + 3 * CE, G::C_BYTES, dv);
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const int eu = (int)ru[i] - (int)du[i], ev = (int)rv[i] - (int)dv[i];
@@ -305,11 +337,15 @@ __global__ void __launch_bounds__(NT) motion_tile_kernel(const TileArgs a) {
                     t3 += __shfl_xor_sync(0xffffffffu, t3, o);
                 }
             }
-            if (lane == 0 && do_sad) atomicAdd(a.sad_out + f, t0);
+            if (lane == 0 && do_sad && MG_OK(a.sad_out + f, 8, a.sad_out, (size_t)a.n * 8))
+                atomicAdd(a.sad_out + f, t0);
             if constexpr (FUSED) {
-                if (lane == 1) atomicAdd(a.sse_out + 3LL * f + 0, t1);
-                if (lane == 2) atomicAdd(a.sse_out + 3LL * f + 1, t2);
-                if (lane == 3) atomicAdd(a.sse_out + 3LL * f + 2, t3);
+                if (lane == 1 && MG_OK(a.sse_out + 3LL * f + 0, 8, a.sse_out, (size_t)a.n * 24))
+                    atomicAdd(a.sse_out + 3LL * f + 0, t1);
+                if (lane == 2 && MG_OK(a.sse_out + 3LL * f + 1, 8, a.sse_out, (size_t)a.n * 24))
+                    atomicAdd(a.sse_out + 3LL * f + 1, t2);
+                if (lane == 3 && MG_OK(a.sse_out + 3LL * f + 2, 8, a.sse_out, (size_t)a.n * 24))
+                    atomicAdd(a.sse_out + 3LL * f + 2, t3);
             }
         }
     }
@@ -325,8 +361,9 @@ __global__ void __launch_bounds__(NT) motion_tile_kernel(const TileArgs a) {
             for (int i = 0; i < 4; ++i) {
                 const int x = x0 + 4 * q + i;
                 if (y < a.h && x < a.w)
-                    reinterpret_cast<Pix*>(a.raw_out + (long long)y * a.raw_pitch)[x] =
-                        raw[(r + 2) * G::RAW_W + G::HX + 4 * q + i];
+                    MG_ST(reinterpret_cast<Pix*>(a.raw_out + (long long)y * a.raw_pitch) + x,
+                          MG_LD(raw + (r + 2) * G::RAW_W + G::HX + 4 * q + i, raw, G::RAW_BYTES),
+                          a.raw_out, (size_t)a.h * a.raw_pitch);
             }
         }
         return;
@@ -338,7 +375,9 @@ __global__ void __launch_bounds__(NT) motion_tile_kernel(const TileArgs a) {
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const int x = x0 + 4 * q + i;
-                if (y < a.h && x < a.w) a.bprev_out[(long long)y * a.bprev_pitch + x] = (uint16_t)bp[k][i];
+                if (y < a.h && x < a.w)
+                    MG_ST(a.bprev_out + (long long)y * a.bprev_pitch + x, (uint16_t)bp[k][i], a.bprev_out,
+                          (size_t)a.h * a.bprev_pitch * sizeof(uint16_t));
             }
         }
     }

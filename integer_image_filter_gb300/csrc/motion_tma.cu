@@ -51,13 +51,16 @@ constexpr long long kWaitCycles = 1LL << 31;  // default wait bound: about one s
 // the 4 centre-row words (the reference luma of the warp's output rows) for
 // the squared error.  8-bit samples use byte-pair dot products: rows are
 // interleaved two at a time so that one dp2a applies two taps to two rows of
-// one column (exact: sums stay below 2^24).
+// one column (exact: sums stay below 2^24).  `box` and `vrows` are the staged
+// box and the warp's V rows (the bounds-checked build checks every access
+// against them).
 template <typename RowOff>
 __device__ __forceinline__ void vertical_quad(const uint8_t* src, RowOff ro, uint32_t* dst,
-                                              uint32_t rnd, int sh, uint32_t (&center)[4]) {
+                                              uint32_t rnd, int sh, uint32_t (&center)[4],
+                                              [[maybe_unused]] Span box, [[maybe_unused]] Span vrows) {
     uint32_t wv[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) wv[i] = *reinterpret_cast<const uint32_t*>(src + ro(i));
+    for (int i = 0; i < 8; ++i) wv[i] = MG_LD(reinterpret_cast<const uint32_t*>(src + ro(i)), box.p, box.n);
 #pragma unroll
     for (int i = 0; i < 4; ++i) center[i] = wv[i + 2];
     uint32_t lo[7], hi[7];  // rows (i, i+1): columns 0,1 in lo, columns 2,3 in hi
@@ -76,15 +79,16 @@ __device__ __forceinline__ void vertical_quad(const uint8_t* src, RowOff ro, uin
         o.y = __dp2a_hi(T01, lo[j], __dp2a_hi(T23, lo[j + 2], __dp2a_hi(T_4, lo[j + 3], rnd))) >> sh;
         o.z = __dp2a_lo(T01, hi[j], __dp2a_lo(T23, hi[j + 2], __dp2a_lo(T_4, hi[j + 3], rnd))) >> sh;
         o.w = __dp2a_hi(T01, hi[j], __dp2a_hi(T23, hi[j + 2], __dp2a_hi(T_4, hi[j + 3], rnd))) >> sh;
-        *reinterpret_cast<uint4*>(dst + j * SVW) = o;
+        MG_ST(reinterpret_cast<uint4*>(dst + j * SVW), o, vrows.p, vrows.n);
     }
 }
 template <typename RowOff>
 __device__ __forceinline__ void vertical_quad(const uint16_t* src, RowOff ro, uint32_t* dst,
-                                              uint32_t rnd, int sh, uint32_t (&center)[4]) {
+                                              uint32_t rnd, int sh, uint32_t (&center)[4],
+                                              [[maybe_unused]] Span box, [[maybe_unused]] Span vrows) {
     uint32_t p[8][4];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) unpack4(src + ro(i), p[i]);
+    for (int i = 0; i < 8; ++i) unpack4_in(src + ro(i), box.p, box.n, p[i]);
 #pragma unroll
     for (int i = 0; i < 4; ++i) center[i] = 0;  // 16-bit SSE reloads its samples
 #pragma unroll
@@ -94,7 +98,7 @@ __device__ __forceinline__ void vertical_quad(const uint16_t* src, RowOff ro, ui
         o.y = vtap(p[j][1], p[j + 1][1], p[j + 2][1], p[j + 3][1], p[j + 4][1], rnd, sh);
         o.z = vtap(p[j][2], p[j + 1][2], p[j + 2][2], p[j + 3][2], p[j + 4][2], rnd, sh);
         o.w = vtap(p[j][3], p[j + 1][3], p[j + 2][3], p[j + 3][3], p[j + 4][3], rnd, sh);
-        *reinterpret_cast<uint4*>(dst + j * SVW) = o;
+        MG_ST(reinterpret_cast<uint4*>(dst + j * SVW), o, vrows.p, vrows.n);
     }
 }
 
@@ -118,10 +122,11 @@ __device__ __forceinline__ void horizontal_quad(const uint32_t (&wv)[12], uint32
 
 // Unrounded vertical sums of 4 rows x 4 columns (8 staged rows from src).
 template <typename RowOff>
-__device__ __forceinline__ void vertical_sums(const uint8_t* src, RowOff ro, uint32_t (&x)[4][4]) {
+__device__ __forceinline__ void vertical_sums(const uint8_t* src, RowOff ro, uint32_t (&x)[4][4],
+                                              [[maybe_unused]] Span box) {
     uint32_t wv[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) wv[i] = *reinterpret_cast<const uint32_t*>(src + ro(i));
+    for (int i = 0; i < 8; ++i) wv[i] = MG_LD(reinterpret_cast<const uint32_t*>(src + ro(i)), box.p, box.n);
     uint32_t lo[7], hi[7];
 #pragma unroll
     for (int i = 0; i < 7; ++i) {
@@ -140,10 +145,11 @@ __device__ __forceinline__ void vertical_sums(const uint8_t* src, RowOff ro, uin
     }
 }
 template <typename RowOff>
-__device__ __forceinline__ void vertical_sums(const uint16_t* src, RowOff ro, uint32_t (&x)[4][4]) {
+__device__ __forceinline__ void vertical_sums(const uint16_t* src, RowOff ro, uint32_t (&x)[4][4],
+                                              [[maybe_unused]] Span box) {
     uint32_t p[8][4];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) unpack4(src + ro(i), p[i]);
+    for (int i = 0; i < 8; ++i) unpack4_in(src + ro(i), box.p, box.n, p[i]);
 #pragma unroll
     for (int j = 0; j < 4; ++j)
 #pragma unroll
@@ -195,6 +201,7 @@ __global__ void __launch_bounds__(Shape::NTK, Shape::MINB)
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     // each warp owns output rows RPW w .. RPW w + RPW-1 of the tile; its V rows are private
     uint32_t* sV = reinterpret_cast<uint32_t*>(smem + STAGES * STAGE) + warp * 4 * SVW;
+    [[maybe_unused]] const Span vrows{sV, 4 * SVW * sizeof(uint32_t)};   // this warp's V rows
     // border tiles of every chunk first, interior tiles after them (tile_of_block)
     int tx, ty, cz;
     tile_of_block(a.w, a.h, gridDim.x, gridDim.y, gridDim.z,
@@ -227,6 +234,7 @@ __global__ void __launch_bounds__(Shape::NTK, Shape::MINB)
         wcount[0] = wcount[1] = 0;
     }
     for (int i = tid; i < 2 * 4 * 32; i += NTK) (&wsum[0][0][0])[i] = 0;
+    MG_BC_BEGIN(a.err);
     if (tid < G::RAW_ROWS) {
         // mirror on read: the boxes arrive zero-filled outside the frame; a row
         // y0 - 2 + r outside [0, h) is read from its mirror, clamped into the
@@ -291,7 +299,10 @@ __global__ void __launch_bounds__(Shape::NTK, Shape::MINB)
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const int x = x0 + 4 * q + i;
-            bp[k][i] = (use_prev && y < a.h && x < a.w) ? a.bprev[(long long)y * a.bprev_pitch + x] : 0u;
+            bp[k][i] = (use_prev && y < a.h && x < a.w)
+                           ? MG_LD(a.bprev + (long long)y * a.bprev_pitch + x, a.bprev,
+                                   (size_t)a.h * a.bprev_pitch * sizeof(uint16_t))
+                           : 0u;
         }
     }
     // valid columns of this thread's quad in each of its rows (edge tiles)
@@ -345,14 +356,17 @@ __global__ void __launch_bounds__(Shape::NTK, Shape::MINB)
             if (v) {
                 const long long g = first + jl;
                 const unsigned long long t = atomicExch(&wsum[wb][0][lane], (Win)0);
-                if (t) atomicAdd(a.sad_out + g, t);
+                if (t && MG_OK(a.sad_out + g, 8, a.sad_out, (size_t)a.n * 8)) atomicAdd(a.sad_out + g, t);
                 if constexpr (FUSED) {
                     const unsigned long long ty = atomicExch(&wsum[wb][1][lane], (Win)0);
                     const unsigned long long tu = atomicExch(&wsum[wb][2][lane], (Win)0);
                     const unsigned long long tv = atomicExch(&wsum[wb][3][lane], (Win)0);
-                    if (ty) atomicAdd(a.sse_out + 3LL * g, ty);
-                    if (tu) atomicAdd(a.sse_out + 3LL * g + 1, tu);
-                    if (tv) atomicAdd(a.sse_out + 3LL * g + 2, tv);
+                    if (MG_OK(a.sse_out + 3LL * g, 8, a.sse_out, (size_t)a.n * 24) &&
+                        MG_OK(a.sse_out + 3LL * g + 2, 8, a.sse_out, (size_t)a.n * 24)) {
+                        if (ty) atomicAdd(a.sse_out + 3LL * g, ty);
+                        if (tu) atomicAdd(a.sse_out + 3LL * g + 1, tu);
+                        if (tv) atomicAdd(a.sse_out + 3LL * g + 2, tv);
+                    }
                 }
             }
             if (lane == 0) wcount[wb] = 0;
@@ -370,6 +384,7 @@ __global__ void __launch_bounds__(Shape::NTK, Shape::MINB)
             const bool ok = mbar_wait_bounded(&full[s], parity, wait_cycles);
             timed_out |= !ok;
             unsigned char* st = smem + s * STAGE;
+            [[maybe_unused]] const Span box{st, (size_t)G::RAW_BYTES};   // the staged luma box
             // the stage of frame l-1 takes frame l+STAGES-1 as soon as every warp
             // has released it
             if (tid == 0 && l >= 1 && l + STAGES - 1 < cnt) {
@@ -394,7 +409,10 @@ __global__ void __launch_bounds__(Shape::NTK, Shape::MINB)
                 const int hr = RPW * warp + halo_r;
                 uint32_t t[5];
 #pragma unroll
-                for (int k = 0; k < 5; ++k) t[k] = c[remap ? rowsrc[hr + k] : (hr + k) * G::RAW_W];
+                for (int k = 0; k < 5; ++k) {
+                    const int ri = remap ? MG_LD(&rowsrc[hr + k], rowsrc, sizeof(rowsrc)) : (hr + k) * G::RAW_W;
+                    t[k] = MG_LD(c + ri, box.p, box.n);
+                }
                 if constexpr (V2) {
                     const uint32_t x = vsum(t[0], t[1], t[2], t[3], t[4]);
                     hv = (uint32_t)vdiff<Pix>(hxp, x, rnd, sh);
@@ -418,9 +436,9 @@ __global__ void __launch_bounds__(Shape::NTK, Shape::MINB)
                     const Pix* colv = reinterpret_cast<const Pix*>(st + off_vcol);
                     const int r0 = RPW * warp + 4 * h;
                     if (remap)
-                        vertical_sums(colv, [&](int i) { return rowsrc[r0 + i]; }, x);
+                        vertical_sums(colv, [&](int i) { return MG_LD(&rowsrc[r0 + i], rowsrc, sizeof(rowsrc)); }, x, box);
                     else
-                        vertical_sums(colv, [=](int i) { return (r0 + i) * G::RAW_W; }, x);
+                        vertical_sums(colv, [=](int i) { return (r0 + i) * G::RAW_W; }, x, box);
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
                         uint4 o;
@@ -428,7 +446,7 @@ __global__ void __launch_bounds__(Shape::NTK, Shape::MINB)
                         o.y = (uint32_t)vdiff<Pix>(bp[4 * h + j][1], x[j][1], rnd, sh);
                         o.z = (uint32_t)vdiff<Pix>(bp[4 * h + j][2], x[j][2], rnd, sh);
                         o.w = (uint32_t)vdiff<Pix>(bp[4 * h + j][3], x[j][3], rnd, sh);
-                        *reinterpret_cast<uint4*>(sV + 4 + 4 * lane + j * SVW) = o;
+                        MG_ST(reinterpret_cast<uint4*>(sV + 4 + 4 * lane + j * SVW), o, vrows.p, vrows.n);
 #pragma unroll
                         for (int i = 0; i < 4; ++i) bp[4 * h + j][i] = x[j][i];
                     }
@@ -436,14 +454,14 @@ __global__ void __launch_bounds__(Shape::NTK, Shape::MINB)
                     const Pix* colv = reinterpret_cast<const Pix*>(st + off_vcol);
                     const int r0 = RPW * warp + 4 * h;
                     if (remap)
-                        vertical_quad(colv, [&](int i) { return rowsrc[r0 + i]; },
-                                      sV + 4 + 4 * lane, rnd, sh, center);
+                        vertical_quad(colv, [&](int i) { return MG_LD(&rowsrc[r0 + i], rowsrc, sizeof(rowsrc)); },
+                                      sV + 4 + 4 * lane, rnd, sh, center, box, vrows);
                     else
                         vertical_quad(colv, [=](int i) { return (r0 + i) * G::RAW_W; },
-                                      sV + 4 + 4 * lane, rnd, sh, center);
+                                      sV + 4 + 4 * lane, rnd, sh, center, box, vrows);
                 }
                 if ((halo_r >> 2) == h)
-                    sV[(halo_r & 3) * SVW + 4 + halo_off] = hv;
+                    MG_ST(&sV[(halo_r & 3) * SVW + 4 + halo_off], hv, vrows.p, vrows.n);
                 __syncwarp();
                 if (!INTERIOR && (pl || pr)) {
                     // the column mirror on V (the vertical pass works per column):
@@ -459,7 +477,9 @@ __global__ void __launch_bounds__(Shape::NTK, Shape::MINB)
                             dc = a.w - x0 + k;
                             sc = a.w - x0 - 2 - k;
                         }
-                        if (dc >= -2 && dc <= TW + 1) sV[row * SVW + 4 + dc] = sV[row * SVW + 4 + sc];
+                        if (dc >= -2 && dc <= TW + 1)
+                            MG_ST(&sV[row * SVW + 4 + dc], MG_LD(&sV[row * SVW + 4 + sc], vrows.p, vrows.n),
+                                  vrows.p, vrows.n);
                     }
                     __syncwarp();
                 }
@@ -469,9 +489,9 @@ __global__ void __launch_bounds__(Shape::NTK, Shape::MINB)
                 for (int kk = 0; kk < 4; ++kk) {
                     const int k = 4 * h + kk;
                     const uint32_t* v = sV + kk * SVW + 4 * q;
-                    const uint4 A = *reinterpret_cast<const uint4*>(v);
-                    const uint4 Bq = *reinterpret_cast<const uint4*>(v + 4);
-                    const uint4 C = *reinterpret_cast<const uint4*>(v + 8);
+                    const uint4 A = MG_LD(reinterpret_cast<const uint4*>(v), vrows.p, vrows.n);
+                    const uint4 Bq = MG_LD(reinterpret_cast<const uint4*>(v + 4), vrows.p, vrows.n);
+                    const uint4 C = MG_LD(reinterpret_cast<const uint4*>(v + 8), vrows.p, vrows.n);
                     if constexpr (V2) {
                         // SAD of |blur(prev - cur)|; invalid samples add 0
                         const int wi[12] = {(int)A.x, (int)A.y, (int)A.z, (int)A.w, (int)Bq.x, (int)Bq.y,
@@ -499,14 +519,15 @@ __global__ void __launch_bounds__(Shape::NTK, Shape::MINB)
                     if constexpr (FUSED) {
                         const Pix* dp = reinterpret_cast<const Pix*>(st + off_dist + k * TW * G::S);
                         if constexpr (sizeof(Pix) == 1) {
-                            uint32_t d = __vabsdiffu4(center[kk], *reinterpret_cast<const uint32_t*>(dp));
+                            uint32_t d = __vabsdiffu4(
+                                center[kk], MG_LD(reinterpret_cast<const uint32_t*>(dp), st + G::RAW_BYTES, G::DIST_BYTES));
                             if (!INTERIOR && !full_tile)
                                 d &= nvalid[k] <= 0 ? 0u : (0xffffffffu >> (8 * (4 - nvalid[k])));
                             sse_y = __dp4a(d, d, sse_y);
                         } else {
                             uint32_t rf[4], ds[4];
-                            unpack4(reinterpret_cast<const Pix*>(st + off_ref + k * G::RAW_W * G::S), rf);
-                            unpack4(dp, ds);
+                            unpack4_in(reinterpret_cast<const Pix*>(st + off_ref + k * G::RAW_W * G::S), box.p, box.n, rf);
+                            unpack4_in(dp, st + G::RAW_BYTES, G::DIST_BYTES, ds);
 #pragma unroll
                             for (int i = 0; i < 4; ++i) {
                                 const long long e = (long long)rf[i] - (long long)ds[i];
@@ -521,22 +542,25 @@ __global__ void __launch_bounds__(Shape::NTK, Shape::MINB)
                 // CRW w .. CRW w + CRW-1, SPL samples per lane; outside the picture
                 // both sides were zero-filled, so they add 0
                 const unsigned char* sc = st + off_chroma;
+                [[maybe_unused]] const unsigned char* cb = st + G::RAW_BYTES + G::DIST_BYTES;   // chroma tiles
 #pragma unroll
                 for (int j = 0; j < SH::SPL / 4; ++j) {
                     const unsigned char* cj = sc + 4 * j * G::S;
                     if constexpr (sizeof(Pix) == 1) {
-                        const uint32_t du = __vabsdiffu4(*reinterpret_cast<const uint32_t*>(cj),
-                                                         *reinterpret_cast<const uint32_t*>(cj + G::C_BYTES));
-                        const uint32_t dv = __vabsdiffu4(*reinterpret_cast<const uint32_t*>(cj + 2 * G::C_BYTES),
-                                                         *reinterpret_cast<const uint32_t*>(cj + 3 * G::C_BYTES));
+                        const uint32_t du = __vabsdiffu4(
+                            MG_LD(reinterpret_cast<const uint32_t*>(cj), cb, G::C_BYTES),
+                            MG_LD(reinterpret_cast<const uint32_t*>(cj + G::C_BYTES), cb + G::C_BYTES, G::C_BYTES));
+                        const uint32_t dv = __vabsdiffu4(
+                            MG_LD(reinterpret_cast<const uint32_t*>(cj + 2 * G::C_BYTES), cb + 2 * G::C_BYTES, G::C_BYTES),
+                            MG_LD(reinterpret_cast<const uint32_t*>(cj + 3 * G::C_BYTES), cb + 3 * G::C_BYTES, G::C_BYTES));
                         sse_u = __dp4a(du, du, sse_u);
                         sse_v = __dp4a(dv, dv, sse_v);
                     } else {
                         uint32_t ru[4], du[4], rv[4], dv[4];
-                        unpack4(reinterpret_cast<const Pix*>(cj), ru);
-                        unpack4(reinterpret_cast<const Pix*>(cj + G::C_BYTES), du);
-                        unpack4(reinterpret_cast<const Pix*>(cj + 2 * G::C_BYTES), rv);
-                        unpack4(reinterpret_cast<const Pix*>(cj + 3 * G::C_BYTES), dv);
+                        unpack4_in(reinterpret_cast<const Pix*>(cj), cb, G::C_BYTES, ru);
+                        unpack4_in(reinterpret_cast<const Pix*>(cj + G::C_BYTES), cb + G::C_BYTES, G::C_BYTES, du);
+                        unpack4_in(reinterpret_cast<const Pix*>(cj + 2 * G::C_BYTES), cb + 2 * G::C_BYTES, G::C_BYTES, rv);
+                        unpack4_in(reinterpret_cast<const Pix*>(cj + 3 * G::C_BYTES), cb + 3 * G::C_BYTES, G::C_BYTES, dv);
 #pragma unroll
                         for (int i = 0; i < 4; ++i) {
                             const long long eu = (long long)ru[i] - (long long)du[i];
@@ -598,8 +622,9 @@ __global__ void __launch_bounds__(Shape::NTK, Shape::MINB)
             for (int i = 0; i < 4; ++i) {
                 const int x = x0 + 4 * q + i;
                 if (y < a.h && x < a.w)
-                    reinterpret_cast<Pix*>(a.raw_out + (long long)y * a.raw_pitch)[x] =
-                        raw[(RPW * warp + k + 2) * G::RAW_W + G::HX + 4 * q + i];
+                    MG_ST(reinterpret_cast<Pix*>(a.raw_out + (long long)y * a.raw_pitch) + x,
+                          MG_LD(raw + (RPW * warp + k + 2) * G::RAW_W + G::HX + 4 * q + i, raw, G::RAW_BYTES),
+                          a.raw_out, (size_t)a.h * a.raw_pitch);
             }
         }
         return;
@@ -611,7 +636,9 @@ __global__ void __launch_bounds__(Shape::NTK, Shape::MINB)
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const int x = x0 + 4 * q + i;
-                if (y < a.h && x < a.w) a.bprev_out[(long long)y * a.bprev_pitch + x] = (uint16_t)bp[k][i];
+                if (y < a.h && x < a.w)
+                    MG_ST(a.bprev_out + (long long)y * a.bprev_pitch + x, (uint16_t)bp[k][i], a.bprev_out,
+                          (size_t)a.h * a.bprev_pitch * sizeof(uint16_t));
             }
         }
     }

@@ -2,6 +2,7 @@
 // the staged regions and the small per-sample helpers of the 5-tap passes.
 #pragma once
 
+#include "bounds_check.cuh"
 #include "motion_common.cuh"
 #include "motion_internal.h"
 
@@ -46,6 +47,15 @@ __device__ __forceinline__ void unpack4(const uint8_t* p, uint32_t (&o)[4]) {
 __device__ __forceinline__ void unpack4(const uint16_t* p, uint32_t (&o)[4]) {
     const uint2 w = *reinterpret_cast<const uint2*>(p);
     o[0] = w.x & 0xffffu; o[1] = w.x >> 16; o[2] = w.y & 0xffffu; o[3] = w.y >> 16;
+}
+
+// unpack4 of 4 samples that must lie inside [lo, lo + bytes) (checked build)
+template <typename Pix>
+__device__ __forceinline__ void unpack4_in(const Pix* p, const void* lo, size_t bytes, uint32_t (&o)[4]) {
+    if (MG_OK(p, 4 * sizeof(Pix), lo, bytes))
+        unpack4(p, o);
+    else
+        o[0] = o[1] = o[2] = o[3] = 0;
 }
 
 // One 5-tap pass with symmetric taps: (t0 (a + e) + t1 (b + d) + t2 c + rnd) >> sh.
