@@ -426,23 +426,46 @@ def run_sequence_workload(args):
         submit = ctx.submit_batch_v2 if args.v2 else ctx.submit_batch
 
         def step():
+            # the calls go to the current stream: the timing stream, or the
+            # capture stream of a CUDA graph
+            cur = torch.cuda.current_stream(dev)
             ctx.reset()
             for b0 in range(0, n, batch):
-                submit(d[b0:b0 + batch], sad[b0:b0 + batch], stream=stream)
+                submit(d[b0:b0 + batch], sad[b0:b0 + batch], stream=cur)
 
         for _ in range(max(args.warmup, 3)):
             step()
         torch.cuda.synchronize(dev)
+        run = step
+        l0 = iif.motion_kernel_launch_count()
+        if args.graph:
+            # one step captured as a CUDA graph (the library launches counted at
+            # capture are the ones every replay runs)
+            side = torch.cuda.Stream(dev)
+            side.wait_stream(stream)
+            with torch.cuda.stream(side):
+                step()
+            stream.wait_stream(side)
+            torch.cuda.synchronize(dev)
+            graph = torch.cuda.CUDAGraph()
+            l0 = iif.motion_kernel_launch_count()
+            with torch.cuda.graph(graph):
+                step()
+            launches = iif.motion_kernel_launch_count() - l0
+            run = graph.replay
+            for _ in range(max(args.warmup, 3)):
+                run()
+            torch.cuda.synchronize(dev)
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
-        l0 = iif.motion_kernel_launch_count()
         e0.record(stream)
         for _ in range(args.steps):
-            step()
+            run()
         e1.record(stream)
         torch.cuda.synchronize(dev)
         ms = e0.elapsed_time(e1) / args.steps
-        launches = (iif.motion_kernel_launch_count() - l0) / args.steps
+        if not args.graph:
+            launches = (iif.motion_kernel_launch_count() - l0) / args.steps
         alg = w * h * s * n
         ops = (MOTION_OPS_PER_PIXEL + (1 if args.v2 else 0)) * w * h * n
         lines.append({"metric": "frames/s (batched motion%s SAD)" % ("_v2" if args.v2 else ""),
@@ -453,7 +476,7 @@ def run_sequence_workload(args):
                       "config": {"workload": args.workload + ("_v2" if args.v2 else ""),
                                  "w": w, "h": h, "bpc": bpc,
                                  "frames_per_step": n, "batch": batch,
-                                 "launches_per_step": launches},
+                                 "launches_per_step": launches, "cuda_graph": bool(args.graph)},
                       "roofline": seq_roofline(alg, ops, ms, peak, peak_kind)})
         ctx.close()
     for ln in lines:
@@ -600,6 +623,8 @@ def main(argv=None):
                          "moment_3840x2160_u8_pairs (stand-alone SSE / luma moment sums)")
     ap.add_argument("--batch", type=int, default=0, help="frames per launch (sequence workloads)")
     ap.add_argument("--sweep", action="store_true", help="sweep batch sizes 1..32")
+    ap.add_argument("--graph", action="store_true",
+                    help="sequence workloads: time replays of one step captured as a CUDA graph")
     ap.add_argument("--v2", action="store_true",
                     help="sequence workloads: motion_v2 (blur of prev - cur) instead of motion")
     args = ap.parse_args(argv)

@@ -44,6 +44,19 @@
  *     MOTION_MAX_DIM on each side.
  *   - Calls on one context must not overlap (one stream per context, or
  *     ordered by the caller); distinct contexts are independent.
+ *   - CUDA graphs: the device-result calls (motion_submit_batch,
+ *     motion_v2_submit_batch, motion_psnr_yuv420_batch, psnr_sse,
+ *     psnr_sse_yuv420_batch, moment_sums_batch) enqueue only stream work (an
+ *     output memset and one kernel) and motion_reset changes host state only,
+ *     so a stream capture of them replays the same computation.  A context's sequence state (which
+ *     resident plane holds the previous frame's blur, whether there is one)
+ *     advances when a call is captured, not when it is replayed: capture a
+ *     sequence that starts with motion_reset and every replay computes it
+ *     from its first frame; a direct call after a replay continues from the
+ *     replay's last frame.  Make one direct call of each kind before
+ *     capturing (motion_v2 allocates its raw planes on its first call).  The
+ *     host-buffer and single-frame calls (motion_psnr_yuv420_batch_host,
+ *     motion_submit) synchronise and are not capturable.
  */
 #ifndef MOTION_GB300_H
 #define MOTION_GB300_H
