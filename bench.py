@@ -422,6 +422,8 @@ def run_sequence_workload(args):
     lines = []
     for batch in batches:
         ctx = iif.MotionContext(w, h, bpc)
+        if args.generic:
+            ctx.set_kernel_path(iif.MOTION_PATH_GENERIC)
 
         submit = ctx.submit_batch_v2 if args.v2 else ctx.submit_batch
 
@@ -476,7 +478,8 @@ def run_sequence_workload(args):
                       "config": {"workload": args.workload + ("_v2" if args.v2 else ""),
                                  "w": w, "h": h, "bpc": bpc,
                                  "frames_per_step": n, "batch": batch,
-                                 "launches_per_step": launches, "cuda_graph": bool(args.graph)},
+                                 "launches_per_step": launches, "cuda_graph": bool(args.graph),
+                                 "kernel_path": "generic" if args.generic else "auto"},
                       "roofline": seq_roofline(alg, ops, ms, peak, peak_kind)})
         ctx.close()
     for ln in lines:
@@ -625,6 +628,8 @@ def main(argv=None):
     ap.add_argument("--sweep", action="store_true", help="sweep batch sizes 1..32")
     ap.add_argument("--graph", action="store_true",
                     help="sequence workloads: time replays of one step captured as a CUDA graph")
+    ap.add_argument("--generic", action="store_true",
+                    help="sequence workloads: force the generic (non-TMA) kernel")
     ap.add_argument("--v2", action="store_true",
                     help="sequence workloads: motion_v2 (blur of prev - cur) instead of motion")
     args = ap.parse_args(argv)
