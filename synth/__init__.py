@@ -7,7 +7,9 @@ are fed the same arrays made here.
 
 Recipes (each one fixed by its seed):
 
-* ``uniform_frames`` -- samples i.i.d. uniform over [0, 2^bpc - 1].
+* ``uniform_frames`` / ``uniform_yuv420`` -- samples i.i.d. uniform over
+  [0, 2^bpc - 1] (integer draws only: identical on every platform, which the
+  stored expected values in tests/golden rely on).
 * ``smooth_sequence`` -- a smooth luma field, 128 + sum of 8 random 2-D
   sinusoids (amplitudes a_k ~ U(0, 100/8), so the sum stays within +-100;
   spatial frequencies of 0.5 to 8 cycles per frame in each axis with random
@@ -49,6 +51,19 @@ def uniform_frames(seed: int, n: int, w: int, h: int, bpc: int = 8) -> np.ndarra
     rng = np.random.default_rng(seed)
     hi = (1 << bpc)
     return rng.integers(0, hi, size=(n, h, w), dtype=np.int64).astype(_dtype(bpc))
+
+
+def uniform_yuv420(seed: int, n: int, w: int, h: int, bpc: int = 8) -> "Yuv420Batch":
+    """4:2:0 pairs whose six planes are i.i.d. uniform over [0, 2^bpc - 1],
+    drawn in the order ref Y, U, V, dist Y, U, V from one generator (integer
+    draws only, so the same seed gives the same planes on every platform)."""
+    rng = np.random.default_rng(seed)
+    hi = 1 << bpc
+    cw, ch = chroma_dims(w, h)
+    dt = _dtype(bpc)
+    shapes = [(n, h, w), (n, ch, cw), (n, ch, cw)] * 2
+    planes = [rng.integers(0, hi, size=sh, dtype=np.int64).astype(dt) for sh in shapes]
+    return Yuv420Batch(w, h, bpc, *planes)
 
 
 def translation_walk(rng: np.random.Generator, n: int, max_shift: int) -> np.ndarray:
