@@ -47,7 +47,7 @@
  *   - CUDA graphs: the device-result calls (motion_submit_batch,
  *     motion_v2_submit_batch, motion_psnr_yuv420_batch, psnr_sse,
  *     psnr_sse_yuv420_batch, moment_sums_batch) enqueue only stream work (an
- *     output memset and one kernel) and motion_reset changes host state only,
+ *     output memset and their kernels) and motion_reset changes host state only,
  *     so a stream capture of them replays the same computation.  A context's sequence state (which
  *     resident plane holds the previous frame's blur, whether there is one)
  *     advances when a call is captured, not when it is replayed: capture a
@@ -56,7 +56,9 @@
  *     replay's last frame.  Make one direct call of each kind before
  *     capturing (motion_v2 allocates its raw planes on its first call).  The
  *     host-buffer and single-frame calls (motion_psnr_yuv420_batch_host,
- *     motion_submit) synchronise and are not capturable.
+ *     motion_submit) synchronise and are not capturable.  A call whose planes
+ *     are not 16-byte aligned adds one copy kernel (see motion_set_kernel_path)
+ *     and allocates its scratch the first time: make it once directly too.
  */
 #ifndef MOTION_GB300_H
 #define MOTION_GB300_H
@@ -234,9 +236,12 @@ MOTION_API int psnr_from_sse(uint64_t sse, uint64_t n_samples, int bpc, double* 
                   double* psnr_db);
 
 /* Kernel selection for a context (diagnostics and tests): MOTION_PATH_AUTO
- * uses the TMA kernel whenever every plane is 16-byte aligned (base, pitch,
- * stride) and the generic kernel otherwise; MOTION_PATH_GENERIC always uses
- * the generic kernel.  Results are identical on both paths. */
+ * always uses the TMA kernel -- planes whose base, pitch or frame stride is
+ * not a multiple of 16 bytes are first copied, in one more launch, into a
+ * scratch the context owns with 16-byte-aligned rows (allocated by the first
+ * such call, n frames' or pairs' worth, grown when a call needs more, freed
+ * by motion_destroy); MOTION_PATH_GENERIC always uses the generic kernel,
+ * which reads any layout in place.  Results are identical on both paths. */
 #define MOTION_PATH_AUTO 0
 #define MOTION_PATH_GENERIC 1
 MOTION_API int motion_set_kernel_path(motion_ctx* ctx, int path);

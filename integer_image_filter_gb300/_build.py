@@ -21,7 +21,7 @@ OUT_DIR = os.path.join(PKG, "_lib")
 LIB_NAME = "libmotion_gb300.so"
 CHECKED_LIB_NAME = "libmotion_gb300_checked.so"
 SOURCES = ["motion_capi.cu", "motion_tile.cu", "motion_tma.cu", "psnr_sse.cu", "motion_noalloc.cu",
-           "moment.cu"]
+           "moment.cu", "repitch.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

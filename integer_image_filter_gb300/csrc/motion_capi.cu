@@ -93,6 +93,11 @@ struct motion_ctx {
     size_t raw_pitch = 0;
     int raw_cur = 0;
     int v2_has_prev = 0;
+    // planes a call passes with rows the TMA cannot address are first copied
+    // here with 16-byte-aligned rows (allocated by the first such call, grown
+    // when a call needs more)
+    uint8_t* d_rp = nullptr;
+    size_t rp_bytes = 0;
 };
 
 namespace {
@@ -123,8 +128,68 @@ void free_staging(motion_ctx* c) {
     c->h_res_pairs = 0;
 }
 
-// The TMA kernel when the layout allows it, else the generic kernel.
-int launch_motion(motion_ctx* c, const mg::TileArgs& a, bool fused, cudaStream_t s) {
+// Planes whose base, pitch or frame stride the TMA cannot take are copied
+// into the context's scratch with 16-byte-aligned rows (one bandwidth-bound
+// launch), and `a` is pointed at the copies, so the TMA kernel serves every
+// layout; the generic kernel stays for motion_set_kernel_path(GENERIC).
+int repitch_for_tma(motion_ctx* c, mg::TileArgs& a, bool fused, cudaStream_t s) {
+    if (c->force_generic || a.n <= 0 || mg::tma_usable(a, fused)) return MOTION_OK;
+    const long long S = sample_bytes(c->bpc);
+    const long long py = ((long long)c->w * S + 15) & ~15LL, sy = py * c->h;
+    const long long puv = ((long long)c->cw * S + 15) & ~15LL, suv = puv * c->ch;
+    const size_t need = (size_t)a.n * (size_t)(fused ? 2 * sy + 4 * suv : sy);
+    if (c->rp_bytes < need) {
+        if (c->d_rp) cudaFree(c->d_rp);
+        c->d_rp = nullptr;
+        c->rp_bytes = 0;
+        MG_CUDA(cudaMalloc(&c->d_rp, need));
+        c->rp_bytes = need;
+    }
+    mg::RepitchArgs r;
+    std::memset(&r, 0, sizeof(r));
+    r.n = a.n;
+    r.err = c->d_err;
+    const uint8_t* src[6] = {a.ref_y, a.dist_y, a.ref_u, a.dist_u, a.ref_v, a.dist_v};
+    uint8_t* base = c->d_rp;
+    r.planes = fused ? 6 : 1;
+    for (int p = 0; p < r.planes; ++p) {
+        const bool luma = p < 2;
+        mg::RepitchPlane& q = r.p[p];
+        q.src = src[p];
+        q.pitch = luma ? a.pitch_y : a.pitch_uv;
+        q.stride = luma ? a.stride_y : a.stride_uv;
+        q.dst = base;
+        q.dpitch = luma ? py : puv;
+        q.dstride = luma ? sy : suv;
+        q.row_bytes = (int)((luma ? c->w : c->cw) * S);
+        q.rows = luma ? c->h : c->ch;
+        base += (size_t)a.n * (size_t)q.dstride;
+    }
+    int launched = 0;
+    const cudaError_t e = mg::launch_repitch(r, s, c->sm_count, &launched);
+    g_launches += (uint64_t)launched;
+    if (e != cudaSuccess) return cuda_fail(e);
+    a.ref_y = r.p[0].dst;
+    a.pitch_y = py;
+    a.stride_y = sy;
+    if (fused) {
+        a.dist_y = r.p[1].dst;
+        a.ref_u = r.p[2].dst;
+        a.dist_u = r.p[3].dst;
+        a.ref_v = r.p[4].dst;
+        a.dist_v = r.p[5].dst;
+        a.pitch_uv = puv;
+        a.stride_uv = suv;
+    }
+    a.aligned16 = 1;
+    return MOTION_OK;
+}
+
+// The TMA kernel (after repitch_for_tma, for any layout), or the generic
+// kernel when motion_set_kernel_path asks for it.
+int launch_motion(motion_ctx* c, mg::TileArgs a, bool fused, cudaStream_t s) {
+    int rc = repitch_for_tma(c, a, fused, s);
+    if (rc) return rc;
     int launched = 0;
     bool used = false;
     cudaError_t e = cudaSuccess;
@@ -248,6 +313,7 @@ int motion_destroy(motion_ctx* c) {
     if (c->d_bprev[1]) cudaFree(c->d_bprev[1]);
     if (c->d_raw[0]) cudaFree(c->d_raw[0]);
     if (c->d_raw[1]) cudaFree(c->d_raw[1]);
+    if (c->d_rp) cudaFree(c->d_rp);
     if (c->d_slot) cudaFree(c->d_slot);
     if (c->d_err) cudaFree(c->d_err);
     if (c->h_slot) cudaFreeHost(c->h_slot);
@@ -322,6 +388,7 @@ int motion_v2_submit_batch(motion_ctx* c, const void* d_frames, int n, size_t fr
     a.raw_prev = c->d_raw[c->raw_cur];
     a.raw_out = c->d_raw[c->raw_cur ^ 1];
     a.raw_pitch = (long long)c->raw_pitch;
+    if ((rc = repitch_for_tma(c, a, false, s))) return rc;
     int launched = 0;
     bool used = false;
     cudaError_t e = cudaSuccess;

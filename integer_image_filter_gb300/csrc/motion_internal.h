@@ -74,6 +74,9 @@ cudaError_t launch_motion_tma(const TileArgs& a, bool fused, cudaStream_t s, int
 // kernel when the layout allows (*used), else the generic kernel.
 cudaError_t launch_motion_v2_tma(const TileArgs& a, cudaStream_t s, int* launches, bool* used);
 cudaError_t launch_motion_v2_tile(const TileArgs& a, cudaStream_t s, int* launches);
+// Whether the TMA kernel can take a's planes (16-byte strides and bases; the
+// driver's tensor-map encoder available).
+bool tma_usable(const TileArgs& a, bool fused);
 // The output tile of the motion kernels (the TMA kernel's TW x TH).
 constexpr int kTileW = 128, kTileH = 32;
 // The tile and frame chunk of block `lin` (x fastest, then y, then chunk) of a
@@ -115,6 +118,26 @@ __host__ __device__ inline void tile_of_block(int w, int h, int gx, int gy, int 
 // `slots` CTAs resident on the device at once; 1 <= result <= max_c.
 int plan_frame_chunks(long long tiles, long long slots, int n, int max_c);
 cudaError_t launch_sse(const SseArgs& a, cudaStream_t s, int sm_count, int* launches);
+
+// Copies of planes into rows the TMA can address (repitch.cu): n frames of
+// `rows` rows of row_bytes bytes, source rows `pitch` and frames `stride` bytes
+// apart, destination rows dpitch (a multiple of 16) and frames dstride apart.
+constexpr int kRepitchMaxPlanes = 6;
+struct RepitchPlane {
+    const uint8_t* src;
+    long long pitch, stride;
+    uint8_t* dst;
+    long long dpitch, dstride;
+    int row_bytes, rows;
+};
+struct RepitchArgs {
+    RepitchPlane p[kRepitchMaxPlanes];
+    int planes, n;
+    int* err;   // device error word (the bounds-checked build reports failed checks here)
+};
+// The largest power of two up to 16 dividing every source base, pitch and stride.
+int repitch_granule(const RepitchArgs& a);
+cudaError_t launch_repitch(const RepitchArgs& a, cudaStream_t s, int sm_count, int* launches);
 
 // Moment sums of n luma pairs (sum ref, sum dist, sum ref^2, sum dist^2).
 struct MomentArgs {
