@@ -408,6 +408,11 @@ def run_sequence_workload(args):
     c = synth.CONFIGS[args.workload]
     w, h, bpc = c["w"], c["h"], c["bpc"]
     frames = synth.make(args.workload)
+    if args.trim:
+        # drop the last columns and pack the rows tightly: rows of an odd
+        # width that the TMA cannot address in place
+        w -= args.trim
+        frames = np.ascontiguousarray(frames[:, :, :w])
     n = frames.shape[0]
     s = 1 if bpc == 8 else 2
     dev = torch.device("cuda", 0)
@@ -475,7 +480,8 @@ def run_sequence_workload(args):
                       "unit": "frames/s", "n_gpus": 1, "steps": args.steps,
                       "warmup": max(args.warmup, 3), "ms_per_step": ms, "higher_is_better": True,
                       "dtype": "u8" if bpc == 8 else "u16", "data": "synthetic",
-                      "config": {"workload": args.workload + ("_v2" if args.v2 else ""),
+                      "config": {"workload": args.workload + ("_v2" if args.v2 else "") +
+                                             ("_trim%d" % args.trim if args.trim else ""),
                                  "w": w, "h": h, "bpc": bpc,
                                  "frames_per_step": n, "batch": batch,
                                  "launches_per_step": launches, "cuda_graph": bool(args.graph),
@@ -628,6 +634,8 @@ def main(argv=None):
     ap.add_argument("--sweep", action="store_true", help="sweep batch sizes 1..32")
     ap.add_argument("--graph", action="store_true",
                     help="sequence workloads: time replays of one step captured as a CUDA graph")
+    ap.add_argument("--trim", type=int, default=0,
+                    help="sequence workloads: drop this many columns and pack the rows tightly")
     ap.add_argument("--generic", action="store_true",
                     help="sequence workloads: force the generic (non-TMA) kernel")
     ap.add_argument("--v2", action="store_true",
