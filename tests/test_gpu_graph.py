@@ -78,6 +78,29 @@ def test_motion_and_v2_steps_replay(iif, oracle, bpc):
         assert ctx.device_error() == 0
 
 
+def test_unaligned_step_replays(iif, oracle):
+    """Frames of an odd width packed row after row take the copy kernel and
+    then the TMA kernel; after one direct step (which allocates the copy's
+    scratch) the captured step replays bit-exact."""
+    import torch
+    w, h, n = 213, 40, 6
+    fr = synth.uniform_frames(5, n, w, h, 8)
+    d = torch.from_numpy(fr).cuda()          # rows 213 bytes apart
+    sad = torch.zeros(n, dtype=torch.int64, device="cuda")
+    want = oracle.motion_sad_sequence(fr, 8).astype(np.uint64)
+    with iif.MotionContext(w, h, 8) as ctx:
+        def step():
+            ctx.reset()
+            ctx.submit_batch(d, sad, stream=torch.cuda.current_stream())
+        g = _capture(step)
+        for _ in range(2):
+            sad.zero_()
+            g.replay()
+            torch.cuda.synchronize()
+            assert sad.cpu().numpy().astype(np.uint64).tolist() == want.tolist()
+        assert ctx.device_error() == 0
+
+
 def test_sse_and_moment_steps_replay(iif, oracle):
     import torch
     b = synth.yuv420_pairs(12, 4, 192, 80, max_shift=2, dist_sigma=3.0)
