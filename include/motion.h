@@ -270,6 +270,16 @@ MOTION_API int motion_plan_chunks(int w, int h, int n, int resident_ctas, int* c
  * tile_out). */
 MOTION_API int motion_tile_order(int w, int h, int chunks, long long block, int* tile_out);
 
+/* Test hook for allocation failures (no counterpart in the paper): the nth
+ * device or pinned-host allocation the library makes from now on (1 = the
+ * next one) fails with MOTION_ERR_OUT_OF_MEMORY without reaching the driver;
+ * 0 turns it off.  Library-wide.  Every entry point that allocates (init,
+ * the first motion_v2 call, the first call that needs the copy scratch, the
+ * host-buffer staging and result buffers) then returns the error, frees what
+ * it had allocated for that call, and leaves the context usable.  Errors:
+ * MOTION_ERR_INVALID_ARGUMENT for nth < 0. */
+MOTION_API int motion_inject_alloc_failure(int nth);
+
 /* Test hook for the kernels' bounded waits (no counterpart in the paper):
  * while on, TMA launches on this context expect 16 bytes per stage more than
  * their boxes deliver, so no stage wait can complete, and bound every wait at

@@ -28,6 +28,7 @@ __all__ = [
     "motion_set_kernel_path", "motion_device_error", "MOTION_PATH_AUTO", "MOTION_PATH_GENERIC",
     "motion_submit_batch_noalloc", "motion_set_stall_injection", "moment_sums_batch",
     "moments_from_sums", "motion_v2_submit_batch", "motion_plan_chunks", "motion_tile_order",
+    "motion_inject_alloc_failure",
 ]
 
 EXPORTED_SYMBOLS = (
@@ -37,7 +38,7 @@ EXPORTED_SYMBOLS = (
     "motion_kernel_launch_count", "motion_strerror", "motion_last_cuda_error",
     "motion_set_kernel_path", "motion_device_error", "motion_submit_batch_noalloc",
     "motion_set_stall_injection", "moment_sums_batch", "moments_from_sums",
-    "motion_v2_submit_batch", "motion_plan_chunks", "motion_tile_order",
+    "motion_v2_submit_batch", "motion_plan_chunks", "motion_tile_order", "motion_inject_alloc_failure",
 )
 
 _LIB: ctypes.CDLL | None = None
@@ -82,6 +83,7 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
         "motion_v2_submit_batch": ([P, P, I, Z, Z, P, P], I),
         "motion_plan_chunks": ([I, I, I, I, ctypes.POINTER(I)], I),
         "motion_tile_order": ([I, I, I, ctypes.c_longlong, ctypes.POINTER(I)], I),
+        "motion_inject_alloc_failure": ([I], I),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -442,6 +444,11 @@ MOTION_PATH_GENERIC = 1
 
 def motion_set_kernel_path(ctx: int, path: int) -> None:
     _check(load_library().motion_set_kernel_path(ctx, path), "motion_set_kernel_path")
+
+
+def motion_inject_alloc_failure(nth: int) -> None:
+    """Test hook: the nth allocation of the library from now on fails (0: off)."""
+    _check(load_library().motion_inject_alloc_failure(nth), "motion_inject_alloc_failure")
 
 
 def motion_set_stall_injection(ctx: int, on: bool) -> None:

@@ -15,6 +15,33 @@ namespace {
 
 std::atomic<uint64_t> g_launches{0};
 std::atomic<int> g_last_cuda_error{0};
+// test hook (motion_inject_alloc_failure): the k-th allocation from now fails
+// without reaching the driver; 0 = off
+std::atomic<int> g_fail_alloc_in{0};
+
+bool injected_alloc_failure() {
+    int k = g_fail_alloc_in.load();
+    while (k > 0) {
+        if (g_fail_alloc_in.compare_exchange_weak(k, k - 1)) return k == 1;
+    }
+    return false;
+}
+
+// Every device and pinned allocation of the library goes through these two.
+cudaError_t dev_alloc(void** p, size_t bytes) {
+    if (injected_alloc_failure()) {
+        *p = nullptr;
+        return cudaErrorMemoryAllocation;
+    }
+    return cudaMalloc(p, bytes);
+}
+cudaError_t host_alloc(void** p, size_t bytes) {
+    if (injected_alloc_failure()) {
+        *p = nullptr;
+        return cudaErrorMemoryAllocation;
+    }
+    return cudaHostAlloc(p, bytes, cudaHostAllocDefault);
+}
 
 int cuda_fail(cudaError_t e) {
     g_last_cuda_error.store((int)e);
@@ -142,7 +169,7 @@ int repitch_for_tma(motion_ctx* c, mg::TileArgs& a, bool fused, cudaStream_t s) 
         if (c->d_rp) cudaFree(c->d_rp);
         c->d_rp = nullptr;
         c->rp_bytes = 0;
-        MG_CUDA(cudaMalloc(&c->d_rp, need));
+        MG_CUDA(dev_alloc(reinterpret_cast<void**>(&c->d_rp), need));
         c->rp_bytes = need;
     }
     mg::RepitchArgs r;
@@ -288,13 +315,13 @@ int motion_init(int w, int h, int bpc, motion_ctx** out) {
     if (e == cudaSuccess)
         e = cudaDeviceGetAttribute(&c->sm_count, cudaDevAttrMultiProcessorCount, c->device);
     if (e == cudaSuccess)
-        e = cudaMalloc(&c->d_bprev[0], sizeof(uint16_t) * (size_t)c->bprev_pitch * (size_t)h);
+        e = dev_alloc(reinterpret_cast<void**>(&c->d_bprev[0]), sizeof(uint16_t) * (size_t)c->bprev_pitch * (size_t)h);
     if (e == cudaSuccess)
-        e = cudaMalloc(&c->d_bprev[1], sizeof(uint16_t) * (size_t)c->bprev_pitch * (size_t)h);
-    if (e == cudaSuccess) e = cudaMalloc(&c->d_slot, sizeof(unsigned long long));
-    if (e == cudaSuccess) e = cudaMalloc(&c->d_err, sizeof(int));
+        e = dev_alloc(reinterpret_cast<void**>(&c->d_bprev[1]), sizeof(uint16_t) * (size_t)c->bprev_pitch * (size_t)h);
+    if (e == cudaSuccess) e = dev_alloc(reinterpret_cast<void**>(&c->d_slot), sizeof(unsigned long long));
+    if (e == cudaSuccess) e = dev_alloc(reinterpret_cast<void**>(&c->d_err), sizeof(int));
     if (e == cudaSuccess) e = cudaMemset(c->d_err, 0, sizeof(int));
-    if (e == cudaSuccess) e = cudaMallocHost(&c->h_slot, sizeof(unsigned long long));
+    if (e == cudaSuccess) e = host_alloc(reinterpret_cast<void**>(&c->h_slot), sizeof(unsigned long long));
     if (e != cudaSuccess) {
         motion_destroy(c);
         return cuda_fail(e);
@@ -361,8 +388,8 @@ int motion_v2_submit_batch(motion_ctx* c, const void* d_frames, int n, size_t fr
         // both planes or neither: a failed second allocation leaves no half state
         const size_t pitch_r = ((size_t)c->w * s_bytes + 15) & ~(size_t)15;
         uint8_t* p[2] = {nullptr, nullptr};
-        cudaError_t e = cudaMalloc(&p[0], pitch_r * (size_t)c->h);
-        if (e == cudaSuccess) e = cudaMalloc(&p[1], pitch_r * (size_t)c->h);
+        cudaError_t e = dev_alloc(reinterpret_cast<void**>(&p[0]), pitch_r * (size_t)c->h);
+        if (e == cudaSuccess) e = dev_alloc(reinterpret_cast<void**>(&p[1]), pitch_r * (size_t)c->h);
         if (e != cudaSuccess) {
             if (p[0]) cudaFree(p[0]);
             return cuda_fail(e);
@@ -453,8 +480,8 @@ int motion_reserve_host_staging(motion_ctx* c, int pairs_per_chunk, size_t strid
     free_staging(c);
     const size_t bytes = 2 * (size_t)pairs_per_chunk * (stride_y + 2 * stride_uv);
     for (int k = 0; k < 2; ++k) {
-        MG_CUDA(cudaMalloc(&c->d_stage[k], bytes));
-        MG_CUDA(cudaMalloc(&c->d_res[k], sizeof(unsigned long long) * 4 * (size_t)pairs_per_chunk));
+        MG_CUDA(dev_alloc(reinterpret_cast<void**>(&c->d_stage[k]), bytes));
+        MG_CUDA(dev_alloc(reinterpret_cast<void**>(&c->d_res[k]), sizeof(unsigned long long) * 4 * (size_t)pairs_per_chunk));
         MG_CUDA(cudaEventCreateWithFlags(&c->ev_in[k], cudaEventDisableTiming));
         MG_CUDA(cudaEventCreateWithFlags(&c->ev_done[k], cudaEventDisableTiming));
     }
@@ -486,7 +513,7 @@ int motion_psnr_yuv420_batch_host(motion_ctx* c, int n, const void* ry, const vo
         if (c->h_res) cudaFreeHost(c->h_res);
         c->h_res = nullptr;
         c->h_res_pairs = 0;
-        MG_CUDA(cudaHostAlloc(&c->h_res, sizeof(unsigned long long) * 4 * (size_t)n, cudaHostAllocDefault));
+        MG_CUDA(host_alloc(reinterpret_cast<void**>(&c->h_res), sizeof(unsigned long long) * 4 * (size_t)n));
         c->h_res_pairs = (size_t)n;
     }
     unsigned long long* h_sad = c->h_res;
@@ -710,6 +737,12 @@ int motion_tile_order(int w, int h, int chunks, long long block, int* tile_out) 
     const int gx = (w + mg::kTileW - 1) / mg::kTileW, gy = (h + mg::kTileH - 1) / mg::kTileH;
     if (block < 0 || block >= (long long)gx * gy * chunks) return MOTION_ERR_INVALID_ARGUMENT;
     mg::tile_of_block(w, h, gx, gy, chunks, (int)block, &tile_out[0], &tile_out[1], &tile_out[2]);
+    return MOTION_OK;
+}
+
+int motion_inject_alloc_failure(int nth) {
+    if (nth < 0) return MOTION_ERR_INVALID_ARGUMENT;
+    g_fail_alloc_in.store(nth);
     return MOTION_OK;
 }
 
