@@ -196,6 +196,39 @@ def cpu_oracle_rate(batch, budget_s: float, min_pairs: int = 2):
     return done / dt, done, dt
 
 
+def cpu_oracle_parallel_rate(batch, budget_s: float, cores: int):
+    """The same per-pair oracle work (as cpu_oracle_rate) spread over `cores`
+    threads for about budget_s seconds, cycling through the batch's pairs (the
+    oracle's C calls release the GIL).  Returns (pairs/s, pairs, seconds)."""
+    import itertools
+    from concurrent.futures import ThreadPoolExecutor
+
+    import oracle
+    o = oracle.Oracle()
+    nxt = itertools.count()
+    lock = threading.Lock()
+    t0 = time.perf_counter()
+    stop = t0 + budget_s
+
+    def worker():
+        done = 0
+        while time.perf_counter() < stop:
+            with lock:
+                i = next(nxt) % batch.n
+            lo = max(i - 1, 0)
+            o.motion_sad_sequence(batch.ref_y[lo:i + 1], batch.bpc)
+            o.sse(batch.ref_y[i], batch.dist_y[i], batch.bpc)
+            o.sse(batch.ref_u[i], batch.dist_u[i], batch.bpc)
+            o.sse(batch.ref_v[i], batch.dist_v[i], batch.bpc)
+            done += 1
+        return done
+
+    with ThreadPoolExecutor(cores) as ex:
+        total = sum(f.result() for f in [ex.submit(worker) for _ in range(cores)])
+    dt = time.perf_counter() - t0
+    return total / dt, total, dt
+
+
 def run_reference(args):
     ws, rank, _ = dist_env()
     if rank != 0:
@@ -347,6 +380,12 @@ def run_gpu(args):
                "sample": (f"the first {done} of the step's {n} pairs ({args.w}x{args.h} 8-bit "
                           f"4:2:0): motion SAD + Y/U/V SSE, single-threaded C oracle, "
                           f"{secs:.1f} s")}
+        cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+        if cores > 1 and args.cpu_seconds > 0:
+            prate, pdone, psecs = cpu_oracle_parallel_rate(batch, args.cpu_seconds / 2, cores)
+            cpu["parallel"] = {"value": prate, "unit": "frames/s", "cores": cores,
+                               "sample": (f"{pdone} pairs of the step's {n} (cycled) over {cores} "
+                                          f"threads of the same oracle, {psecs:.1f} s")}
     line = {
         "metric": METRIC, "value": value, "unit": "frames/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
