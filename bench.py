@@ -526,6 +526,24 @@ def run_sequence_workload(args):
             launches = (iif.motion_kernel_launch_count() - l0) / args.steps
         alg = w * h * s * n
         ops = (MOTION_OPS_PER_PIXEL + (1 if args.v2 else 0)) * w * h * n
+        e2e = None
+        if not args.v2 and not args.graph and not args.generic:
+            # end to end: the same sequence from pinned host memory through
+            # motion_submit_batch_host, chunks of the batch size (uploads
+            # overlap the kernels), SADs back to the host
+            host = torch.from_numpy(frames.view(np.int16) if bpc > 8 else frames).pin_memory().numpy()
+            ctx.reset()
+            ctx.submit_batch_host(host, frames_per_chunk=batch)
+            t0 = time.perf_counter()
+            e2e_steps = max(1, min(args.steps, 5))
+            for _ in range(e2e_steps):
+                ctx.reset()
+                h_sad = ctx.submit_batch_host(host, frames_per_chunk=batch)
+            e2e_s = time.perf_counter() - t0
+            assert np.array_equal(h_sad, sad.cpu().numpy().astype(np.uint64)), \
+                "device-resident and host-buffer paths disagree"
+            e2e = {"value": n * e2e_steps / e2e_s, "unit": "frames/s",
+                   "h2d_bytes_per_step": int(host.nbytes), "d2h_bytes_per_step": 8 * n}
         lines.append({"metric": "frames/s (batched motion%s SAD)" % ("_v2" if args.v2 else ""),
                       "value": n / (ms * 1e-3),
                       "unit": "frames/s", "n_gpus": 1, "steps": args.steps,
@@ -537,7 +555,7 @@ def run_sequence_workload(args):
                                  "frames_per_step": n, "batch": batch,
                                  "launches_per_step": launches, "cuda_graph": bool(args.graph),
                                  "kernel_path": "generic" if args.generic else "auto"},
-                      "roofline": seq_roofline(alg, ops, ms, peak, peak_kind)})
+                      "roofline": seq_roofline(alg, ops, ms, peak, peak_kind), "e2e": e2e})
         ctx.close()
     for ln in lines:
         print(json.dumps(ln), flush=True)

@@ -173,6 +173,23 @@ MOTION_API int motion_psnr_yuv420_batch_host(motion_ctx* ctx, int n,
                                   size_t stride_y, size_t stride_uv,
                                   uint64_t* h_sad_out, uint64_t* h_sse_out);
 
+/* motion_submit_batch with HOST frames and HOST results: n frames
+ * (frame_stride bytes apart, rows pitch bytes apart, as motion_submit_batch)
+ * are copied host->device in chunks of frames_per_chunk frames (0 picks about
+ * 256 MB of frames, 1 to 256) into the context's staging sets on one stream
+ * while the motion kernel of the previous chunk runs on another ("Making it
+ * fast" -- the upload is the wall-time bottleneck; the same pipeline as
+ * motion_psnr_yuv420_batch_host, whose staging sets it shares and grows when
+ * needed).  The frames continue the context's sequence (SAD_0 against the last
+ * frame of the previous call, device or host).  Blocks until h_sad_out
+ * (uint64[n]) is written; pinned host frames give full copy speed.  Errors as
+ * motion_submit_batch, plus MOTION_ERR_BAD_PITCH if consecutive host frames
+ * overlap; after a CUDA error the sequence may have advanced by the chunks
+ * that ran. */
+MOTION_API int motion_submit_batch_host(motion_ctx* ctx, const void* h_frames, int n,
+                                        size_t frame_stride_bytes, size_t pitch_bytes,
+                                        int frames_per_chunk, uint64_t* h_sad_out);
+
 /* Allocate the two device staging sets, result buffers and streams used by
  * motion_psnr_yuv420_batch_host, for chunks of `pairs_per_chunk` pairs whose
  * planes are stride_y / stride_uv bytes apart (0 picks about 256 MB of

@@ -28,7 +28,7 @@ __all__ = [
     "motion_set_kernel_path", "motion_device_error", "MOTION_PATH_AUTO", "MOTION_PATH_GENERIC",
     "motion_submit_batch_noalloc", "motion_set_stall_injection", "moment_sums_batch",
     "moments_from_sums", "motion_v2_submit_batch", "motion_plan_chunks", "motion_tile_order",
-    "motion_inject_alloc_failure",
+    "motion_inject_alloc_failure", "motion_submit_batch_host",
 ]
 
 EXPORTED_SYMBOLS = (
@@ -39,6 +39,7 @@ EXPORTED_SYMBOLS = (
     "motion_set_kernel_path", "motion_device_error", "motion_submit_batch_noalloc",
     "motion_set_stall_injection", "moment_sums_batch", "moments_from_sums",
     "motion_v2_submit_batch", "motion_plan_chunks", "motion_tile_order", "motion_inject_alloc_failure",
+    "motion_submit_batch_host",
 )
 
 _LIB: ctypes.CDLL | None = None
@@ -84,6 +85,7 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
         "motion_plan_chunks": ([I, I, I, I, ctypes.POINTER(I)], I),
         "motion_tile_order": ([I, I, I, ctypes.c_longlong, ctypes.POINTER(I)], I),
         "motion_inject_alloc_failure": ([I], I),
+        "motion_submit_batch_host": ([P, P, I, Z, Z, I, P], I),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -247,6 +249,25 @@ def motion_submit_batch(ctx: int, frames, sad_out, n: int | None = None,
     _check(load_library().motion_submit_batch(ctx, _addr(frames), n, frame_stride, pitch_bytes,
                                               _stream(stream), _addr(sad_out)),
            "motion_submit_batch")
+
+
+def motion_submit_batch_host(ctx: int, frames, sad_out: np.ndarray | None = None,
+                             n: int | None = None, frame_stride: int | None = None,
+                             pitch_bytes: int | None = None, frames_per_chunk: int = 0) -> np.ndarray:
+    """Host frames in, host SADs out (uint64[n]); uploads overlap the kernels."""
+    if n is None:
+        n = int(frames.shape[0])
+    if pitch_bytes is None or frame_stride is None:
+        p, s = _layout(frames)
+        pitch_bytes = p if pitch_bytes is None else pitch_bytes
+        frame_stride = s if frame_stride is None else frame_stride
+    if sad_out is None:
+        sad_out = np.zeros(n, np.uint64)
+    _need_out(sad_out, n, "sad_out")
+    _check(load_library().motion_submit_batch_host(ctx, _host_addr(frames), n, frame_stride, pitch_bytes,
+                                                   frames_per_chunk, _host_addr(sad_out)),
+           "motion_submit_batch_host")
+    return sad_out
 
 
 def motion_v2_submit_batch(ctx: int, frames, sad_out, n: int | None = None,
@@ -525,6 +546,11 @@ class MotionContext:
     def submit_batch(self, frames, sad_out, stream=None) -> None:
         self._frames_fit(frames, int(frames.shape[0]))
         motion_submit_batch(self.handle, frames, sad_out, stream=stream)
+
+    def submit_batch_host(self, frames, sad_out=None, frames_per_chunk: int = 0) -> np.ndarray:
+        """motion_submit_batch_host: host frames (numpy or a CPU tensor), host SADs."""
+        self._frames_fit(frames, int(frames.shape[0]))
+        return motion_submit_batch_host(self.handle, frames, sad_out, frames_per_chunk=frames_per_chunk)
 
     def submit_batch_v2(self, frames, sad_out, stream=None) -> None:
         self._frames_fit(frames, int(frames.shape[0]))

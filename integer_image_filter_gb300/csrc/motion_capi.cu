@@ -105,6 +105,7 @@ struct motion_ctx {
     // host-buffer pipeline
     int stage_pairs = 0;
     size_t stage_stride_y = 0, stage_stride_uv = 0;
+    size_t stage_set_bytes = 0, stage_res_n = 0;   // bytes of each staging set, results per set
     uint8_t* d_stage[2] = {nullptr, nullptr};
     unsigned long long* d_res[2] = {nullptr, nullptr};
     cudaStream_t s_copy = nullptr, s_comp = nullptr;
@@ -150,9 +151,42 @@ void free_staging(motion_ctx* c) {
     if (c->s_comp) cudaStreamDestroy(c->s_comp);
     c->s_copy = c->s_comp = nullptr;
     c->stage_pairs = 0;
+    c->stage_set_bytes = c->stage_res_n = 0;
     if (c->h_res) cudaFreeHost(c->h_res);
     c->h_res = nullptr;
     c->h_res_pairs = 0;
+}
+
+// The two staging sets of the host-buffer calls: at least set_bytes each and
+// res_n uint64 results each (grown, never shrunk), their events and streams.
+int reserve_stage(motion_ctx* c, size_t set_bytes, size_t res_n) {
+    if (c->d_stage[0] && c->stage_set_bytes >= set_bytes && c->stage_res_n >= res_n) return MOTION_OK;
+    if (set_bytes < c->stage_set_bytes) set_bytes = c->stage_set_bytes;
+    if (res_n < c->stage_res_n) res_n = c->stage_res_n;
+    free_staging(c);
+    for (int k = 0; k < 2; ++k) {
+        MG_CUDA(dev_alloc(reinterpret_cast<void**>(&c->d_stage[k]), set_bytes));
+        MG_CUDA(dev_alloc(reinterpret_cast<void**>(&c->d_res[k]), sizeof(unsigned long long) * res_n));
+        MG_CUDA(cudaEventCreateWithFlags(&c->ev_in[k], cudaEventDisableTiming));
+        MG_CUDA(cudaEventCreateWithFlags(&c->ev_done[k], cudaEventDisableTiming));
+    }
+    MG_CUDA(cudaStreamCreateWithFlags(&c->s_copy, cudaStreamNonBlocking));
+    MG_CUDA(cudaStreamCreateWithFlags(&c->s_comp, cudaStreamNonBlocking));
+    c->stage_set_bytes = set_bytes;
+    c->stage_res_n = res_n;
+    return MOTION_OK;
+}
+
+// The pinned result buffer of the host-buffer calls: at least n uint64.
+int reserve_host_results(motion_ctx* c, size_t n) {
+    if (c->h_res_pairs * 4 >= n) return MOTION_OK;
+    if (c->h_res) cudaFreeHost(c->h_res);
+    c->h_res = nullptr;
+    c->h_res_pairs = 0;
+    const size_t pairs = (n + 3) / 4;
+    MG_CUDA(host_alloc(reinterpret_cast<void**>(&c->h_res), sizeof(unsigned long long) * 4 * pairs));
+    c->h_res_pairs = pairs;
+    return MOTION_OK;
 }
 
 // Planes whose base, pitch or frame stride the TMA cannot take are copied
@@ -475,18 +509,11 @@ int motion_reserve_host_staging(motion_ctx* c, int pairs_per_chunk, size_t strid
         if (pairs_per_chunk > 64) pairs_per_chunk = 64;
     }
     if (c->stage_pairs >= pairs_per_chunk && c->stage_stride_y >= stride_y &&
-        c->stage_stride_uv >= stride_uv)
+        c->stage_stride_uv >= stride_uv && c->d_stage[0])
         return MOTION_OK;
-    free_staging(c);
-    const size_t bytes = 2 * (size_t)pairs_per_chunk * (stride_y + 2 * stride_uv);
-    for (int k = 0; k < 2; ++k) {
-        MG_CUDA(dev_alloc(reinterpret_cast<void**>(&c->d_stage[k]), bytes));
-        MG_CUDA(dev_alloc(reinterpret_cast<void**>(&c->d_res[k]), sizeof(unsigned long long) * 4 * (size_t)pairs_per_chunk));
-        MG_CUDA(cudaEventCreateWithFlags(&c->ev_in[k], cudaEventDisableTiming));
-        MG_CUDA(cudaEventCreateWithFlags(&c->ev_done[k], cudaEventDisableTiming));
-    }
-    MG_CUDA(cudaStreamCreateWithFlags(&c->s_copy, cudaStreamNonBlocking));
-    MG_CUDA(cudaStreamCreateWithFlags(&c->s_comp, cudaStreamNonBlocking));
+    rc = reserve_stage(c, 2 * (size_t)pairs_per_chunk * (stride_y + 2 * stride_uv),
+                       4 * (size_t)pairs_per_chunk);
+    if (rc) return rc;
     c->stage_pairs = pairs_per_chunk;
     c->stage_stride_y = stride_y;
     c->stage_stride_uv = stride_uv;
@@ -509,13 +536,7 @@ int motion_psnr_yuv420_batch_host(motion_ctx* c, int n, const void* ry, const vo
         stride_uv < pitch_uv * (size_t)(c->ch - 1) + (size_t)c->cw * s)
         return MOTION_ERR_BAD_PITCH;  // host pairs must not overlap
     if ((rc = motion_reserve_host_staging(c, c->stage_pairs, stride_y, stride_uv))) return rc;
-    if (c->h_res_pairs < (size_t)n) {
-        if (c->h_res) cudaFreeHost(c->h_res);
-        c->h_res = nullptr;
-        c->h_res_pairs = 0;
-        MG_CUDA(host_alloc(reinterpret_cast<void**>(&c->h_res), sizeof(unsigned long long) * 4 * (size_t)n));
-        c->h_res_pairs = (size_t)n;
-    }
+    if ((rc = reserve_host_results(c, 4 * (size_t)n))) return rc;
     unsigned long long* h_sad = c->h_res;
     unsigned long long* h_sse = c->h_res + n;
     const int P = c->stage_pairs;
@@ -560,6 +581,57 @@ int motion_psnr_yuv420_batch_host(motion_ctx* c, int n, const void* ry, const vo
     MG_CUDA(cudaStreamSynchronize(c->s_comp));
     std::memcpy(h_sad_out, h_sad, sizeof(uint64_t) * (size_t)n);
     std::memcpy(h_sse_out, h_sse, sizeof(uint64_t) * 3 * (size_t)n);
+    return MOTION_OK;
+}
+
+int motion_submit_batch_host(motion_ctx* c, const void* h_frames, int n, size_t frame_stride,
+                             size_t pitch, int frames_per_chunk, uint64_t* h_sad_out) {
+    if (!c || n < 0 || frames_per_chunk < 0) return MOTION_ERR_INVALID_ARGUMENT;
+    if (n == 0) return MOTION_OK;
+    if (!h_sad_out) return MOTION_ERR_INVALID_ARGUMENT;
+    int rc = check_layout(h_frames, pitch, frame_stride, n, c->w, c->bpc);
+    if (rc) return rc;
+    if ((rc = ctx_device_ok(c))) return rc;
+    const size_t last = pitch * (size_t)(c->h - 1) + (size_t)c->w * (size_t)sample_bytes(c->bpc);
+    if (n > 1 && frame_stride < last) return MOTION_ERR_BAD_PITCH;   // host frames must not overlap
+    const size_t slot = n > 1 ? frame_stride : last;
+    int F = frames_per_chunk;
+    if (F == 0) {
+        // about 256 MB of frames per chunk (copies of that size run at the host
+        // link's rate), 1 to 256 frames
+        const size_t f = ((size_t)256 << 20) / slot;
+        F = f < 1 ? 1 : (f > 256 ? 256 : (int)f);
+    }
+    if (F > n) F = n;
+    if ((rc = reserve_stage(c, (size_t)(F - 1) * slot + last, (size_t)F))) return rc;
+    if ((rc = reserve_host_results(c, (size_t)n))) return rc;
+    unsigned long long* h_sad = c->h_res;
+    const int nchunks = (n + F - 1) / F;
+    for (int ci = 0; ci < nchunks; ++ci) {
+        const int k = ci & 1;
+        const int first = ci * F;
+        const int m = (n - first) < F ? (n - first) : F;
+        // the staging set k is free once the kernel of chunk ci-2 has finished
+        MG_CUDA(cudaStreamWaitEvent(c->s_copy, c->ev_done[k], 0));
+        MG_CUDA(cudaMemcpyAsync(c->d_stage[k], (const uint8_t*)h_frames + (size_t)first * slot,
+                                (size_t)(m - 1) * slot + last, cudaMemcpyHostToDevice, c->s_copy));
+        MG_CUDA(cudaEventRecord(c->ev_in[k], c->s_copy));
+        MG_CUDA(cudaStreamWaitEvent(c->s_comp, c->ev_in[k], 0));
+        unsigned long long* d_sad = c->d_res[k];
+        MG_CUDA(cudaMemsetAsync(d_sad, 0, sizeof(uint64_t) * (size_t)m, c->s_comp));
+        mg::TileArgs a = motion_args(c, m);
+        a.ref_y = c->d_stage[k];
+        a.pitch_y = (long long)pitch;
+        a.stride_y = (long long)slot;
+        a.aligned16 = aligned16(c->d_stage[k], pitch, slot, m);
+        a.sad_out = d_sad;
+        if ((rc = launch_motion(c, a, false, c->s_comp))) return rc;
+        MG_CUDA(cudaMemcpyAsync(h_sad + first, d_sad, sizeof(uint64_t) * (size_t)m,
+                                cudaMemcpyDeviceToHost, c->s_comp));
+        MG_CUDA(cudaEventRecord(c->ev_done[k], c->s_comp));
+    }
+    MG_CUDA(cudaStreamSynchronize(c->s_comp));
+    std::memcpy(h_sad_out, h_sad, sizeof(uint64_t) * (size_t)n);
     return MOTION_OK;
 }
 
