@@ -352,7 +352,7 @@ def run_gpu(args):
     for _ in range(1):
         ctx.reset()
         ctx.yuv420_batch_host(*pinned)
-    e2e_steps = max(1, min(args.steps, 5))
+    e2e_steps = max(1, min(args.steps, 10))
     if ws > 1:
         dist.barrier()
     t0 = time.perf_counter()
@@ -535,7 +535,7 @@ def run_sequence_workload(args):
             ctx.reset()
             ctx.submit_batch_host(host, frames_per_chunk=batch)
             t0 = time.perf_counter()
-            e2e_steps = max(1, min(args.steps, 5))
+            e2e_steps = max(1, min(args.steps, 10))
             for _ in range(e2e_steps):
                 ctx.reset()
                 h_sad = ctx.submit_batch_host(host, frames_per_chunk=batch)
