@@ -256,12 +256,18 @@ MOTION_API int psnr_from_sse(uint64_t sse, uint64_t n_samples, int bpc, double* 
  * always uses the TMA kernel -- planes whose base, pitch or frame stride is
  * not a multiple of 16 bytes are first copied, in one more launch, into a
  * scratch the context owns with 16-byte-aligned rows (allocated by the first
- * such call, n frames' or pairs' worth, grown when a call needs more, freed
- * by motion_destroy); MOTION_PATH_GENERIC always uses the generic kernel,
+ * such call, n frames' or pairs' worth up to motion_set_copy_limit, grown
+ * when a call needs more, freed by motion_destroy); MOTION_PATH_GENERIC always uses the generic kernel,
  * which reads any layout in place.  Results are identical on both paths. */
 #define MOTION_PATH_AUTO 0
 #define MOTION_PATH_GENERIC 1
 MOTION_API int motion_set_kernel_path(motion_ctx* ctx, int path);
+
+/* The most scratch the copy of MOTION_PATH_AUTO may use for one launch, in
+ * bytes (0, the default: 1 GiB).  A call whose planes need the copy and do
+ * not fit runs as several launches of as many frames (or pairs) as fit, each
+ * continuing the sequence; results are the same. */
+MOTION_API int motion_set_copy_limit(motion_ctx* ctx, size_t bytes);
 
 /* Diagnostic, host only, no GPU: the number of frame chunks (1..8) a batched
  * launch of n frames of w x h splits into on a device where `resident_ctas`

@@ -28,7 +28,7 @@ __all__ = [
     "motion_set_kernel_path", "motion_device_error", "MOTION_PATH_AUTO", "MOTION_PATH_GENERIC",
     "motion_submit_batch_noalloc", "motion_set_stall_injection", "moment_sums_batch",
     "moments_from_sums", "motion_v2_submit_batch", "motion_plan_chunks", "motion_tile_order",
-    "motion_inject_alloc_failure", "motion_submit_batch_host",
+    "motion_inject_alloc_failure", "motion_submit_batch_host", "motion_set_copy_limit",
 ]
 
 EXPORTED_SYMBOLS = (
@@ -39,7 +39,7 @@ EXPORTED_SYMBOLS = (
     "motion_set_kernel_path", "motion_device_error", "motion_submit_batch_noalloc",
     "motion_set_stall_injection", "moment_sums_batch", "moments_from_sums",
     "motion_v2_submit_batch", "motion_plan_chunks", "motion_tile_order", "motion_inject_alloc_failure",
-    "motion_submit_batch_host",
+    "motion_submit_batch_host", "motion_set_copy_limit",
 )
 
 _LIB: ctypes.CDLL | None = None
@@ -86,6 +86,7 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
         "motion_tile_order": ([I, I, I, ctypes.c_longlong, ctypes.POINTER(I)], I),
         "motion_inject_alloc_failure": ([I], I),
         "motion_submit_batch_host": ([P, P, I, Z, Z, I, P], I),
+        "motion_set_copy_limit": ([P, Z], I),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -472,6 +473,10 @@ def motion_inject_alloc_failure(nth: int) -> None:
     _check(load_library().motion_inject_alloc_failure(nth), "motion_inject_alloc_failure")
 
 
+def motion_set_copy_limit(ctx: int, nbytes: int) -> None:
+    _check(load_library().motion_set_copy_limit(ctx, nbytes), "motion_set_copy_limit")
+
+
 def motion_set_stall_injection(ctx: int, on: bool) -> None:
     _check(load_library().motion_set_stall_injection(ctx, 1 if on else 0),
            "motion_set_stall_injection")
@@ -517,6 +522,9 @@ class MotionContext:
 
     def reset(self) -> None:
         motion_reset(self.handle)
+
+    def set_copy_limit(self, nbytes: int) -> None:
+        motion_set_copy_limit(self.handle, nbytes)
 
     def set_kernel_path(self, path: int) -> None:
         motion_set_kernel_path(self.handle, path)

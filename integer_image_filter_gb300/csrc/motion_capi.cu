@@ -126,6 +126,7 @@ struct motion_ctx {
     // when a call needs more)
     uint8_t* d_rp = nullptr;
     size_t rp_bytes = 0;
+    size_t rp_limit = 0;            // most bytes of one copy (0: 1 GiB); longer calls go in parts
 };
 
 namespace {
@@ -248,7 +249,53 @@ int repitch_for_tma(motion_ctx* c, mg::TileArgs& a, bool fused, cudaStream_t s) 
 
 // The TMA kernel (after repitch_for_tma, for any layout), or the generic
 // kernel when motion_set_kernel_path asks for it.
+// Frames (or pairs) of one launch whose planes the copy kernel re-pitches:
+// as many as fit the context's copy limit, at least one; all of them when the
+// planes need no copy.
+int frames_per_copy(const motion_ctx* c, const mg::TileArgs& a, bool fused) {
+    if (c->force_generic || a.n <= 1 || mg::tma_usable(a, fused)) return a.n;
+    const long long S = sample_bytes(c->bpc);
+    const long long py = ((long long)c->w * S + 15) & ~15LL, puv = ((long long)c->cw * S + 15) & ~15LL;
+    const size_t per = (size_t)(fused ? 2 * py * c->h + 4 * puv * c->ch : py * c->h);
+    const size_t limit = c->rp_limit ? c->rp_limit : ((size_t)1 << 30);
+    const size_t m = limit / per;
+    return m < 1 ? 1 : (m >= (size_t)a.n ? a.n : (int)m);
+}
+
+// The planes of frames [f0, f0 + m) of a launch.
+mg::TileArgs frames_slice(const mg::TileArgs& a, int f0, int m) {
+    mg::TileArgs b = a;
+    b.n = m;
+    b.ref_y = a.ref_y + (long long)f0 * a.stride_y;
+    if (a.dist_y) b.dist_y = a.dist_y + (long long)f0 * a.stride_y;
+    if (a.ref_u) b.ref_u = a.ref_u + (long long)f0 * a.stride_uv;
+    if (a.dist_u) b.dist_u = a.dist_u + (long long)f0 * a.stride_uv;
+    if (a.ref_v) b.ref_v = a.ref_v + (long long)f0 * a.stride_uv;
+    if (a.dist_v) b.dist_v = a.dist_v + (long long)f0 * a.stride_uv;
+    if (a.sad_out) b.sad_out = a.sad_out + f0;
+    if (a.sse_out) b.sse_out = a.sse_out + 3LL * f0;
+    return b;
+}
+
+int launch_motion_one(motion_ctx* c, mg::TileArgs a, bool fused, cudaStream_t s);
+
+// A launch, in parts when its planes need the copy kernel and do not fit the
+// copy limit (each part continues the sequence of the one before).
 int launch_motion(motion_ctx* c, mg::TileArgs a, bool fused, cudaStream_t s) {
+    const int m = frames_per_copy(c, a, fused);
+    if (m >= a.n) return launch_motion_one(c, a, fused, s);
+    for (int f0 = 0; f0 < a.n; f0 += m) {
+        mg::TileArgs b = frames_slice(a, f0, (a.n - f0) < m ? (a.n - f0) : m);
+        b.has_prev = c->has_prev;
+        b.bprev = c->d_bprev[c->cur];
+        b.bprev_out = c->d_bprev[c->cur ^ 1];
+        const int rc = launch_motion_one(c, b, fused, s);
+        if (rc) return rc;
+    }
+    return MOTION_OK;
+}
+
+int launch_motion_one(motion_ctx* c, mg::TileArgs a, bool fused, cudaStream_t s) {
     int rc = repitch_for_tma(c, a, fused, s);
     if (rc) return rc;
     int launched = 0;
@@ -444,21 +491,25 @@ int motion_v2_submit_batch(motion_ctx* c, const void* d_frames, int n, size_t fr
     a.stride_y = (long long)frame_stride;
     a.aligned16 = aligned16(d_frames, pitch, frame_stride, n);
     a.sad_out = (unsigned long long*)d_sad_out;
-    a.has_prev = c->v2_has_prev;
     a.bprev = a.bprev_out = nullptr;
-    a.raw_prev = c->d_raw[c->raw_cur];
-    a.raw_out = c->d_raw[c->raw_cur ^ 1];
     a.raw_pitch = (long long)c->raw_pitch;
-    if ((rc = repitch_for_tma(c, a, false, s))) return rc;
-    int launched = 0;
-    bool used = false;
-    cudaError_t e = cudaSuccess;
-    if (!c->force_generic) e = mg::launch_motion_v2_tma(a, s, &launched, &used);
-    if (e == cudaSuccess && !used) e = mg::launch_motion_v2_tile(a, s, &launched);
-    g_launches += (uint64_t)launched;
-    if (e != cudaSuccess) return cuda_fail(e);
-    c->v2_has_prev = 1;
-    c->raw_cur ^= 1;   // the plane just written holds the last frame
+    const int m = frames_per_copy(c, a, false);
+    for (int f0 = 0; f0 < n; f0 += m) {
+        mg::TileArgs b = frames_slice(a, f0, (n - f0) < m ? (n - f0) : m);
+        b.has_prev = c->v2_has_prev;
+        b.raw_prev = c->d_raw[c->raw_cur];
+        b.raw_out = c->d_raw[c->raw_cur ^ 1];
+        if ((rc = repitch_for_tma(c, b, false, s))) return rc;
+        int launched = 0;
+        bool used = false;
+        cudaError_t e = cudaSuccess;
+        if (!c->force_generic) e = mg::launch_motion_v2_tma(b, s, &launched, &used);
+        if (e == cudaSuccess && !used) e = mg::launch_motion_v2_tile(b, s, &launched);
+        g_launches += (uint64_t)launched;
+        if (e != cudaSuccess) return cuda_fail(e);
+        c->v2_has_prev = 1;
+        c->raw_cur ^= 1;   // the plane just written holds the last frame
+    }
     return MOTION_OK;
 }
 
@@ -809,6 +860,12 @@ int motion_tile_order(int w, int h, int chunks, long long block, int* tile_out) 
     const int gx = (w + mg::kTileW - 1) / mg::kTileW, gy = (h + mg::kTileH - 1) / mg::kTileH;
     if (block < 0 || block >= (long long)gx * gy * chunks) return MOTION_ERR_INVALID_ARGUMENT;
     mg::tile_of_block(w, h, gx, gy, chunks, (int)block, &tile_out[0], &tile_out[1], &tile_out[2]);
+    return MOTION_OK;
+}
+
+int motion_set_copy_limit(motion_ctx* c, size_t bytes) {
+    if (!c) return MOTION_ERR_INVALID_ARGUMENT;
+    c->rp_limit = bytes;
     return MOTION_OK;
 }
 

@@ -109,3 +109,50 @@ def test_unaligned_fused_pairs(iif, oracle, w, h, bpc):
         assert ctx.device_error() == 0
     assert sad.cpu().numpy().astype(np.uint64).tolist() == [int(x) for x in oracle.motion_sad_sequence(b.ref_y, bpc)]
     assert np.array_equal(sse.cpu().numpy().astype(np.uint64), oracle_sse420(oracle, b))
+
+
+@pytest.mark.parametrize("kind", ["motion", "motion_v2", "fused"])
+def test_copy_limit_splits_a_call_into_parts(iif, oracle, kind):
+    """A copy limit of about 3 frames' (pairs') scratch turns a 10-frame call on
+    unaligned planes into 4 parts (4 copies and 4 motion launches), each
+    continuing the sequence; the results are the oracle's."""
+    import torch
+    w, h, bpc, n = 213, 48, 8, 10
+    lib = iif.load_library()
+    if kind == "fused":
+        b = synth.uniform_yuv420(91, n, w, h, bpc)
+        keep, views = [], []
+        for p in b.planes():
+            buf, o, pitch = _layout(p, 0, 1)
+            keep.append(buf)
+            views.append((buf.data_ptr() + o, pitch, p.shape[1] * pitch))
+        py, puv = (w + 15) // 16 * 16, ((w + 1) // 2 + 15) // 16 * 16
+        per = 2 * py * h + 4 * puv * ((h + 1) // 2)
+        sad = torch.zeros(n, dtype=torch.int64, device="cuda")
+        sse = torch.zeros((n, 3), dtype=torch.int64, device="cuda")
+        with iif.MotionContext(w, h, bpc) as ctx:
+            ctx.set_copy_limit(3 * per)
+            l0 = iif.motion_kernel_launch_count()
+            rc = lib.motion_psnr_yuv420_batch(ctx.handle, n, views[0][0], views[1][0], views[2][0],
+                                              views[3][0], views[4][0], views[5][0], views[0][1],
+                                              views[1][1], views[0][2], views[1][2], None,
+                                              sad.data_ptr(), sse.data_ptr())
+            assert rc == 0, iif.motion_strerror(rc)
+            torch.cuda.synchronize()
+            assert iif.motion_kernel_launch_count() - l0 == 8
+            assert ctx.device_error() == 0
+        assert sad.cpu().numpy().astype(np.uint64).tolist() == [int(x) for x in oracle.motion_sad_sequence(b.ref_y, bpc)]
+        assert np.array_equal(sse.cpu().numpy().astype(np.uint64), oracle_sse420(oracle, b))
+        return
+    fr = synth.uniform_frames(92, n, w, h, bpc)
+    want = (oracle.motion_v2_sequence if kind == "motion_v2" else oracle.motion_sad_sequence)(fr, bpc)
+    buf, offset, pitch = _layout(fr, 0, 0)
+    out = torch.zeros(n, dtype=torch.int64, device="cuda")
+    with iif.MotionContext(w, h, bpc) as ctx:
+        ctx.set_copy_limit(3 * ((w + 15) // 16 * 16) * h)
+        l0 = iif.motion_kernel_launch_count()
+        _submit(iif, ctx, kind, buf, offset, pitch, n, h, out)
+        torch.cuda.synchronize()
+        assert iif.motion_kernel_launch_count() - l0 == 8
+        assert ctx.device_error() == 0
+    assert out.cpu().numpy().astype(np.uint64).tolist() == [int(x) for x in want]
