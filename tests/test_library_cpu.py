@@ -135,6 +135,10 @@ def test_binding_refuses_short_buffers(lib):
     with pytest.raises(ValueError, match=short):
         iif.motion_psnr_yuv420_batch_host(0, y.numpy(), c.numpy(), c.numpy(), y.numpy(),
                                           c.numpy(), c.numpy(), np.zeros(2, np.uint64))
+    with pytest.raises(ValueError, match=short):             # host frames: 2 of 3 SADs
+        iif.motion_submit_batch_host(0, y.numpy(), np.zeros(2, np.uint64))
+    with pytest.raises(TypeError, match="64-bit"):
+        iif.motion_submit_batch_host(0, y.numpy(), np.zeros(3, np.uint32))
 
 
 def test_frame_chunk_plan(lib):
