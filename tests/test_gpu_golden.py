@@ -25,7 +25,6 @@ def iif():
 
 def _padded(a):
     """The same frames with 16-byte row pitch (the TMA path takes them)."""
-    import torch
     n, h, w = a.shape
     wp = (w * a.itemsize + 15) // 16 * 16 // a.itemsize
     big = np.zeros((n, h, wp), a.dtype)
