@@ -257,8 +257,9 @@ MOTION_API int psnr_from_sse(uint64_t sse, uint64_t n_samples, int bpc, double* 
  * not a multiple of 16 bytes are first copied, in one more launch, into a
  * scratch the context owns with 16-byte-aligned rows (allocated by the first
  * such call, n frames' or pairs' worth up to motion_set_copy_limit, grown
- * when a call needs more, freed by motion_destroy); MOTION_PATH_GENERIC always uses the generic kernel,
- * which reads any layout in place.  Results are identical on both paths. */
+ * when a call needs more, freed by motion_destroy); MOTION_PATH_GENERIC
+ * always uses the generic kernel, which reads any layout in place.  Results
+ * are identical on both paths. */
 #define MOTION_PATH_AUTO 0
 #define MOTION_PATH_GENERIC 1
 MOTION_API int motion_set_kernel_path(motion_ctx* ctx, int path);
