@@ -43,7 +43,10 @@
  *   - Frames must be at least 3 x 3 (the mirror rule needs n >= 3) and at most
  *     MOTION_MAX_DIM on each side.
  *   - Calls on one context must not overlap (one stream per context, or
- *     ordered by the caller); distinct contexts are independent.
+ *     ordered by the caller); distinct contexts are independent and may be
+ *     driven from different host threads at the same time (the library's
+ *     one-time set-up -- driver entry point, launch attributes, occupancy --
+ *     is safe under that race).  motion_inject_alloc_failure is process-wide.
  *   - CUDA graphs: the device-result calls (motion_submit_batch,
  *     motion_v2_submit_batch, motion_psnr_yuv420_batch, psnr_sse,
  *     psnr_sse_yuv420_batch, moment_sums_batch) enqueue only stream work (an
@@ -294,7 +297,7 @@ MOTION_API int motion_plan_chunks(int w, int h, int n, int resident_ctas, int* c
  * tile_out). */
 MOTION_API int motion_tile_order(int w, int h, int chunks, long long block, int* tile_out);
 
-/* Test hook for allocation failures (no counterpart in the paper): the nth
+/* Test hook for allocation failures (not part of the method): the nth
  * device or pinned-host allocation the library makes from now on (1 = the
  * next one) fails with MOTION_ERR_OUT_OF_MEMORY without reaching the driver;
  * 0 turns it off.  Library-wide.  Every entry point that allocates (init,
@@ -304,7 +307,7 @@ MOTION_API int motion_tile_order(int w, int h, int chunks, long long block, int*
  * MOTION_ERR_INVALID_ARGUMENT for nth < 0. */
 MOTION_API int motion_inject_alloc_failure(int nth);
 
-/* Test hook for the kernels' bounded waits (no counterpart in the paper):
+/* Test hook for the kernels' bounded waits (not part of the method):
  * while on, TMA launches on this context expect 16 bytes per stage more than
  * their boxes deliver, so no stage wait can complete, and bound every wait at
  * about 2 ms; the kernels then set bit 0 of the device error word and leave.
@@ -320,7 +323,7 @@ MOTION_API int motion_device_error(motion_ctx* ctx, int* flags);
  * samples times h must not exceed this (3840x2160 and 4096x2048 fit). */
 #define MOTION_NOALLOC_MAX_SAMPLES (8u * 1024u * 1024u)
 
-/* Batched motion SAD that allocates nothing (no counterpart in the paper: it
+/* Batched motion SAD that allocates nothing (not part of the method: it
  * exists for callers that may not allocate device memory -- a host program
  * that owns all device memory through its own pool and forbids libraries to
  * call cudaMalloc, or a latency-critical loop where an allocation, which can

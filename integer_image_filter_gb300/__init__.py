@@ -13,6 +13,7 @@ from __future__ import annotations
 
 import ctypes
 import os
+import threading
 from dataclasses import dataclass
 
 import numpy as np
@@ -43,6 +44,7 @@ EXPORTED_SYMBOLS = (
 )
 
 _LIB: ctypes.CDLL | None = None
+_LIB_LOCK = threading.Lock()
 
 
 class MotionError(RuntimeError):
@@ -98,14 +100,15 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
 def load_library(path: str | None = None) -> ctypes.CDLL:
     """Load libmotion_gb300.so (built in-tree by ``__graft_entry__.build()``)."""
     global _LIB
-    if _LIB is None:
-        p = path or _build.lib_path()
-        if not os.path.exists(p):
-            raise RuntimeError(
-                f"{p} is missing: build the CUDA library first (python -c 'import "
-                "__graft_entry__ as g; g.build()'); there is no CPU fallback")
-        _LIB = _declare(ctypes.CDLL(p))
-    return _LIB
+    with _LIB_LOCK:   # threads that get here first together load it once
+        if _LIB is None:
+            p = path or _build.lib_path()
+            if not os.path.exists(p):
+                raise RuntimeError(
+                    f"{p} is missing: build the CUDA library first (python -c 'import "
+                    "__graft_entry__ as g; g.build()'); there is no CPU fallback")
+            _LIB = _declare(ctypes.CDLL(p))
+        return _LIB
 
 
 def _check(code: int, what: str) -> None:

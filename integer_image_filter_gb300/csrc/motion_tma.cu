@@ -681,18 +681,18 @@ int plan_frame_chunks(long long tiles, long long slots, int n, int max_c) {
 
 namespace {
 
+// The driver's tensor-map encoder, looked up once (a function-local static is
+// initialised exactly once even when several host threads get here together).
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static bool tried = false;
-    if (!tried) {
+    static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
         void* p = nullptr;
         cudaDriverEntryPointQueryResult q;
         if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
                                              &q) == cudaSuccess &&
             q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-        tried = true;
-    }
+            return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+        return static_cast<PFN_cuTensorMapEncodeTiled_v12000>(nullptr);
+    }();
     return fn;
 }
 
@@ -729,8 +729,10 @@ cudaError_t launch_tma_one(const TmaMaps& maps, const TileArgs& a, cudaStream_t 
         __atomic_fetch_or(&configured, bit, __ATOMIC_RELEASE);
     }
     // Size the launch by the SM count (ADR-1226): plan_frame_chunks.
+    // resident CTAs on the whole device, per device (threads racing here
+    // compute and store the same value)
     static int slots_per_sm[64] = {0};
-    int& spm = slots_per_sm[dev & 63];
+    int spm = __atomic_load_n(&slots_per_sm[dev & 63], __ATOMIC_RELAXED);
     if (spm == 0) {
         int per_sm = 0, sms = 0;
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, motion_tma_kernel<Pix, FUSED, STAGES, V2>,
@@ -739,6 +741,7 @@ cudaError_t launch_tma_one(const TmaMaps& maps, const TileArgs& a, cudaStream_t 
         e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return e;
         spm = (per_sm > 0 ? per_sm : 1) * sms;
+        __atomic_store_n(&slots_per_sm[dev & 63], spm, __ATOMIC_RELAXED);
     }
     TileArgs b = a;
     const long long tiles = (long long)((a.w + TW - 1) / TW) * ((a.h + TH - 1) / TH);
