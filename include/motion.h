@@ -39,7 +39,9 @@
  *     9 <= bpc <= 16.  Values >= 2^bpc violate a precondition and give
  *     unspecified (but memory-safe) results.  uint16 planes must be 2-byte
  *     aligned (pointer, pitch and frame stride).
- *   - pitch / stride arguments are in BYTES.
+ *   - pitch / stride arguments are in BYTES; a pitch above 2^40, a frame
+ *     stride above 2^46 or n frames spanning more than 2^48 bytes is
+ *     MOTION_ERR_INVALID_ARGUMENT.
  *   - Frames must be at least 3 x 3 (the mirror rule needs n >= 3) and at most
  *     MOTION_MAX_DIM on each side.
  *   - Calls on one context must not overlap (one stream per context, or
@@ -83,7 +85,7 @@ extern "C" {
 
 enum motion_status {
     MOTION_OK = 0,
-    MOTION_ERR_INVALID_ARGUMENT = 1,   /* NULL pointer, n < 0, bad plane index */
+    MOTION_ERR_INVALID_ARGUMENT = 1,   /* NULL pointer, n < 0, bad plane index, layout too large */
     MOTION_ERR_FRAME_TOO_SMALL = 2,     /* w < 3 or h < 3 */
     MOTION_ERR_UNSUPPORTED_BITDEPTH = 3,/* bpc outside [8, 16] */
     MOTION_ERR_BAD_PITCH = 4,           /* pitch < w * sample size, or misaligned uint16 layout */

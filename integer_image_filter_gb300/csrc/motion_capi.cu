@@ -70,6 +70,8 @@ int check_layout(const void* p, size_t pitch, size_t stride, int n, int w, int b
     if (s == 2 && (((uintptr_t)p & 1) || (pitch & 1) || (n > 1 && (stride & 1))))
         return MOTION_ERR_BAD_PITCH;
     if (pitch > (size_t)1 << 40 || stride > (size_t)1 << 46) return MOTION_ERR_INVALID_ARGUMENT;
+    // n frames stride apart must fit a 48-bit address space (no frame offset wraps)
+    if (n > 1 && stride > ((size_t)1 << 48) / (size_t)n) return MOTION_ERR_INVALID_ARGUMENT;
     return MOTION_OK;
 }
 

@@ -66,6 +66,35 @@ def test_host_argument_validation(lib):
     assert lib.motion_submit_batch(None, None, 0, 0, 0, None, None) == 1
 
 
+def test_layout_validation_before_any_device_call(lib):
+    """Context-free batch calls check every plane layout on the host and
+    return before touching the device: pitches shorter than a row, odd
+    16-bit layouts, and frame spans that leave a 48-bit address space.  Every
+    case here must fail validation: the pointers are not device memory."""
+    import ctypes
+    p = ctypes.c_void_p(4096)                     # never dereferenced: validation fails first
+    out = ctypes.cast(ctypes.c_void_p(4096), ctypes.POINTER(ctypes.c_uint64))
+    W, H = 64, 32
+
+    def yuv(n, py, puv, sy, suv, bpc=8):
+        return lib.psnr_sse_yuv420_batch(W, H, bpc, n, p, p, p, p, p, p, py, puv, sy, suv, None, out)
+
+    def moments(n, pitch, stride, bpc=8):
+        return lib.moment_sums_batch(W, H, bpc, n, p, p, pitch, stride, None, out)
+
+    assert yuv(2, W - 1, W // 2, W * H, W * H // 4) == 4          # luma pitch < row
+    assert yuv(2, W, W // 2 - 1, W * H, W * H // 4) == 4          # chroma pitch < row
+    assert yuv(2, 2 * W + 1, W, 2 * W * H, W * H // 2, bpc=10) == 4   # odd 16-bit pitch
+    assert yuv(2, W, W // 2, 1 << 47, W * H // 4) == 1            # stride beyond 2^46
+    assert yuv(1 << 10, W, W // 2, 1 << 40, W * H // 4) == 1      # 2^50 bytes of frames
+    assert moments(2, W - 1, W * H) == 4
+    assert moments(3, W, 1 << 47) == 1
+    assert moments(1 << 12, W, 1 << 37) == 1                     # 2^49 bytes
+    assert moments(1 << 20, W, (1 << 28) + 16) == 1               # just over 2^48
+    assert moments(2, W, W * H, bpc=17) == 3
+    assert moments(-1, W, W * H) == 1
+
+
 def test_init_without_device_reports_it(lib):
     import ctypes
     import torch
