@@ -1,7 +1,8 @@
 """Seeded fuzz cases for the C ABI (used by tests/test_gpu_fuzz.py).
 
 Case i draws, from one seeded generator, a kind (motion, motion_v2, fused
-4:2:0, stand-alone 4:2:0 SSE, single-plane SSE, moment sums), a frame size
+4:2:0, stand-alone 4:2:0 SSE, single-plane SSE, moment sums; after them the
+host-buffer pipelines and the single-frame call), a frame size
 from 3x3 up, a bit depth from 8 to 16, padded rows, a base offset, the cut
 points that split the frames over consecutive calls and the kernel path; it
 places uniform samples in that layout, calls the library through its raw
@@ -25,6 +26,10 @@ import synth
 KINDS = ("motion", "motion_v2", "yuv420", "sse420", "sse", "moments")
 CHECKED_KINDS = ("motion", "motion_v2", "yuv420")
 N_CASES = 120
+# host-buffer pipelines and the single-frame call, after the device cases
+HOST_KINDS = ("yuv420_host", "motion_host", "single")
+N_HOST_CASES = 36
+N_ALL = N_CASES + N_HOST_CASES
 
 
 def check(cond: bool, msg) -> None:
@@ -35,7 +40,7 @@ def check(cond: bool, msg) -> None:
 def draw(i: int) -> dict:
     """Case i: every choice from one seeded generator."""
     rng = np.random.default_rng(9000 + i)
-    kind = KINDS[i % len(KINDS)]
+    kind = KINDS[i % len(KINDS)] if i < N_CASES else HOST_KINDS[(i - N_CASES) % len(HOST_KINDS)]
     bpc = int(rng.choice([8, 8, 9, 10, 12, 14, 16]))
     s = 1 if bpc == 8 else 2
     w = int(rng.integers(3, 300))
@@ -47,8 +52,11 @@ def draw(i: int) -> dict:
     off = int(rng.integers(0, 24)) * s if rng.random() < 0.5 else 0     # bytes before the first sample
     cuts = sorted(set(int(c) for c in rng.integers(1, n, size=int(rng.integers(0, 3))))) if n > 1 else []
     generic = bool(rng.random() < 0.3)
-    return dict(kind=kind, bpc=bpc, s=s, w=w, h=h, n=n, pad=pad, off=off, cuts=cuts,
-                generic=generic, seed=int(rng.integers(0, 2**31 - 1)))
+    d = dict(kind=kind, bpc=bpc, s=s, w=w, h=h, n=n, pad=pad, off=off, cuts=cuts,
+             generic=generic, seed=int(rng.integers(0, 2**31 - 1)))
+    if i >= N_CASES:                              # drawn last: the device cases stay as they were
+        d["chunk"] = int(rng.integers(0, 4))      # frames (pairs) per host chunk, 0 = the default
+    return d
 
 
 def place(frames: np.ndarray, pad: int, off: int):
@@ -64,6 +72,17 @@ def place(frames: np.ndarray, pad: int, off: int):
     buf = torch.zeros(off + host.size + 64, dtype=torch.uint8, device="cuda")
     buf[off:off + host.size] = torch.from_numpy(host.reshape(-1)).to("cuda")
     return buf, buf.data_ptr() + off, pitch, h * pitch
+
+
+def place_host(frames: np.ndarray, pad: int, off: int):
+    """As place(), in a host (pageable) byte buffer."""
+    n, h, w = frames.shape
+    s = frames.itemsize
+    pitch = w * s + pad
+    buf = np.zeros(off + n * h * pitch + 64, np.uint8)
+    view = buf[off:off + n * h * pitch].reshape(n, h, pitch)
+    view[:, :, :w * s] = frames.view(np.uint8).reshape(n, h, w * s)
+    return buf, buf.ctypes.data + off, pitch, h * pitch
 
 
 def spans(n: int, cuts):
@@ -87,6 +106,9 @@ def run_case(iif, o, i: int) -> None:
     def ok(rc):
         check(rc == 0, (what, iif.motion_strerror(rc)))
 
+    if kind in HOST_KINDS:
+        run_host_case(iif, o, c, what)
+        return
     if kind in ("motion", "motion_v2"):
         fr = synth.uniform_frames(c["seed"], n, w, h, bpc)
         buf, addr, pitch, stride = place(fr, c["pad"], c["off"])
@@ -148,6 +170,80 @@ def run_case(iif, o, i: int) -> None:
         check(sad.cpu().numpy().astype(np.uint64).tolist() ==
               [int(x) for x in o.motion_sad_sequence(b.ref_y, bpc)], what)
     check(np.array_equal(sse.cpu().numpy().astype(np.uint64), sse420(o, b)), what)
+
+
+def run_host_case(iif, o, c: dict, what: str) -> None:
+    """Host-buffer pipelines (host pictures in, host results out, in chunks of
+    c["chunk"]) and the single-frame call mixed with batches on one sequence."""
+    import ctypes
+
+    import torch
+    kind, bpc, w, h, n = c["kind"], c["bpc"], c["w"], c["h"], c["n"]
+    lib = iif.load_library()
+
+    def ok(rc):
+        check(rc == 0, (what, iif.motion_strerror(rc)))
+
+    if kind == "motion_host":
+        fr = synth.uniform_frames(c["seed"], n, w, h, bpc)
+        buf, addr, pitch, stride = place_host(fr, c["pad"], c["off"])
+        out = np.zeros(n, np.uint64)
+        with iif.MotionContext(w, h, bpc) as ctx:
+            for a, b in spans(n, c["cuts"]):
+                ok(lib.motion_submit_batch_host(ctx.handle, addr + a * stride, b - a, stride, pitch,
+                                                c["chunk"], out.ctypes.data + 8 * a))
+            check(ctx.device_error() == 0, ("device error", what))
+        check(out.tolist() == [int(x) for x in o.motion_sad_sequence(fr, bpc)], what)
+        return
+    if kind == "single":
+        fr = synth.uniform_frames(c["seed"], n, w, h, bpc)
+        buf, addr, pitch, stride = place(fr, c["pad"], c["off"])
+        sad = np.zeros(n, np.uint64)
+        score = np.zeros(n, np.float64)
+        d_out = torch.zeros(n, dtype=torch.int64, device="cuda")
+        with iif.MotionContext(w, h, bpc) as ctx:
+            if c["generic"]:
+                ctx.set_kernel_path(iif.MOTION_PATH_GENERIC)
+            for j, (a, b) in enumerate(spans(n, c["cuts"])):
+                if j % 2 == 0:                    # frame by frame, with the 8-byte readback
+                    for k in range(a, b):
+                        v, sc = ctypes.c_uint64(), ctypes.c_double()
+                        ok(lib.motion_submit(ctx.handle, addr + k * stride, pitch, None,
+                                             ctypes.byref(v), ctypes.byref(sc)))
+                        sad[k], score[k] = v.value, sc.value
+                else:                             # then a batch continuing the sequence
+                    ok(lib.motion_submit_batch(ctx.handle, addr + a * stride, b - a, stride, pitch, None,
+                                               d_out.data_ptr() + 8 * a))
+                    torch.cuda.synchronize()
+                    sad[a:b] = d_out[a:b].cpu().numpy().astype(np.uint64)
+                    score[a:b] = (sad[a:b].astype(np.float64) / 256.0) / float(w * h)
+            check(ctx.device_error() == 0, ("device error", what))
+        want = o.motion_sad_sequence(fr, bpc)
+        check(sad.tolist() == [int(x) for x in want], what)
+        check(score.tolist() == o.scores(want, w, h)[0].tolist(), ("score", what))
+        return
+    b = synth.uniform_yuv420(c["seed"], n, w, h, bpc)
+    keep, views = [], []
+    for p in b.planes():
+        pad = c["pad"] if p.shape[2] == w else c["s"] * (c["pad"] // (2 * c["s"]))
+        buf, addr, pitch, stride = place_host(p, pad, c["off"])
+        keep.append(buf)
+        views.append((addr, pitch, stride))
+    (py, sy), (puv, suv) = views[0][1:], views[1][1:]
+    sad = np.zeros(n, np.uint64)
+    sse = np.zeros((n, 3), np.uint64)
+    with iif.MotionContext(w, h, bpc) as ctx:
+        if c["generic"]:
+            ctx.set_kernel_path(iif.MOTION_PATH_GENERIC)
+        if c["chunk"]:
+            ok(lib.motion_reserve_host_staging(ctx.handle, c["chunk"], sy, suv))
+        for a, e in spans(n, c["cuts"]):
+            ptrs = [v[0] + a * (sy if k in (0, 3) else suv) for k, v in enumerate(views)]
+            ok(lib.motion_psnr_yuv420_batch_host(ctx.handle, e - a, *ptrs, py, puv, sy, suv,
+                                                 sad.ctypes.data + 8 * a, sse.ctypes.data + 24 * a))
+        check(ctx.device_error() == 0, ("device error", what))
+    check(sad.tolist() == [int(x) for x in o.motion_sad_sequence(b.ref_y, bpc)], what)
+    check(np.array_equal(sse, sse420(o, b)), what)
 
 
 def main(mode: str) -> int:

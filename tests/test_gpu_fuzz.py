@@ -41,6 +41,6 @@ def test_fuzz_cases_on_the_bounds_checked_library(iif):
     assert res["n_failures"] == 0, res["failures"]
 
 
-@pytest.mark.parametrize("i", range(fc.N_CASES))
+@pytest.mark.parametrize("i", range(fc.N_ALL))
 def test_fuzz_case(iif, oracle, i):
     fc.run_case(iif, oracle, i)
