@@ -80,24 +80,27 @@ bool tma_usable(const TileArgs& a, bool fused);
 // The output tile of the motion kernels (the TMA kernel's TW x TH).
 constexpr int kTileW = 128, kTileH = 32;
 // The tile and frame chunk of block `lin` (x fastest, then y, then chunk) of a
-// TMA launch over gx x gy tiles and gz chunks: the tiles on the frame border
-// of every chunk first, then the interior tiles (those that read no mirrored
-// sample: x0 > 0, y0 > 0, x0 + TW + 2 <= w and y0 + TH + 2 <= h).  The two
-// kinds run different copies of the frame loop, and an SM that runs both at
-// once misses in its instruction cache; in this order only the first wave
-// mixes them, and the last wave is made of the faster interior tiles.  A
-// bijection of [0, gx gy gz).
+// TMA launch over gx x gy tiles and gz chunks.  Tiles whose staged rows reach
+// past the top or bottom frame edge (tile row 0 and the rows after niy), and
+// a partial last tile column, run the border copy of the frame loop; all other
+// tiles run the interior copy -- the left and right edge columns included,
+// whose halo lanes read the mirrored columns inside the frame instead.  The
+// border tiles of every chunk come first, then the interior tiles in row-major
+// order, so that horizontally and vertically adjacent tiles run at the same
+// time and share their halo columns and rows in L2; an SM that ran both
+// copies of the loop at once would miss in its instruction cache, and in this
+// order only the first wave mixes them.  A bijection of [0, gx gy gz).
 __host__ __device__ inline void tile_of_block(int w, int h, int gx, int gy, int gz, int lin,
                                               int* tx, int* ty, int* cz) {
-    const int nix = w >= kTileW + 2 ? (w - kTileW - 2) / kTileW : 0;   // interior columns 1..nix
     const int niy = h >= kTileH + 2 ? (h - kTileH - 2) / kTileH : 0;   // interior rows 1..niy
-    const int ni = nix * niy, nb = gx * gy - ni;
+    const int nfull = w / kTileW;                                       // full columns 0..nfull-1
+    const int ni = nfull * niy, nb = gx * gy - ni;
     if (lin >= nb * gz) {
         const int idx = lin - nb * gz;
         *cz = idx / ni;
         const int r = idx - *cz * ni;
-        *ty = 1 + r / nix;
-        *tx = 1 + r % nix;
+        *ty = 1 + r / nfull;
+        *tx = r % nfull;
         return;
     }
     *cz = lin / nb;
@@ -107,11 +110,10 @@ __host__ __device__ inline void tile_of_block(int w, int h, int gx, int gy, int 
         const int k = r / gx;
         *tx = r % gx;
         *ty = k == 0 ? 0 : niy + k;
-    } else {                           // rows 1..niy: column 0 and columns after nix
-        const int rr = r - nbr, per = gx - nix;
+    } else {                           // rows 1..niy: the partial last column
+        const int rr = r - nbr, per = gx - nfull;
         *ty = 1 + rr / per;
-        const int c = rr % per;
-        *tx = c == 0 ? 0 : nix + c;
+        *tx = nfull + rr % per;
     }
 }
 // Chunks of a TMA launch (host only): n frames over `tiles` tiles with

@@ -15,11 +15,15 @@
 //    read rows through a per-CTA table of mirrored rows (i<0 -> -i,
 //    i>=n -> 2n-i-2) and mirror the V columns of their own rows, so no tile
 //    takes a sample-by-sample path and no block barrier is left in the frame
-//    loop.
-//  * Blocks take the border tiles of every chunk first and the interior tiles
-//    after them (tile_of_block): the two kinds run different copies of the
-//    frame loop, and an SM that runs both at once misses in its instruction
-//    cache.
+//    loop.  Full tiles on the left or right edge need only mirrored halo
+//    columns: their halo lanes read the mirrored columns inside the frame, and
+//    they run the interior copy of the frame loop.
+//  * Blocks take the border tiles (top and bottom tile rows, a partial last
+//    column) of every chunk first and the interior tiles after them in
+//    row-major order (tile_of_block): the two kinds run different copies of
+//    the frame loop, and an SM that runs both at once misses in its
+//    instruction cache; adjacent interior tiles run together and share their
+//    halos in L2.
 //  * Separable blur: the vertical 5-tap pass once per sample (rounded >> bpc)
 //    into a shared V tile, then the horizontal 5-tap pass (rounded >> 16)
 //    ("ADR-1392: CUDA motion, PSNR and moment kernels add one atomic per
@@ -35,6 +39,7 @@
 //    the copies it issued before the block exits.
 #include <cuda.h>
 
+#include <algorithm>
 #include <cmath>
 #include <type_traits>
 
@@ -202,7 +207,8 @@ __global__ void __launch_bounds__(Shape::NTK, Shape::MINB)
     // each warp owns output rows RPW w .. RPW w + RPW-1 of the tile; its V rows are private
     uint32_t* sV = reinterpret_cast<uint32_t*>(smem + STAGES * STAGE) + warp * 4 * SVW;
     [[maybe_unused]] const Span vrows{sV, 4 * SVW * sizeof(uint32_t)};   // this warp's V rows
-    // border tiles of every chunk first, interior tiles after them (tile_of_block)
+    // border tiles of every chunk first, interior tiles after them in row-major
+    // order (tile_of_block)
     int tx, ty, cz;
     tile_of_block(a.w, a.h, gridDim.x, gridDim.y, gridDim.z,
                   blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z), &tx, &ty, &cz);
@@ -210,7 +216,8 @@ __global__ void __launch_bounds__(Shape::NTK, Shape::MINB)
     const bool full_tile = (x0 + TW <= a.w) && (y0 + TH <= a.h);
     const bool pl = x0 == 0, pt = y0 == 0;
     const bool pr = x0 + TW + 2 > a.w, pb = y0 + TH + 2 > a.h;
-    const bool edge = pl || pr || pt || pb;
+    // interior copy of the frame loop: no mirrored rows, no partial columns
+    const bool interior = full_tile && !pt && !pb;
     const uint32_t rnd = 1u << (a.bpc - 1);
     const int sh = a.bpc;
     const long long wait_cycles = a.wait_cycles > 0 ? a.wait_cycles : kWaitCycles;
@@ -316,7 +323,16 @@ __global__ void __launch_bounds__(Shape::NTK, Shape::MINB)
     const int off_vcol = (G::HX + 4 * lane) * G::S;   // this lane's columns in staged row 0
     const int halo_r = lane >> 2, halo_which = lane & 3;   // halo row 0..7, column
     const int halo_off = halo_which == 0 ? -2 : halo_which == 1 ? -1 : halo_which == 2 ? TW : TW + 1;
-    const int off_hcol = (G::HX + halo_off) * G::S;   // the halo lane's column in staged row 0
+    // an interior tile on the left or right frame edge reads a halo column
+    // outside the frame from its mirror inside it (x < 0 -> -x, x >= w ->
+    // 2w - 2 - x; here always within the staged box); border tiles mirror V
+    // after the vertical pass instead
+    int hsrc = halo_off;
+    if (interior) {
+        if (x0 + hsrc < 0) hsrc = -2 * x0 - hsrc;
+        else if (x0 + hsrc >= a.w) hsrc = 2 * (a.w - x0) - 2 - hsrc;
+    }
+    const int off_hcol = (G::HX + hsrc) * G::S;   // the halo lane's column in staged row 0
     // only warps whose rows reach above row 0 or below row h - 1 read rows
     // through rowsrc
     const bool wmirror = (pt && RPW * warp < 2) || (pb && RPW * warp + RPW + 3 >= a.h - y0 + 2);
@@ -373,9 +389,10 @@ __global__ void __launch_bounds__(Shape::NTK, Shape::MINB)
         }
     };
 
-    // The frame loop, compiled twice: for interior tiles (no mirrored reads,
-    // no masks) and for tiles on the frame border.  A runtime test per frame
-    // costs the interior tiles several percent.
+    // The frame loop, compiled twice: for interior tiles (no mirrored rows, no
+    // masks) and for tiles on the top or bottom border or with a partial
+    // column.  A runtime test per frame costs the interior tiles several
+    // percent.
     auto frames = [&](auto interior_tag) -> bool {
         constexpr bool INTERIOR = decltype(interior_tag)::value;
         for (int l = 0; l < cnt; ++l) {
@@ -601,7 +618,6 @@ __global__ void __launch_bounds__(Shape::NTK, Shape::MINB)
         }
         return true;
     };
-    const bool interior = full_tile && !edge;
     const bool alive = interior ? frames(std::true_type{}) : frames(std::false_type{});
     if (tid == 0) {
         // no copy may still be landing in this block's shared memory when it
@@ -648,16 +664,19 @@ __global__ void __launch_bounds__(Shape::NTK, Shape::MINB)
 // Frame chunks of a launch, sized by the SM count (ADR-1226): n frames over
 // `tiles` tiles run as c chunks of CTAs, `slots` CTAs resident at once.  A
 // chunk after the first pays one warm-up frame and every chunk its own
-// pipeline fill (about half a frame); a launch under one wave leaves SMs idle,
-// and the last, partial wave of a longer one costs a quarter of its idle
-// share (the SMs it leaves short of CTAs run the ones they hold faster: the
-// kernel is bound by instruction issue).  Chunks keep at least 5 frames;
-// c <= max_c.
-//   cost(c) = (n + (c - 1) + c / 2) / n / eff, waves = tiles c / slots,
-//   eff = min(1, waves) / (1 + (ceil(waves) / waves - 1) / 4).
-// Fitted to forced-chunk timings on GB300 with the border-first block order:
-// 1080p x 16 frames is fastest at 1-2 chunks, x 32 at 2; 4K x 16 at one,
-// x 32 at 1-2, x 50 4:2:0 pairs at 2.
+// pipeline fill (about half a frame).  A launch under one wave leaves SMs idle
+// but runs the CTAs it has faster (the kernel is bound by instruction issue),
+// so it pays a quarter of its idle share; a longer launch pays for the idle
+// slots of its last, partial wave in proportion p = min(1, 2.6 / waves^2):
+// fully at under ~1.6 waves, less and less as CTAs of many waves start at
+// staggered times.  Chunks keep at least 5 frames; c <= max_c.
+//   cost(c) = (n + (c - 1) + c / 2) / n / eff,  waves = tiles c / slots,
+//   eff = waves / (1 + (1 / waves - 1) / 4)                  (waves <= 1)
+//   eff = 1 / (1 + p (ceil(waves) / waves - 1))              (waves > 1)
+// Fitted to forced-chunk timings on GB300 with the block order of
+// tile_of_block: 1080p x 16 frames is fastest at one chunk (three is as fast,
+// two 2 % slower), x 32 at three (4 % over two); 4K x 16 and the 10-bit 4K x 32
+// at one, the 4K 4:2:0 x 50 pairs at two (2 % over one and three).
 int plan_frame_chunks(long long tiles, long long slots, int n, int max_c) {
     if (n <= 1 || tiles <= 0 || slots <= 0) return 1;
     int best_c = 1;
@@ -667,8 +686,13 @@ int plan_frame_chunks(long long tiles, long long slots, int n, int max_c) {
         if (c > 1 && len < 5) break;
         const int cz = (n + len - 1) / len;
         const double waves = (double)tiles * cz / (double)slots;
-        const double q = std::ceil(waves) / waves;
-        const double eff = (waves < 1.0 ? waves : 1.0) / (1.0 + 0.25 * (q - 1.0));
+        double eff;
+        if (waves <= 1.0) {
+            eff = waves / (1.0 + 0.25 * (1.0 / waves - 1.0));
+        } else {
+            const double p = std::min(1.0, 2.6 / (waves * waves));
+            eff = 1.0 / (1.0 + p * (std::ceil(waves) / waves - 1.0));
+        }
         const double work = (n + (cz - 1) + 0.5 * cz) / (double)n;
         const double cost = work / eff;
         if (cost < best - 1e-9) {

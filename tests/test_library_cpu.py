@@ -172,16 +172,16 @@ def test_binding_refuses_short_buffers(lib):
 
 def test_frame_chunk_plan(lib):
     """Launch sizing by SM count: the chunk counts that forced-chunk timings
-    on a GB300 (608 resident CTAs, border tiles first) found fastest, and the
-    invariants of the plan (1..8 chunks, at least 5 frames per chunk, one
-    chunk for one frame)."""
+    on a GB300 (608 resident CTAs, the block order of motion_tile_order) found
+    fastest, and the invariants of the plan (1..8 chunks, at least 5 frames per
+    chunk, one chunk for one frame)."""
     import integer_image_filter_gb300 as iif
     plan = iif.motion_plan_chunks
-    assert plan(3840, 2160, 50, 608) == 2      # fused 4K 4:2:0 pairs (+2 % over one)
-    assert plan(3840, 2160, 32, 608) in (1, 2)  # 10-bit 4K, batch 32: a tie
+    assert plan(3840, 2160, 50, 608) == 2      # fused 4K 4:2:0 pairs (+2 % over one and three)
+    assert plan(3840, 2160, 32, 608) == 1      # 10-bit 4K, batch 32 (+1 % over two, +4 % over three)
     assert plan(3840, 2160, 16, 608) == 1      # (+3.5 % over two)
-    assert plan(1920, 1080, 32, 608) == 2      # (+2 % over three, +7 % over one)
-    assert plan(1920, 1080, 16, 608) in (1, 2)  # a tie, +4 % over three
+    assert plan(1920, 1080, 32, 608) == 3      # (+4 % over two, +1.5 % over four, +6 % over one)
+    assert plan(1920, 1080, 16, 608) in (1, 3)  # a tie, +2 % over two
     assert plan(1920, 1080, 8, 608) == 1
     assert plan(576, 324, 48, 608) == 8        # 55 tiles: as many chunks as allowed
     for (w, h) in ((64, 48), (576, 324), (1920, 1080), (3840, 2160), (8192, 4320)):
@@ -199,8 +199,11 @@ def test_frame_chunk_plan(lib):
 
 
 def test_tile_order(lib):
-    """Block order of a batched launch: every (tile, chunk) exactly once, the
-    frame-border tiles first, the tiles that read no mirrored sample last."""
+    """Block order of a batched launch: every (tile, chunk) exactly once; the
+    tiles that run the border copy of the frame loop (top row, rows whose halo
+    passes the bottom edge, a partial last column) first; then the full tiles
+    whose staged rows all lie in the frame -- left and right edge columns
+    included -- in row-major order within each chunk."""
     import integer_image_filter_gb300 as iif
     order = iif.motion_tile_order
     for (w, h, chunks) in ((3840, 2160, 2), (1920, 1080, 3), (576, 324, 8), (64, 48, 1),
@@ -208,16 +211,19 @@ def test_tile_order(lib):
                            (32768, 40, 2), (40, 32768, 1), (8192, 4320, 1)):
         gx, gy = -(-w // 128), -(-h // 32)
         seen = set()
-        kinds = []
+        kinds, interior = [], []
         for b in range(gx * gy * chunks):
             tx, ty, cz = order(w, h, chunks, b)
             assert 0 <= tx < gx and 0 <= ty < gy and 0 <= cz < chunks
             seen.add((tx, ty, cz))
             x0, y0 = 128 * tx, 32 * ty
-            kinds.append(x0 > 0 and y0 > 0 and x0 + 130 <= w and y0 + 34 <= h)
+            kinds.append(x0 + 128 <= w and y0 > 0 and y0 + 34 <= h)
+            if kinds[-1]:
+                interior.append((cz, ty, tx))
         assert len(seen) == gx * gy * chunks, (w, h, chunks)
         n_border = len(kinds) - sum(kinds)
         assert not any(kinds[:n_border]) and all(kinds[n_border:]), (w, h, chunks)
+        assert interior == sorted(interior), (w, h, chunks)      # row-major per chunk
     for bad in ((0, 10, 1, 0), (10, 10, 0, 0), (10, 10, 9, 0), (10, 10, 1, 1), (10, 10, 1, -1),
                 (32769, 10, 1, 0)):
         with pytest.raises(iif.MotionError):
