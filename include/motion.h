@@ -280,7 +280,9 @@ MOTION_API int motion_set_copy_limit(motion_ctx* ctx, size_t bytes);
  * motion CTAs run at once (4 per SM on GB300: 608).  The launch sizing
  * follows "ADR-1226: Size the CUDA AIM CM launch by SM count, not by a fixed
  * rows-per-thread": chunks after the first re-blur one warm-up frame, and
- * the count balances that work against the idle part of the last wave.
+ * the count balances that work against the idle part of the last wave.  This
+ * is the plan of the motion and fused kernels; motion_v2 launches weigh a
+ * partial last wave less (1080p x 16 frames: two chunks).
  * *chunks_out (host int) receives the count.  Errors:
  * MOTION_ERR_INVALID_ARGUMENT (w, h < 1, n < 0, resident_ctas < 1, NULL
  * chunks_out).  A launch that continues a sequence in place (the

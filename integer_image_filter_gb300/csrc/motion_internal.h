@@ -117,8 +117,9 @@ __host__ __device__ inline void tile_of_block(int w, int h, int gx, int gy, int 
     }
 }
 // Chunks of a TMA launch (host only): n frames over `tiles` tiles with
-// `slots` CTAs resident on the device at once; 1 <= result <= max_c.
-int plan_frame_chunks(long long tiles, long long slots, int n, int max_c);
+// `slots` CTAs resident on the device at once; 1 <= result <= max_c; v2
+// selects the motion_v2 kernel's constants.
+int plan_frame_chunks(long long tiles, long long slots, int n, int max_c, bool v2 = false);
 cudaError_t launch_sse(const SseArgs& a, cudaStream_t s, int sm_count, int* launches);
 
 // Copies of planes into rows the TMA can address (repitch.cu): n frames of

@@ -664,20 +664,24 @@ __global__ void __launch_bounds__(Shape::NTK, Shape::MINB)
 // Frame chunks of a launch, sized by the SM count (ADR-1226): n frames over
 // `tiles` tiles run as c chunks of CTAs, `slots` CTAs resident at once.  A
 // chunk after the first pays one warm-up frame and every chunk its own
-// pipeline fill (about half a frame).  A launch under one wave leaves SMs idle
-// but runs the CTAs it has faster (the kernel is bound by instruction issue),
-// so it pays a quarter of its idle share; a longer launch pays for the idle
-// slots of its last, partial wave in proportion p = min(1, 2.6 / waves^2):
-// fully at under ~1.6 waves, less and less as CTAs of many waves start at
-// staggered times.  Chunks keep at least 5 frames; c <= max_c.
-//   cost(c) = (n + (c - 1) + c / 2) / n / eff,  waves = tiles c / slots,
-//   eff = waves / (1 + (1 / waves - 1) / 4)                  (waves <= 1)
-//   eff = 1 / (1 + p (ceil(waves) / waves - 1))              (waves > 1)
-// Fitted to forced-chunk timings on GB300 with the block order of
-// tile_of_block: 1080p x 16 frames is fastest at one chunk (three is as fast,
-// two 2 % slower), x 32 at three (4 % over two); 4K x 16 and the 10-bit 4K x 32
-// at one, the 4K 4:2:0 x 50 pairs at two (2 % over one and three).
-int plan_frame_chunks(long long tiles, long long slots, int n, int max_c) {
+// pipeline fill (about half a frame):
+//   cost(c) = (n + (c - 1) + c / 2) / n / eff,  waves = tiles c / slots.
+// A launch under one wave leaves SMs idle but runs the CTAs it holds faster,
+// so it pays a quarter of its idle share:
+//   eff = waves / (1 + (1 / waves - 1) / 4)                  (waves <= 1).
+// Past one wave the motion kernel (bound by instruction issue) pays for the
+// idle slots of its last, partial wave in proportion p = min(1, 2.6 /
+// waves^2) -- fully under ~1.6 waves, less and less as CTAs of many waves
+// start at staggered times -- while motion_v2 (its 64-bit horizontal pass has
+// long dependency chains) pays a quarter of them at any count:
+//   eff = 1 / (1 + p (ceil(waves) / waves - 1)),  p as above or 1/4 (v2).
+// Chunks keep at least 5 frames; c <= max_c.  Fitted to forced-chunk timings
+// on GB300 with the block order of tile_of_block.  Motion: 1080p x 16 frames
+// is fastest at one chunk (three as fast, two 2 % slower), x 32 at three (4 %
+// over two); 4K x 16 and the 10-bit 4K x 32 at one; the 4K 4:2:0 x 50 pairs at
+// two (2 % over one and three).  motion_v2: 1080p x 16 and x 32 at two (one is
+// 13 % and 19 % slower), 10-bit 4K x 32 at one or two.
+int plan_frame_chunks(long long tiles, long long slots, int n, int max_c, bool v2) {
     if (n <= 1 || tiles <= 0 || slots <= 0) return 1;
     int best_c = 1;
     double best = 1e30;
@@ -690,7 +694,7 @@ int plan_frame_chunks(long long tiles, long long slots, int n, int max_c) {
         if (waves <= 1.0) {
             eff = waves / (1.0 + 0.25 * (1.0 / waves - 1.0));
         } else {
-            const double p = std::min(1.0, 2.6 / (waves * waves));
+            const double p = v2 ? 0.25 : std::min(1.0, 2.6 / (waves * waves));
             eff = 1.0 / (1.0 + p * (std::ceil(waves) / waves - 1.0));
         }
         const double work = (n + (cz - 1) + 0.5 * cz) / (double)n;
@@ -772,7 +776,7 @@ cudaError_t launch_tma_one(const TmaMaps& maps, const TileArgs& a, cudaStream_t 
     // a launch that reads and writes the same resident plane keeps one chunk:
     // the last chunk's store must not overtake the first chunk's read
     const bool same_plane = !V2 && a.has_prev && a.bprev == a.bprev_out;
-    const int best_c = plan_frame_chunks(tiles, spm, a.n, same_plane ? 1 : 8);
+    const int best_c = plan_frame_chunks(tiles, spm, a.n, same_plane ? 1 : 8, V2);
     b.chunk = (a.n + best_c - 1) / best_c;
     dim3 grid((a.w + TW - 1) / TW, (a.h + TH - 1) / TH, (a.n + b.chunk - 1) / b.chunk);
     motion_tma_kernel<Pix, FUSED, STAGES, V2><<<grid, Shape::NTK, SMEM, s>>>(maps, b);
