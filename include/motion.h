@@ -292,10 +292,13 @@ MOTION_API int motion_plan_chunks(int w, int h, int n, int resident_ctas, int* c
 /* Diagnostic, host only, no GPU: the output tile and frame chunk that block
  * `block` of a batched TMA launch of w x h frames in `chunks` chunks works on
  * (blocks counted x fastest, then y, then chunk, over ceil(w/128) x
- * ceil(h/32) x chunks blocks).  The tiles on the frame border come first for
- * every chunk, then the interior tiles -- those that read no mirrored sample
- * of the "Gaussian blur with mirror boundaries" -- so that after the first
- * wave an SM runs one kind of frame loop at a time.  tile_out (host int[3]) receives
+ * ceil(h/32) x chunks blocks).  The tiles that read mirrored rows (the top
+ * tile row and the rows whose halo passes the bottom edge) or hold a partial
+ * last column come first for every chunk, then the other tiles in row-major
+ * order -- the full tiles of the left and right edges among them, which read
+ * their mirrored halo columns directly -- so that after the first wave an SM
+ * runs one kind of frame loop at a time and neighbouring tiles share their
+ * halos in L2.  tile_out (host int[3]) receives
  * {tile column, tile row, chunk}.  Errors: MOTION_ERR_INVALID_ARGUMENT (w, h
  * outside 1..32768, chunks outside 1..8, block outside the launch, NULL
  * tile_out). */
