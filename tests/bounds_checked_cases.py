@@ -17,7 +17,8 @@ import sys
 
 import numpy as np
 
-SIZES = [(3, 3), (5, 7), (17, 9), (67, 35), (129, 33), (130, 34), (200, 100), (257, 70)]
+SIZES = [(3, 3), (5, 7), (17, 9), (67, 35), (129, 33), (130, 34), (200, 100), (257, 70),
+         (256, 70), (129, 100)]   # full right-edge tiles with mirrored halo reads
 FUSED_SIZES = [(4, 4), (67, 35), (130, 70), (258, 66)]
 
 

@@ -28,5 +28,6 @@ def test_bounds_checked_kernels_match_the_oracle():
                        capture_output=True, text=True, timeout=1200)
     assert r.returncode == 0, r.stderr[-3000:]
     res = json.loads(r.stdout.strip().splitlines()[-1])
-    assert res["cases"] == 2 * (8 * 3 * 2 * 2 + 4 * 2 * 2), res["cases"]
+    from tests import bounds_checked_cases as bc
+    assert res["cases"] == 2 * (len(bc.SIZES) * 3 * 2 * 2 + len(bc.FUSED_SIZES) * 2 * 2), res["cases"]
     assert res["n_failures"] == 0, res["failures"]

@@ -105,7 +105,8 @@ def test_paths_and_layouts(iif, oracle, bpc):
 
 
 @pytest.mark.parametrize("bpc", [8, 10, 16])
-@pytest.mark.parametrize("wh", [(3, 3), (5, 7), (127, 33), (130, 36), (257, 131), (1283, 723)])
+@pytest.mark.parametrize("wh", [(3, 3), (5, 7), (127, 33), (130, 36), (257, 131), (1283, 723),
+                                (128, 100), (256, 70), (385, 98)])
 def test_tiny_and_ragged(iif, oracle, bpc, wh):
     w, h = wh
     rng = np.random.default_rng(w * 3 + h + bpc)

@@ -142,7 +142,10 @@ def test_u10_batch_sizes_agree(iif, oracle, batch):
 # --------------------------------------------------------------- shapes, layouts
 SIZES = [(w, h) for w in (3, 4, 5, 7, 9) for h in (3, 4, 6, 9)] + [
     (16, 16), (17, 33), (67, 35), (127, 31), (128, 32), (129, 33), (131, 70), (160, 36),
-    (255, 97), (300, 65), (513, 129)]
+    (255, 97), (300, 65), (513, 129),
+    # full tiles on the left and right edges with all rows inside the frame: their
+    # halo lanes read the mirrored columns (w - x0 = 128 and 129, one and several columns)
+    (128, 100), (129, 100), (256, 70), (385, 98)]
 
 
 @pytest.mark.parametrize("bpc", [8, 10, 16])
