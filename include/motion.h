@@ -30,6 +30,19 @@
  * Conventions for every entry point:
  *   - Return 0 (MOTION_OK) on success or a MOTION_ERR_* code; nothing is written
  *     to an output on error.  motion_strerror() names a code.
+ *   - Device errors: the motion kernels never spin without bound.  A stage
+ *     wait that runs out (about one second), or a failed check in the
+ *     bounds-checked build, sets a sticky device error word (one per context;
+ *     one per device for the allocation-free entry point) and the kernel
+ *     leaves, so its results are incomplete.  The calls that wait for their
+ *     results anyway (motion_submit, which reads the word in the same 16-byte
+ *     readback as the SAD, and the two host-buffer calls, which read it after
+ *     their final synchronisation) return MOTION_ERR_DEVICE and write no
+ *     output; the asynchronous calls cannot see it, and motion_device_error
+ *     (motion_noalloc_device_error) is their collect step.  Whenever the word
+ *     is found set it is cleared and the context's sequences restart (the next
+ *     frame has SAD 0), since the resident planes may be incomplete (the
+ *     per-frame result readback behind the stream, ADR-1380 Decision).
  *   - "d_" pointers are device memory (cudaMalloc / PyTorch CUDA tensors) owned
  *     by the caller; "h_" pointers are host memory owned by the caller (pinned
  *     memory gives full copy speed; pageable memory works).
@@ -93,7 +106,8 @@ enum motion_status {
     MOTION_ERR_CUDA = 6,                /* a CUDA runtime call failed (motion_last_cuda_error) */
     MOTION_ERR_OUT_OF_MEMORY = 7,       /* device or pinned allocation failed */
     MOTION_ERR_NO_DEVICE = 8,           /* no CUDA device visible */
-    MOTION_ERR_WRONG_DEVICE = 9         /* called with a device other than the context's */
+    MOTION_ERR_WRONG_DEVICE = 9,        /* called with a device other than the context's */
+    MOTION_ERR_DEVICE = 10              /* a kernel set the device error word: results incomplete */
 };
 
 typedef struct motion_ctx motion_ctx;  /* opaque, library-owned */
@@ -115,7 +129,10 @@ MOTION_API int motion_reset(motion_ctx* ctx);
  * blur + SAD on `stream`, waits for it, and returns the frame's SAD against
  * the previously submitted frame (0 for the first frame of a sequence) and its
  * score.  Either output pointer may be NULL.  Follows the submit / collect
- * pattern with one 8-byte readback per frame (ADR-1380, Decision). */
+ * pattern with one small readback per frame (ADR-1380, Decision): 16 bytes,
+ * the SAD and the context's device error word; if the word is set the call
+ * returns MOTION_ERR_DEVICE, writes neither output, clears the word and
+ * restarts the sequence. */
 MOTION_API int motion_submit(motion_ctx* ctx, const void* d_frame, size_t pitch_bytes,
                   void* stream, uint64_t* sad_out, double* score_out);
 
@@ -169,7 +186,10 @@ MOTION_API int motion_psnr_yuv420_batch(motion_ctx* ctx, int n,
  * context keeps (grown to n pairs when a call needs more; the caller's result
  * arrays may be pageable).  Blocks until h_sad_out (uint64[n]) and h_sse_out
  * (uint64[n][3]) are written.  Host planes are tightly packed with the given
- * pitches and strides.  Pinned host memory recommended for the pictures. */
+ * pitches and strides.  Pinned host memory recommended for the pictures.
+ * After the last chunk the context's device error word is read: if a kernel
+ * set it the call returns MOTION_ERR_DEVICE, writes no output, clears the
+ * word and restarts the sequence. */
 MOTION_API int motion_psnr_yuv420_batch_host(motion_ctx* ctx, int n,
                                   const void* h_ref_y, const void* h_ref_u,
                                   const void* h_ref_v, const void* h_dist_y,
@@ -190,7 +210,7 @@ MOTION_API int motion_psnr_yuv420_batch_host(motion_ctx* ctx, int n,
  * (uint64[n]) is written; pinned host frames give full copy speed.  Errors as
  * motion_submit_batch, plus MOTION_ERR_BAD_PITCH if consecutive host frames
  * overlap; after a CUDA error the sequence may have advanced by the chunks
- * that ran. */
+ * that ran.  MOTION_ERR_DEVICE as motion_psnr_yuv420_batch_host. */
 MOTION_API int motion_submit_batch_host(motion_ctx* ctx, const void* h_frames, int n,
                                         size_t frame_stride_bytes, size_t pitch_bytes,
                                         int frames_per_chunk, uint64_t* h_sad_out);
@@ -321,9 +341,13 @@ MOTION_API int motion_inject_alloc_failure(int nth);
  * Results of such launches are incomplete.  Turn it off to compute again. */
 MOTION_API int motion_set_stall_injection(motion_ctx* ctx, int on);
 
-/* Read and clear the context's device error word after waiting for the
- * device: bit 0 set means a kernel's bounded wait for a staged tile ran out
- * (its results are then incomplete).  *flags receives the word. */
+/* The collect step of the asynchronous calls: read and clear the context's
+ * device error word after waiting for the device.  Bit 0 set means a
+ * kernel's bounded wait for a staged tile ran out, bit 1 a failed check in
+ * the bounds-checked build; the results written since the previous read are
+ * then incomplete, and the context's sequences restart (the next frame has
+ * SAD 0).  *flags receives the word; the return is MOTION_OK when it could be
+ * read. */
 MOTION_API int motion_device_error(motion_ctx* ctx, int* flags);
 
 /* Largest frame of motion_submit_batch_noalloc: rows of round_up(w, 8)
@@ -347,11 +371,31 @@ MOTION_API int motion_device_error(motion_ctx* ctx, int* flags);
  * current, looks up the array's device address (no allocation); make that
  * first call before any stream capture.  All calls on a device share the one
  * array and keep the last call's contents: calls that overlap on the GPU race,
- * so order them on one stream. */
+ * so order them on one stream.  Host threads calling at once are serialised
+ * around the library's per-device bookkeeping, but their GPU work still
+ * races: order them.  Layouts are checked as for motion_submit_batch
+ * (pitch <= 2^40, frame stride <= 2^46, n frames within 2^48 bytes).  A
+ * bounded wait that runs out sets this device's error word, which only
+ * motion_noalloc_device_error reads. */
 MOTION_API int motion_submit_batch_noalloc(const void* d_frames, int n, int w, int h, int bpc,
                                            size_t frame_stride_bytes, size_t pitch_bytes,
                                            int continue_sequence, void* stream,
                                            uint64_t* d_sad_out);
+
+/* The collect step of motion_submit_batch_noalloc (not part of the method):
+ * waits for `stream`, then reads and clears the current device's error word
+ * of the allocation-free calls (bits as motion_device_error).  A set word
+ * means the SADs written since the previous read are incomplete and so may be
+ * the built-in plane: the next call with continue_sequence = 1 is refused
+ * (MOTION_ERR_INVALID_ARGUMENT) until one starts a sequence.  Allocates
+ * nothing.  *flags receives the word. */
+MOTION_API int motion_noalloc_device_error(void* stream, int* flags);
+
+/* Test hook for the allocation-free calls' bounded waits (not part of the
+ * method), process-wide: while on, their TMA launches expect 16 bytes per stage
+ * more than their boxes deliver and bound every wait at about 2 ms, so the
+ * kernels set bit 0 of the error word and leave. */
+MOTION_API int motion_noalloc_set_stall_injection(int on);
 
 /* Number of this library's kernels launched by the calls above since load. */
 MOTION_API uint64_t motion_kernel_launch_count(void);

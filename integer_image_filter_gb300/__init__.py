@@ -30,6 +30,7 @@ __all__ = [
     "motion_submit_batch_noalloc", "motion_set_stall_injection", "moment_sums_batch",
     "moments_from_sums", "motion_v2_submit_batch", "motion_plan_chunks", "motion_tile_order",
     "motion_inject_alloc_failure", "motion_submit_batch_host", "motion_set_copy_limit",
+    "motion_noalloc_device_error", "motion_noalloc_set_stall_injection", "MOTION_ERR_DEVICE",
 ]
 
 EXPORTED_SYMBOLS = (
@@ -40,8 +41,12 @@ EXPORTED_SYMBOLS = (
     "motion_set_kernel_path", "motion_device_error", "motion_submit_batch_noalloc",
     "motion_set_stall_injection", "moment_sums_batch", "moments_from_sums",
     "motion_v2_submit_batch", "motion_plan_chunks", "motion_tile_order", "motion_inject_alloc_failure",
-    "motion_submit_batch_host", "motion_set_copy_limit",
+    "motion_submit_batch_host", "motion_set_copy_limit", "motion_noalloc_device_error",
+    "motion_noalloc_set_stall_injection",
 )
+
+# Status of a call whose kernel set the device error word (include/motion.h).
+MOTION_ERR_DEVICE = 10
 
 _LIB: ctypes.CDLL | None = None
 _LIB_LOCK = threading.Lock()
@@ -89,6 +94,8 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
         "motion_inject_alloc_failure": ([I], I),
         "motion_submit_batch_host": ([P, P, I, Z, Z, I, P], I),
         "motion_set_copy_limit": ([P, Z], I),
+        "motion_noalloc_device_error": ([P, ctypes.POINTER(I)], I),
+        "motion_noalloc_set_stall_injection": ([I], I),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -461,6 +468,22 @@ def motion_submit_batch_noalloc(frames, sad_out, w: int | None = None, h: int | 
     _check(load_library().motion_submit_batch_noalloc(
         _addr(frames), n, w, h, bpc, frame_stride, pitch_bytes, 1 if continue_sequence else 0,
         _stream(stream), _addr(sad_out)), "motion_submit_batch_noalloc")
+
+
+def motion_noalloc_device_error(stream=None) -> int:
+    """The collect step of the allocation-free calls: waits for `stream`, reads
+    and clears this device's error word (a set word also makes the next
+    continuing call refuse until a sequence is started)."""
+    v = ctypes.c_int()
+    _check(load_library().motion_noalloc_device_error(_stream(stream), ctypes.byref(v)),
+           "motion_noalloc_device_error")
+    return int(v.value)
+
+
+def motion_noalloc_set_stall_injection(on: bool) -> None:
+    """Test hook: the allocation-free calls' stage waits can never complete."""
+    _check(load_library().motion_noalloc_set_stall_injection(1 if on else 0),
+           "motion_noalloc_set_stall_injection")
 
 
 MOTION_PATH_AUTO = 0

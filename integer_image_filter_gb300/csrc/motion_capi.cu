@@ -53,6 +53,25 @@ int cuda_fail(cudaError_t e) {
         if (e_ != cudaSuccess) return cuda_fail(e_); \
     } while (0)
 
+using mg::check_dims;
+using mg::check_layout;
+using mg::sample_bytes;
+
+bool aligned16(const void* p, size_t pitch, size_t stride, int n) {
+    return (((uintptr_t)p | pitch) % 16 == 0) && (n <= 1 || stride % 16 == 0);
+}
+
+int current_device(int* dev) {
+    cudaError_t e = cudaGetDevice(dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return MOTION_OK;
+}
+
+}  // namespace
+
+namespace mg {
+void note_launches(int n) { g_launches += (uint64_t)n; }
+
 int sample_bytes(int bpc) { return bpc == 8 ? 1 : 2; }
 
 int check_dims(int w, int h, int bpc) {
@@ -74,21 +93,6 @@ int check_layout(const void* p, size_t pitch, size_t stride, int n, int w, int b
     if (n > 1 && stride > ((size_t)1 << 48) / (size_t)n) return MOTION_ERR_INVALID_ARGUMENT;
     return MOTION_OK;
 }
-
-bool aligned16(const void* p, size_t pitch, size_t stride, int n) {
-    return (((uintptr_t)p | pitch) % 16 == 0) && (n <= 1 || stride % 16 == 0);
-}
-
-int current_device(int* dev) {
-    cudaError_t e = cudaGetDevice(dev);
-    if (e != cudaSuccess) return cuda_fail(e);
-    return MOTION_OK;
-}
-
-}  // namespace
-
-namespace mg {
-void note_launches(int n) { g_launches += (uint64_t)n; }
 }  // namespace mg
 
 struct motion_ctx {
@@ -99,11 +103,14 @@ struct motion_ctx {
     uint16_t* d_bprev[2] = {nullptr, nullptr};  // previous frame's blurred plane, ping-pong
     int cur = 0;                    // index of the plane that holds B_{i-1}
     int has_prev = 0;
-    int* d_err = nullptr;           // device error word (bounded waits that timed out)
+    // device error word (bit 0: a bounded wait ran out; bit 1: a failed check in
+    // the bounds-checked build): the low half of d_slot[1], so that one 16-byte
+    // copy reads a frame's SAD and the word together
+    int* d_err = nullptr;
     int force_generic = 0;          // diagnostics: always use the generic kernel
     int stall_injection = 0;        // test hook: stage waits that can never complete
-    unsigned long long* d_slot = nullptr;   // single-submit result
-    unsigned long long* h_slot = nullptr;   // pinned readback slot
+    unsigned long long* d_slot = nullptr;   // [0]: single-submit SAD, [1]: error word
+    unsigned long long* h_slot = nullptr;   // pinned readback of d_slot (16 bytes)
     // host-buffer pipeline
     int stage_pairs = 0;
     size_t stage_stride_y = 0, stage_stride_uv = 0;
@@ -372,6 +379,24 @@ int launch_fused(motion_ctx* c, int n, const void* ry, const void* ru, const voi
     return launch_motion(c, a, true, s);
 }
 
+// A kernel of this context set the device error word: clear it on `s`, start
+// the sequences afresh (the resident planes may be incomplete) and report it.
+int device_failed(motion_ctx* c, cudaStream_t s) {
+    MG_CUDA(cudaMemsetAsync(c->d_err, 0, sizeof(int), s));
+    MG_CUDA(cudaStreamSynchronize(s));
+    c->has_prev = 0;
+    c->v2_has_prev = 0;
+    return MOTION_ERR_DEVICE;
+}
+
+// Queue the read of the error word into h_slot[1] on `s` (the host-buffer
+// calls check it after their final synchronisation).
+int queue_error_read(motion_ctx* c, cudaStream_t s) {
+    c->h_slot[1] = 0;
+    MG_CUDA(cudaMemcpyAsync(&c->h_slot[1], c->d_err, sizeof(int), cudaMemcpyDeviceToHost, s));
+    return MOTION_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -401,10 +426,10 @@ int motion_init(int w, int h, int bpc, motion_ctx** out) {
         e = dev_alloc(reinterpret_cast<void**>(&c->d_bprev[0]), sizeof(uint16_t) * (size_t)c->bprev_pitch * (size_t)h);
     if (e == cudaSuccess)
         e = dev_alloc(reinterpret_cast<void**>(&c->d_bprev[1]), sizeof(uint16_t) * (size_t)c->bprev_pitch * (size_t)h);
-    if (e == cudaSuccess) e = dev_alloc(reinterpret_cast<void**>(&c->d_slot), sizeof(unsigned long long));
-    if (e == cudaSuccess) e = dev_alloc(reinterpret_cast<void**>(&c->d_err), sizeof(int));
-    if (e == cudaSuccess) e = cudaMemset(c->d_err, 0, sizeof(int));
-    if (e == cudaSuccess) e = host_alloc(reinterpret_cast<void**>(&c->h_slot), sizeof(unsigned long long));
+    if (e == cudaSuccess) e = dev_alloc(reinterpret_cast<void**>(&c->d_slot), 2 * sizeof(unsigned long long));
+    if (e == cudaSuccess) e = cudaMemset(c->d_slot, 0, 2 * sizeof(unsigned long long));
+    if (e == cudaSuccess) c->d_err = reinterpret_cast<int*>(c->d_slot + 1);
+    if (e == cudaSuccess) e = host_alloc(reinterpret_cast<void**>(&c->h_slot), 2 * sizeof(unsigned long long));
     if (e != cudaSuccess) {
         motion_destroy(c);
         return cuda_fail(e);
@@ -424,8 +449,7 @@ int motion_destroy(motion_ctx* c) {
     if (c->d_raw[0]) cudaFree(c->d_raw[0]);
     if (c->d_raw[1]) cudaFree(c->d_raw[1]);
     if (c->d_rp) cudaFree(c->d_rp);
-    if (c->d_slot) cudaFree(c->d_slot);
-    if (c->d_err) cudaFree(c->d_err);
+    if (c->d_slot) cudaFree(c->d_slot);   // holds the error word too
     if (c->h_slot) cudaFreeHost(c->h_slot);
     if (prev >= 0) cudaSetDevice(prev);
     delete c;
@@ -521,10 +545,12 @@ int motion_submit(motion_ctx* c, const void* d_frame, size_t pitch, void* stream
     cudaStream_t s = (cudaStream_t)stream;
     int rc = motion_submit_batch(c, d_frame, 1, 0, pitch, stream, (uint64_t*)c->d_slot);
     if (rc) return rc;
-    MG_CUDA(cudaMemcpyAsync(c->h_slot, c->d_slot, sizeof(unsigned long long),
+    // one readback: the SAD and, beside it, the device error word
+    MG_CUDA(cudaMemcpyAsync(c->h_slot, c->d_slot, 2 * sizeof(unsigned long long),
                             cudaMemcpyDeviceToHost, s));
     MG_CUDA(cudaStreamSynchronize(s));
-    const uint64_t sad = (uint64_t)*c->h_slot;
+    if ((int)(uint32_t)c->h_slot[1] != 0) return device_failed(c, s);
+    const uint64_t sad = (uint64_t)c->h_slot[0];
     if (sad_out) *sad_out = sad;
     if (score_out) *score_out = ((double)sad / 256.0) / ((double)c->w * (double)c->h);
     return MOTION_OK;
@@ -631,7 +657,9 @@ int motion_psnr_yuv420_batch_host(motion_ctx* c, int n, const void* ry, const vo
                                 cudaMemcpyDeviceToHost, c->s_comp));
         MG_CUDA(cudaEventRecord(c->ev_done[k], c->s_comp));
     }
+    if ((rc = queue_error_read(c, c->s_comp))) return rc;
     MG_CUDA(cudaStreamSynchronize(c->s_comp));
+    if ((int)(uint32_t)c->h_slot[1] != 0) return device_failed(c, c->s_comp);
     std::memcpy(h_sad_out, h_sad, sizeof(uint64_t) * (size_t)n);
     std::memcpy(h_sse_out, h_sse, sizeof(uint64_t) * 3 * (size_t)n);
     return MOTION_OK;
@@ -683,7 +711,9 @@ int motion_submit_batch_host(motion_ctx* c, const void* h_frames, int n, size_t 
                                 cudaMemcpyDeviceToHost, c->s_comp));
         MG_CUDA(cudaEventRecord(c->ev_done[k], c->s_comp));
     }
+    if ((rc = queue_error_read(c, c->s_comp))) return rc;
     MG_CUDA(cudaStreamSynchronize(c->s_comp));
+    if ((int)(uint32_t)c->h_slot[1] != 0) return device_failed(c, c->s_comp);
     std::memcpy(h_sad_out, h_sad, sizeof(uint64_t) * (size_t)n);
     return MOTION_OK;
 }
@@ -891,6 +921,11 @@ int motion_device_error(motion_ctx* c, int* flags) {
     int v = 0;
     MG_CUDA(cudaMemcpy(&v, c->d_err, sizeof(int), cudaMemcpyDeviceToHost));
     MG_CUDA(cudaMemset(c->d_err, 0, sizeof(int)));
+    if (v) {
+        // the resident planes may be incomplete: the next call starts a sequence
+        c->has_prev = 0;
+        c->v2_has_prev = 0;
+    }
     *flags = v;
     return MOTION_OK;
 }
@@ -911,6 +946,9 @@ const char* motion_strerror(int code) {
         case MOTION_ERR_OUT_OF_MEMORY: return "out of memory";
         case MOTION_ERR_NO_DEVICE: return "no CUDA device";
         case MOTION_ERR_WRONG_DEVICE: return "current device is not the context's device";
+        case MOTION_ERR_DEVICE:
+            return "a kernel reported a device error (a bounded wait ran out or a bounds check "
+                   "failed); results incomplete, sequence restarted";
         default: return "unknown status";
     }
 }

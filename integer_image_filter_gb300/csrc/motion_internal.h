@@ -155,4 +155,15 @@ cudaError_t launch_moment(const MomentArgs& a, cudaStream_t s, int sm_count, int
 // Adds to the library-wide kernel launch count (motion_kernel_launch_count).
 void note_launches(int n);
 
+// Host-side argument checks shared by the entry points (motion_capi.cu); each
+// returns MOTION_OK or a MOTION_ERR_* code of include/motion.h.
+// Bytes per sample: 1 at 8 bits, 2 above.
+int sample_bytes(int bpc);
+// bpc in [8, 16], 3 <= w, h <= MOTION_MAX_DIM.
+int check_dims(int w, int h, int bpc);
+// n planes of w samples per row, rows `pitch` bytes apart, planes `stride`
+// bytes apart: a non-null base, pitch >= w samples, 2-byte alignment for
+// uint16 samples, pitch <= 2^40, stride <= 2^46, n strides within 2^48.
+int check_layout(const void* p, size_t pitch, size_t stride, int n, int w, int bpc);
+
 }  // namespace mg

@@ -13,8 +13,16 @@
 // device address (it names a host-side stand-in), so the entry point asks the
 // runtime for the device address once per device, on its first call on that
 // device with the device current, and keeps it.
+//
+// The kernels report a bounded wait that ran out (or, in the bounds-checked
+// build, a failed check) in a device error word beside the array; the call
+// that enqueues them cannot see it without waiting, so
+// motion_noalloc_device_error reads and clears it, and a set word makes the
+// next call start a new sequence instead of continuing from an incomplete
+// plane.
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 
 #include "motion.h"
 #include "motion_internal.h"
@@ -36,7 +44,15 @@ struct DeviceSlot {
     bool valid = false;
 };
 DeviceSlot g_slots[kMaxDevices];
+// Guards every slot's host-side fields: host threads calling at once on one
+// device are serialised here (their launches still race on the GPU array
+// unless the caller orders them).
+std::mutex g_slots_mu;
+// test hook (motion_noalloc_set_stall_injection): stage waits that can never
+// complete, bounded at about 2 ms
+bool g_stall_injection = false;
 
+// With g_slots_mu held.
 int setup_device(int dev, DeviceSlot** out) {
     if (dev < 0 || dev >= kMaxDevices) return MOTION_ERR_INVALID_ARGUMENT;
     DeviceSlot& s = g_slots[dev];
@@ -62,26 +78,22 @@ extern "C" int motion_submit_batch_noalloc(const void* d_frames, int n, int w, i
                                            int continue_sequence, void* stream,
                                            uint64_t* d_sad_out) {
     if (n < 0) return MOTION_ERR_INVALID_ARGUMENT;
-    if (bpc < 8 || bpc > 16) return MOTION_ERR_UNSUPPORTED_BITDEPTH;
-    if (w < 3 || h < 3) return MOTION_ERR_FRAME_TOO_SMALL;
-    if (w > MOTION_MAX_DIM || h > MOTION_MAX_DIM) return MOTION_ERR_TOO_LARGE;
+    int rc = mg::check_dims(w, h, bpc);
+    if (rc) return rc;
     const size_t bprev_pitch = ((size_t)w + 7) & ~(size_t)7;
     if (bprev_pitch * (size_t)h > kNoallocSamples) return MOTION_ERR_TOO_LARGE;
     if (n == 0) return MOTION_OK;
-    if (!d_frames || !d_sad_out) return MOTION_ERR_INVALID_ARGUMENT;
-    const size_t s = bpc == 8 ? 1 : 2;
-    if (pitch < (size_t)w * s) return MOTION_ERR_BAD_PITCH;
-    if (s == 2 && ((((uintptr_t)d_frames) & 1) || (pitch & 1) || (n > 1 && (frame_stride & 1))))
-        return MOTION_ERR_BAD_PITCH;
+    if (!d_sad_out) return MOTION_ERR_INVALID_ARGUMENT;
+    if ((rc = mg::check_layout(d_frames, pitch, frame_stride, n, w, bpc))) return rc;
 
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) {
         cudaGetLastError();
         return MOTION_ERR_CUDA;
     }
+    std::lock_guard<std::mutex> lock(g_slots_mu);
     DeviceSlot* slot = nullptr;
-    int rc = setup_device(dev, &slot);
-    if (rc) return rc;
+    if ((rc = setup_device(dev, &slot))) return rc;
     // continuing needs the array to hold the last frame of a sequence of the
     // same size and depth
     if (continue_sequence && !(slot->valid && slot->w == w && slot->h == h && slot->bpc == bpc))
@@ -111,6 +123,10 @@ extern "C" int motion_submit_batch_noalloc(const void* d_frames, int n, int w, i
     a.bprev_pitch = (int)bprev_pitch;
     a.sad_out = (unsigned long long*)d_sad_out;
     a.err = slot->err;
+    if (g_stall_injection) {
+        a.tx_extra = 16;               // the stage expects 16 bytes that never arrive
+        a.wait_cycles = 1LL << 22;     // and gives up after about 2 ms
+    }
     int launched = 0;
     bool used = false;
     cudaError_t e = mg::launch_motion_tma(a, false, st, &launched, &used);
@@ -121,5 +137,36 @@ extern "C" int motion_submit_batch_noalloc(const void* d_frames, int n, int w, i
     slot->h = h;
     slot->bpc = bpc;
     slot->valid = true;
+    return MOTION_OK;
+}
+
+extern "C" int motion_noalloc_device_error(void* stream, int* flags) {
+    if (!flags) return MOTION_ERR_INVALID_ARGUMENT;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return MOTION_ERR_CUDA;
+    }
+    std::lock_guard<std::mutex> lock(g_slots_mu);
+    DeviceSlot* slot = nullptr;
+    int rc = setup_device(dev, &slot);
+    if (rc) return rc;
+    cudaStream_t st = (cudaStream_t)stream;
+    int v = 0;
+    // the word is read after the stream's earlier work, then cleared on it
+    if (cudaMemcpyAsync(&v, slot->err, sizeof(int), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+        cudaMemsetAsync(slot->err, 0, sizeof(int), st) != cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess) {
+        cudaGetLastError();
+        return MOTION_ERR_CUDA;
+    }
+    if (v) slot->valid = false;   // the array's plane may be incomplete
+    *flags = v;
+    return MOTION_OK;
+}
+
+extern "C" int motion_noalloc_set_stall_injection(int on) {
+    std::lock_guard<std::mutex> lock(g_slots_mu);
+    g_stall_injection = on != 0;
     return MOTION_OK;
 }

@@ -8,7 +8,9 @@ context's device error word.  Each case below runs both kernel paths (TMA and
 generic) on frames of odd, ragged and tile-straddling sizes, contiguous and
 with padded rows, at 8, 10 and 16 bits, over two calls (the second continues
 the sequence), and records a failure when a result differs from the oracle or
-the error word is not 0.  Prints one JSON line: {"cases": N, "failures": [...]}.
+the error word is not 0.  The allocation-free entry point runs the same way
+(start, then continue) with its own error word read after each case.  Prints
+one JSON line: {"cases": N, "failures": [...]}.
 """
 from __future__ import annotations
 
@@ -20,6 +22,9 @@ import numpy as np
 SIZES = [(3, 3), (5, 7), (17, 9), (67, 35), (129, 33), (130, 34), (200, 100), (257, 70),
          (256, 70), (129, 100)]   # full right-edge tiles with mirrored halo reads
 FUSED_SIZES = [(4, 4), (67, 35), (130, 70), (258, 66)]
+# the allocation-free entry point: packed odd rows take the generic kernel,
+# 16-byte rows the TMA kernel
+NOALLOC_SIZES = [(67, 35), (256, 70), (130, 34)]
 
 
 def _dev(a: np.ndarray, pad: bool):
@@ -98,6 +103,21 @@ def main() -> int:
                     if err != 0 or not np.array_equal(u64(sad), want_sad) or not np.array_equal(u64(sse), want_sse):
                         failures.append({"kind": "fused", "w": w, "h": h, "bpc": bpc, "pad": pad, "path": path,
                                          "err": err})
+    for (w, h) in NOALLOC_SIZES:
+        for bpc in (8, 10):
+            for pad in (False, True):
+                fr = _frames(rng, 6, h, w, bpc)
+                d = _dev(fr, pad)
+                want = o.motion_sad_sequence(fr, bpc).astype(np.uint64)
+                out = torch.zeros(6, dtype=torch.int64, device="cuda")
+                iif.motion_submit_batch_noalloc(d[:4], out[:4], bpc=bpc, continue_sequence=False)
+                iif.motion_submit_batch_noalloc(d[4:], out[4:], bpc=bpc, continue_sequence=True)
+                torch.cuda.synchronize()
+                err = iif.motion_noalloc_device_error()
+                cases += 1
+                if err != 0 or not np.array_equal(u64(out), want):
+                    failures.append({"kind": "noalloc", "w": w, "h": h, "bpc": bpc, "pad": pad,
+                                     "err": err, "got": u64(out).tolist(), "want": want.tolist()})
     print(json.dumps({"cases": cases, "failures": failures[:20], "n_failures": len(failures)}))
     return 0
 

@@ -34,9 +34,9 @@ def _frames(w, h, n, bpc=8, seed=3):
 
 def test_init_fails_cleanly_at_each_allocation(iif, oracle):
     import torch
-    # motion_init allocates two resident planes, the result slot, the error
-    # word and the pinned readback slot
-    for k in range(1, 6):
+    # motion_init allocates two resident planes, the result slot (which also
+    # holds the device error word) and the pinned readback slot
+    for k in range(1, 5):
         iif.motion_inject_alloc_failure(k)
         with pytest.raises(iif.MotionError) as e:
             iif.MotionContext(64, 48, 8)

@@ -95,6 +95,33 @@ def test_layout_validation_before_any_device_call(lib):
     assert moments(-1, W, W * H) == 1
 
 
+def test_noalloc_layout_validation_before_any_device_call(lib):
+    """The allocation-free entry point applies the same layout checks as the
+    context calls (pitch <= 2^40, stride <= 2^46, n frames within 2^48
+    bytes, 16-bit alignment) and refuses before any CUDA call: a frame stride
+    above 2^63 would otherwise turn negative as a signed offset."""
+    import ctypes
+    p = ctypes.c_void_p(4096)                     # never dereferenced: validation fails first
+    out = ctypes.cast(ctypes.c_void_p(4096), ctypes.POINTER(ctypes.c_uint64))
+    W, H = 64, 32
+
+    def call(n, pitch, stride, bpc=8, frames=p, cont=0):
+        return lib.motion_submit_batch_noalloc(frames, n, W, H, bpc, stride, pitch, cont, None, out)
+
+    assert call(2, W - 1, W * H) == 4                       # pitch < row
+    assert call(2, 2 * W + 1, 2 * W * H, bpc=10) == 4       # odd 16-bit pitch
+    assert call(2, 2 * W, 2 * W * H + 1, bpc=10) == 4       # odd 16-bit stride
+    assert call(2, (1 << 40) + 16, W * H) == 1              # pitch beyond 2^40
+    assert call(2, W, 1 << 47) == 1                         # stride beyond 2^46
+    assert call(2, W, (1 << 63) + 16) == 1                  # stride above 2^63
+    assert call(1 << 12, W, 1 << 37) == 1                   # 2^49 bytes of frames
+    assert call(2, W, W * H, frames=None) == 1
+    assert call(2, W, W * H, bpc=7) == 3
+    assert lib.motion_submit_batch_noalloc(p, 2, 2, H, 8, W * H, W, 0, None, out) == 2
+    assert lib.motion_submit_batch_noalloc(p, 1, 4096, 4096, 8, 0, 4096, 0, None, out) == 5
+    assert lib.motion_noalloc_device_error(None, None) == 1
+
+
 def test_init_without_device_reports_it(lib):
     import ctypes
     import torch
@@ -106,7 +133,7 @@ def test_init_without_device_reports_it(lib):
 
 def test_strerror_names_every_status(lib):
     import integer_image_filter_gb300 as iif
-    for code in range(10):
+    for code in range(11):
         assert iif.motion_strerror(code) != "unknown status"
     assert iif.motion_strerror(99) == "unknown status"
 
@@ -301,7 +328,7 @@ def test_kernel_source_contract():
 
 
 @pytest.mark.parametrize("plant", [
-    'asm("cp.async.bulk.tensor.2d.shared::cluster.global.multicast::cluster");',
+    'asm("op.multicast::cluster");',
     "    atomicAdd(a.sad_out + f, t0);",
     "    __shared__ unsigned wsum[4];\n    atomicAdd(&out[f], t0);",
     "    const uint8_t* p = a.planes[plane];",
