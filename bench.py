@@ -134,6 +134,7 @@ class ClockSampler:
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.rows = []
+        self.times = []
         self.proc = None
         self.thread = None
 
@@ -154,6 +155,7 @@ class ClockSampler:
             parts = [x.strip() for x in line.split(",")]
             if len(parts) >= 9:
                 self.rows.append(parts)
+                self.times.append(time.time())
 
     def stop(self):
         if self.proc is not None:
@@ -165,16 +167,49 @@ class ClockSampler:
         if self.thread is not None:
             self.thread.join(timeout=5)
 
-    def summary(self):
-        if not self.rows:
+    def summary(self, t0: float | None = None, t1: float | None = None):
+        """Clocks over the samples taken in [t0, t1] (all samples by default)."""
+        rows = [r for r, t in zip(self.rows, self.times)
+                if (t0 is None or t >= t0) and (t1 is None or t <= t1)]
+        if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
-        sm = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
-        mx = [float(r[2]) for r in self.rows if r[2].replace(".", "").isdigit()]
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
         names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
-        reasons = sorted({n for r in self.rows for n, v in zip(names, r[5:9]) if v == "Active"})
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v == "Active"})
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
-                "samples": len(self.rows)}
+                "samples": len(rows)}
+
+
+def sustained_launches(run, stream, min_seconds: float = 1.0, min_launches: int = 200,
+                       max_launches: int = 100000) -> dict:
+    """Repeat one unit of work (`run` enqueues it on `stream`) back to back for
+    at least min_seconds and min_launches, each bracketed by CUDA events on the
+    stream; returns the distribution of the per-launch device times (ms)."""
+    import torch
+    probe = []
+    for _ in range(5):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        run()
+        b.record(stream)
+        probe.append((a, b))
+    torch.cuda.synchronize()
+    est = max(statistics.median(a.elapsed_time(b) for a, b in probe), 1e-3)
+    n = int(min(max_launches, max(min_launches, min_seconds * 1e3 / est)))
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    t0 = time.time()
+    for a, b in ev:
+        a.record(stream)
+        run()
+        b.record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    ms = sorted(a.elapsed_time(b) for a, b in ev)
+    return {"launches": n, "seconds": ev[0][0].elapsed_time(ev[-1][1]) / 1e3,
+            "median_ms": statistics.median(ms), "mean_ms": statistics.mean(ms),
+            "p10_ms": ms[len(ms) // 10], "p90_ms": ms[(9 * len(ms)) // 10], "t0": t0, "t1": t1}
 
 
 def cpu_oracle_rate(batch, budget_s: float, min_pairs: int = 2):
@@ -286,6 +321,122 @@ def run_reference(args):
     return 0
 
 
+def _graph_of(step, dev, stream):
+    """One call of step() captured as a CUDA graph (after a direct warm-up on a
+    side stream); returns the replay function."""
+    import torch
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        step()
+    stream.wait_stream(side)
+    torch.cuda.synchronize(dev)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    torch.cuda.synchronize(dev)
+    return graph.replay
+
+
+def secondary_measurements(dev, stream, planes, n_pairs: int, w420: int, h420: int, clocks,
+                           min_seconds: float = 0.4) -> dict:
+    """The other configurations, each timed as back-to-back steps for at least
+    min_seconds (median step time) with the clocks of its own window: the 10-bit
+    4K sequence at batch 32 and swept over batch 1..32, the 1080p sequence at
+    batch 16, the 576x324 sequence as one 48-frame launch (host-launched and as
+    a CUDA graph), the 64x48 pair per submitted frame, and the stand-alone SSE
+    and moment launches on the 4:2:0 pairs of the default step."""
+    import math
+
+    import numpy as np
+    import torch
+
+    import integer_image_filter_gb300 as iif
+    import synth
+    peak, peak_kind = peaks()
+    out = {}
+
+    def seq_entry(name, batches, graph=False):
+        c = synth.CONFIGS[name]
+        w, h, bpc = c["w"], c["h"], c["bpc"]
+        frames = synth.make(name)
+        n = frames.shape[0]
+        s = 1 if bpc == 8 else 2
+        d = torch.from_numpy(frames.view(np.int16) if bpc > 8 else frames).to(dev)
+        sad = torch.zeros(n, dtype=torch.int64, device=dev)
+        res = {}
+        with iif.MotionContext(w, h, bpc) as ctx:
+            for batch in batches:
+                def step():
+                    cur = torch.cuda.current_stream(dev)
+                    ctx.reset()
+                    for b0 in range(0, n, batch):
+                        ctx.submit_batch(d[b0:b0 + batch], sad[b0:b0 + batch], stream=cur)
+                for _ in range(3):
+                    step()
+                torch.cuda.synchronize(dev)
+                run = _graph_of(step, dev, stream) if graph else step
+                for _ in range(3):
+                    run()
+                r = sustained_launches(run, stream, min_seconds=min_seconds, min_launches=20)
+                ms = r["median_ms"]
+                launches = math.ceil(n / batch)
+                alg = w * h * s * n
+                ops = MOTION_OPS_PER_PIXEL * w * h * n
+                res[batch] = {"frames_per_s": n / (ms * 1e-3), "gb_per_s": alg / (ms * 1e-3) / 1e9,
+                              "hbm_frac": alg / (ms * 1e-3) / 1e9 / peak, "step_ms": ms,
+                              "kernel_ms_per_launch": ms / launches, "batch": batch,
+                              "frames_per_step": n, "steps_timed": r["launches"],
+                              "cuda_graph": graph,
+                              "roofline": seq_roofline(alg, ops, ms, peak, peak_kind),
+                              "clocks": clocks.summary(r["t0"], r["t1"])}
+        return res
+
+    t_all = time.time()
+    u10 = seq_entry("seq_3840x2160_u10", [32, 1, 2, 4, 8, 16])
+    out["seq_3840x2160_u10"] = dict(u10[32], sweep={b: {"frames_per_s": v["frames_per_s"],
+                                                        "hbm_frac": v["hbm_frac"],
+                                                        "kernel_ms_per_launch": v["kernel_ms_per_launch"]}
+                                                    for b, v in sorted(u10.items())})
+    out["seq_1920x1080_u8_cuts"] = seq_entry("seq_1920x1080_u8_cuts", [16])[16]
+    out["seq_576x324_u8"] = seq_entry("seq_576x324_u8", [48])[48]
+    out["seq_576x324_u8_graph"] = seq_entry("seq_576x324_u8", [48], graph=True)[48]
+    # the 64x48 pair: one submitted frame per call (launch + 16-byte readback)
+    pair = synth.make("pair_64x48_u8")
+    dp = torch.from_numpy(pair).to(dev)
+    with iif.MotionContext(64, 48, 8) as ctx:
+        for _ in range(20):
+            ctx.submit(dp[0])
+        t0 = time.perf_counter()
+        k = 0
+        while time.perf_counter() - t0 < min_seconds:
+            ctx.reset()
+            ctx.submit(dp[0])
+            ctx.submit(dp[1])
+            k += 2
+        us = (time.perf_counter() - t0) / k * 1e6
+    out["pair_64x48_u8"] = {"us_per_submitted_frame": us, "frames": k}
+    # stand-alone SSE and moment sums on the default step's pairs
+    sse = torch.zeros((n_pairs, 3), dtype=torch.int64, device=dev)
+    mom = torch.zeros((n_pairs, 4), dtype=torch.int64, device=dev)
+    for name, fn, alg in (
+            ("sse_yuv420_%dx%d_u8_pairs" % (w420, h420),
+             lambda: iif.psnr_sse_yuv420_batch(w420, h420, 8, *planes, sse, stream=stream),
+             algorithmic_bytes_per_pair(w420, h420, 8) * n_pairs),
+            ("moment_%dx%d_u8_pairs" % (w420, h420),
+             lambda: iif.moment_sums_batch(planes[0], planes[3], 8, mom, stream=stream),
+             2 * w420 * h420 * n_pairs)):
+        for _ in range(3):
+            fn()
+        r = sustained_launches(fn, stream, min_seconds=min_seconds, min_launches=50)
+        ms = r["median_ms"]
+        out[name] = {"pairs_per_s": n_pairs / (ms * 1e-3), "gb_per_s": alg / (ms * 1e-3) / 1e9,
+                     "hbm_frac": alg / (ms * 1e-3) / 1e9 / peak, "kernel_ms": ms,
+                     "launches_timed": r["launches"], "clocks": clocks.summary(r["t0"], r["t1"])}
+    out["seconds"] = time.time() - t_all
+    return out
+
+
 def run_gpu(args):
     import numpy as np
     import torch
@@ -345,6 +496,14 @@ def run_gpu(args):
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         total_ms = float(t.item())
         dist.barrier()
+    # the same step repeated back to back for at least a second: the launch
+    # time the roofline uses (median of >= 200 launch events), with the clocks
+    # of that window
+    sus = sustained_launches(step, stream, min_seconds=args.sustain_seconds, min_launches=200)
+    sus["clocks"] = clocks.summary(sus["t0"], sus["t1"])
+    secondary = None
+    if ws == 1 and not args.no_secondary:
+        secondary = secondary_measurements(dev, stream, planes, n, args.w, args.h, clocks)
     clocks.stop()
 
     # the same metric end to end: pinned host pictures -> device -> results on the host
@@ -381,8 +540,8 @@ def run_gpu(args):
     bytes_per_launch = algorithmic_bytes_per_pair(args.w, args.h, 8) * n
     ops_per_launch = n * (MOTION_OPS_PER_PIXEL * args.w * args.h +
                           SSE_OPS_PER_SAMPLE * (args.w * args.h + 2 * ((args.w + 1) // 2) * ((args.h + 1) // 2)))
-    kern_ms = statistics.mean(step_ms)
-    clk = clocks.summary()
+    kern_ms = sus["median_ms"]
+    clk = clocks.summary(None, sus["t1"])
     achieved = bytes_per_launch / (kern_ms * 1e-3) / 1e9
     value = ws * n * args.steps / (total_ms * 1e-3)
     cpu = None
@@ -414,12 +573,19 @@ def run_gpu(args):
                      "kernel": "motion_tma_kernel<uint8_t, fused>",
                      "algorithmic_bytes_per_launch": bytes_per_launch,
                      "kernel_ms": kern_ms,
+                     "kernel_ms_basis": ("median of %d launch events over %.2f s of back-to-back steps "
+                                         "(each step: the call's two output memsets and the fused "
+                                         "kernel); the timed steps' mean is %.4f ms"
+                                         % (sus["launches"], sus["seconds"], statistics.mean(step_ms))),
+                     "sustained": {k: sus[k] for k in ("launches", "seconds", "median_ms", "mean_ms",
+                                                        "p10_ms", "p90_ms", "clocks")},
                      "alu": alu_co_bound(ops_per_launch, kern_ms, (clk or {}).get("sm_max_mhz"))},
         "cpu_baseline": cpu,
         "e2e": {"value": ws * n * e2e_steps / e2e_s, "unit": "frames/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches,
         "clocks": clk,
+        "secondary": secondary,
     }
     print(json.dumps(line), flush=True)
     ctx.close()
@@ -683,6 +849,37 @@ def run_latency_workload(args):
     return 0
 
 
+def run_pipe_rates(args):
+    """The instruction-throughput microbenchmark (libpipe_rates_gb300.so):
+    lane-operations per SM clock per SM of each instruction class the motion
+    kernels issue, measured on this device; one JSON line."""
+    import ctypes
+
+    import torch
+
+    from integer_image_filter_gb300 import _build
+    lib = ctypes.CDLL(_build.build_pipe_rates())
+    lib.pipe_rates_name.restype = ctypes.c_char_p
+    n = lib.pipe_rates_count()
+    out = (ctypes.c_double * n)()
+    torch.cuda.set_device(0)
+    clocks = ClockSampler(0)
+    clocks.start()
+    time.sleep(0.3)
+    rc = lib.pipe_rates_measure(out)
+    time.sleep(0.3)
+    clocks.stop()
+    if rc != 0:
+        raise RuntimeError("pipe_rates_measure failed")
+    rates = {lib.pipe_rates_name(i).decode(): round(out[i], 2) for i in range(n)}
+    print(json.dumps({"metric": "lane-operations per SM clock per SM (shared loads: bytes)",
+                      "rates": rates, "sms": torch.cuda.get_device_properties(0).multi_processor_count,
+                      "clocks": clocks.summary(),
+                      "config": {"workload": "pipe_rates", "threads_per_sm": 1024,
+                                 "chains_per_thread": 8}}), flush=True)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -694,6 +891,10 @@ def main(argv=None):
     ap.add_argument("--h", type=int, default=2160)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-secondary", action="store_true",
+                    help="skip the other configurations' measurements in the default line")
+    ap.add_argument("--sustain-seconds", type=float, default=1.0,
+                    help="length of the back-to-back launch loop behind roofline.kernel_ms")
     ap.add_argument("--workload", default=WORKLOAD,
                     help="the headline 4:2:0 workload (default) or one of the motion-only "
                          "configurations: seq_3840x2160_u10, seq_1920x1080_u8_cuts, "
@@ -710,6 +911,8 @@ def main(argv=None):
     ap.add_argument("--v2", action="store_true",
                     help="sequence workloads: motion_v2 (blur of prev - cur) instead of motion")
     args = ap.parse_args(argv)
+    if args.workload == "pipe_rates" and args.impl == "ours":
+        return run_pipe_rates(args)
     if args.workload == "sse_yuv420_3840x2160_u8_pairs" and args.impl == "ours":
         return run_sse_workload(args)
     if args.workload == "moment_3840x2160_u8_pairs" and args.impl == "ours":

@@ -20,6 +20,10 @@ INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "_lib")
 LIB_NAME = "libmotion_gb300.so"
 CHECKED_LIB_NAME = "libmotion_gb300_checked.so"
+# the instruction-throughput microbenchmark behind the integer co-bound
+# (pipe_rates.cu; a library of its own, not part of the motion library)
+PIPE_LIB_NAME = "libpipe_rates_gb300.so"
+PIPE_SOURCE = "pipe_rates.cu"
 SOURCES = ["motion_capi.cu", "motion_tile.cu", "motion_tma.cu", "psnr_sse.cu", "motion_noalloc.cu",
            "moment.cu", "repitch.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -36,8 +40,28 @@ def lib_path(checked: bool = False) -> str:
     return os.path.join(OUT_DIR, CHECKED_LIB_NAME if checked else LIB_NAME)
 
 
+def pipe_lib_path() -> str:
+    return os.path.join(OUT_DIR, PIPE_LIB_NAME)
+
+
+def build_pipe_rates(force: bool = False) -> str:
+    """Build libpipe_rates_gb300.so (one translation unit)."""
+    src = os.path.join(CSRC, PIPE_SOURCE)
+    out = pipe_lib_path()
+    if not force and os.path.exists(out) and os.path.getmtime(out) >= os.path.getmtime(src):
+        return out
+    os.makedirs(OUT_DIR, exist_ok=True)
+    cmd = [nvcc()] + ARCH + ["-O3", "-std=c++17", "-Xcompiler", "-fPIC,-fvisibility=hidden", "-shared",
+                             "-o", out + ".tmp", src]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"nvcc failed on {PIPE_SOURCE}:\n{r.stdout}\n{r.stderr}")
+    os.replace(out + ".tmp", out)
+    return out
+
+
 def _newest_source_mtime() -> float:
-    files = [os.path.join(CSRC, f) for f in os.listdir(CSRC)]
+    files = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f != PIPE_SOURCE]
     files.append(os.path.join(INCLUDE, "motion.h"))
     files.append(os.path.abspath(__file__))
     return max(os.path.getmtime(f) for f in files)
