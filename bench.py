@@ -46,27 +46,42 @@ def algorithmic_bytes_per_pair(w: int, h: int, bpc: int) -> int:
     return 2 * (w * h + 2 * cw * ch) * s
 
 
-# The integer-arithmetic co-bound.  Algorithmic operations of the definition:
-# per luma pixel 10 multiply-adds for the two 5-tap passes, one absolute
-# difference and one add for the SAD (motion_v2: one subtract more for
-# prev - cur); per sample one subtract and one multiply-add for the squared
-# error.  Peak: two integer pipes of 64 lanes per SM (multiply / dot product,
-# and add / logic / permute; each measured at 64 lane-operations per clock per
-# SM on GB300) at the maximum SM clock.
-MOTION_OPS_PER_PIXEL = 12
-SSE_OPS_PER_SAMPLE = 2
-INT_LANES_PER_SM_CLOCK = 128
+def motion_kernel_name(bpc: int, v2: bool = False) -> str:
+    """The key of a motion-only launch in the recorded profiles."""
+    return "motion_tma_kernel<%s, %s>" % ("uint8_t" if bpc == 8 else "uint16_t",
+                                            "motion_v2" if v2 else "motion")
 
 
-def alu_co_bound(ops_per_launch: float, launch_ms: float, sm_max_mhz) -> dict:
+def numa_placement(host_tensor) -> dict:
+    """NUMA nodes of the host, the node the GPU is attached to, and the node
+    that holds the first page of a pinned host buffer (move_pages query)."""
+    import ctypes
+    import glob
+
     import torch
-    sms = torch.cuda.get_device_properties(0).multi_processor_count
-    mhz = float(sm_max_mhz) if sm_max_mhz else 2070.0
-    peak = sms * INT_LANES_PER_SM_CLOCK * mhz * 1e6 / 1e12
-    achieved = ops_per_launch / (launch_ms * 1e-3) / 1e12
-    return {"achieved": achieved, "peak": peak, "unit": "Tops/s", "frac": achieved / peak,
-            "ops_per_launch": ops_per_launch,
-            "peak_basis": f"{sms} SMs x {INT_LANES_PER_SM_CLOCK} integer lanes x {mhz:.0f} MHz"}
+    info = {}
+    try:
+        info["host_nodes"] = sorted(int(p.rsplit("node", 1)[1])
+                                    for p in glob.glob("/sys/devices/system/node/node[0-9]*"))
+    except Exception:
+        info["host_nodes"] = None
+    try:
+        pr = torch.cuda.get_device_properties(0)
+        bus = "%04x:%02x:%02x.0" % (pr.pci_domain_id, pr.pci_bus_id, pr.pci_device_id)
+        with open(f"/sys/bus/pci/devices/{bus}/numa_node") as f:
+            info["gpu_node"] = int(f.read().strip())
+    except Exception:
+        info["gpu_node"] = None
+    try:
+        libc = ctypes.CDLL(None, use_errno=True)
+        nr = 239 if os.uname().machine == "aarch64" else 279      # move_pages
+        page = (ctypes.c_void_p * 1)(host_tensor.data_ptr())
+        status = (ctypes.c_int * 1)(-1)
+        rc = libc.syscall(nr, 0, ctypes.c_ulong(1), page, None, status, 0)
+        info["pinned_pages_node"] = int(status[0]) if rc == 0 and status[0] >= 0 else None
+    except Exception:
+        info["pinned_pages_node"] = None
+    return info
 
 
 def dist_env():
@@ -108,6 +123,59 @@ def kernel_source_hash() -> str:
         with open(os.path.join(csrc, f), encoding="utf-8") as fh:
             h.update(f.encode() + b"\0" + _code_tokens(fh.read()))
     return h.hexdigest()[:16]
+
+
+# Warp instructions each unit can take per SM clock, from the measured rates
+# (profiles/pipe_rates_gb300.md: every integer class at 64 lanes per SM clock
+# = 2 warp instructions; the 4 schedulers issue one warp instruction each).
+PIPE_WARP_INST_PER_SM_CLOCK = {"issue": 4.0, "alu": 2.0, "fmaheavy": 2.0}
+
+
+def recorded_inst_mix(kernel: str, workload: str):
+    """ncu instruction counts per launch (total and per pipe) from the committed
+    record, or None when the kernel sources changed since the capture."""
+    p = os.path.join(ROOT, "profiles", "inst_mix.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        e = d[kernel][workload]
+        if e.get("source_hash") != kernel_source_hash():
+            return None
+        return e
+    except Exception:
+        return None
+
+
+def instruction_co_bound(kernel: str, workload: str, launch_ms: float, sm_mhz,
+                         units: float | None = None, batch: int | None = None) -> dict:
+    """The integer co-bound of a launch (or a step of `units` frames or pairs):
+    for the issue slots (4 warp instructions per SM clock) and each integer pipe
+    (ALU and FMA-heavy, 2 per SM clock), the time its recorded instruction count
+    needs at that rate ÷ the measured time; the largest is the bound.  Counts
+    are recorded per captured launch of rec["units"] units and scaled."""
+    import torch
+    rec = recorded_inst_mix(kernel, workload)
+    if rec is None:
+        return {"available": False,
+                "why": "no ncu instruction counts recorded for these kernel sources and this launch"}
+    if batch is not None and rec.get("batch") not in (None, batch):
+        return {"available": False, "why": "instruction counts recorded for batch %s" % rec.get("batch")}
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    mhz = float(sm_mhz) if sm_mhz else 2070.0
+    scale = (units / float(rec["units"])) if units else 1.0
+    per = {}
+    for unit, rate in PIPE_WARP_INST_PER_SM_CLOCK.items():
+        count = scale * float(rec["inst"] if unit == "issue" else rec[unit])
+        need_ms = count / (rate * sms * mhz * 1e6) * 1e3
+        per[unit] = {"warp_inst_per_launch": count, "ms_at_peak": need_ms, "frac": need_ms / launch_ms}
+    bound = max(per, key=lambda k: per[k]["frac"])
+    peak = PIPE_WARP_INST_PER_SM_CLOCK[bound] * sms * mhz * 1e6 / 1e9
+    return {"bound": bound, "achieved": per[bound]["warp_inst_per_launch"] / (launch_ms * 1e-3) / 1e9,
+            "peak": peak, "unit": "G warp instructions/s", "frac": per[bound]["frac"],
+            "per_unit": per, "thread_inst_per_pixel": rec.get("thread_inst_per_pixel"),
+            "peak_basis": (f"{sms} SMs x {PIPE_WARP_INST_PER_SM_CLOCK[bound]:.0f} warp instructions per "
+                           f"SM clock ({bound}; measured rates, profiles/pipe_rates_gb300.md) x {mhz:.0f} MHz"),
+            "counts": "profiles/inst_mix.json (ncu, same kernel sources and launch)"}
 
 
 def recorded_traffic(kernel: str, workload: str):
@@ -382,14 +450,14 @@ def secondary_measurements(dev, stream, planes, n_pairs: int, w420: int, h420: i
                 ms = r["median_ms"]
                 launches = math.ceil(n / batch)
                 alg = w * h * s * n
-                ops = MOTION_OPS_PER_PIXEL * w * h * n
                 res[batch] = {"frames_per_s": n / (ms * 1e-3), "gb_per_s": alg / (ms * 1e-3) / 1e9,
                               "hbm_frac": alg / (ms * 1e-3) / 1e9 / peak, "step_ms": ms,
                               "kernel_ms_per_launch": ms / launches, "batch": batch,
                               "frames_per_step": n, "steps_timed": r["launches"],
                               "cuda_graph": graph,
-                              "roofline": seq_roofline(alg, ops, ms, peak, peak_kind),
                               "clocks": clocks.summary(r["t0"], r["t1"])}
+                res[batch]["roofline"] = seq_roofline(alg, ms, peak, peak_kind, motion_kernel_name(bpc), name,
+                                                      n, res[batch]["clocks"].get("sm_mhz"), batch)
         return res
 
     t_all = time.time()
@@ -524,6 +592,7 @@ def run_gpu(args):
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         e2e_s = float(t.item())
     h2d = sum(p.numel() * p.element_size() for p in pinned)
+    numa = numa_placement(pinned[0])
     d2h = h_sad.nbytes + h_sse.nbytes
     dev_sad = sad.cpu().numpy().astype(np.uint64)
     dev_sse = sse.cpu().numpy().astype(np.uint64)
@@ -538,8 +607,6 @@ def run_gpu(args):
 
     peak, peak_kind = peaks()
     bytes_per_launch = algorithmic_bytes_per_pair(args.w, args.h, 8) * n
-    ops_per_launch = n * (MOTION_OPS_PER_PIXEL * args.w * args.h +
-                          SSE_OPS_PER_SAMPLE * (args.w * args.h + 2 * ((args.w + 1) // 2) * ((args.h + 1) // 2)))
     kern_ms = sus["median_ms"]
     clk = clocks.summary(None, sus["t1"])
     achieved = bytes_per_launch / (kern_ms * 1e-3) / 1e9
@@ -579,10 +646,12 @@ def run_gpu(args):
                                          % (sus["launches"], sus["seconds"], statistics.mean(step_ms))),
                      "sustained": {k: sus[k] for k in ("launches", "seconds", "median_ms", "mean_ms",
                                                         "p10_ms", "p90_ms", "clocks")},
-                     "alu": alu_co_bound(ops_per_launch, kern_ms, (clk or {}).get("sm_max_mhz"))},
+                     "alu": instruction_co_bound("motion_tma_kernel<uint8_t, fused>", WORKLOAD, kern_ms,
+                                                 (clk or {}).get("sm_mhz"))},
         "cpu_baseline": cpu,
         "e2e": {"value": ws * n * e2e_steps / e2e_s, "unit": "frames/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "host_link_gbs": h2d * e2e_steps / e2e_s / 1e9, "numa": numa},
         "gpu_launches": launches,
         "clocks": clk,
         "secondary": secondary,
@@ -594,22 +663,18 @@ def run_gpu(args):
     return 0
 
 
-def seq_roofline(alg_bytes: int, ops: int, ms: float, peak_gbs: float, peak_kind: str) -> dict:
-    """Roofline of a motion-only step: the lower of the HBM roof (algorithmic
-    bytes at the measured copy bandwidth) and the integer roof (algorithmic
-    operations at the integer lane peak) is the bound; the other is reported
-    beside it.  8-bit motion has 12 operations per byte and is bound by the
-    integer roof; the 4:2:0 pairs, with their SSE bytes, by HBM."""
-    hbm = {"achieved": alg_bytes / (ms * 1e-3) / 1e9, "peak": peak_gbs, "unit": "GB/s",
-           "frac": alg_bytes / (ms * 1e-3) / 1e9 / peak_gbs, "peak_kind": peak_kind,
+def seq_roofline(alg_bytes: int, ms: float, peak_gbs: float, peak_kind: str, kernel: str,
+                 workload: str, frames: int, sm_mhz=None, batch: int | None = None) -> dict:
+    """Roofline of a motion-only step: HBM (algorithmic bytes, every frame read
+    once, at the measured copy bandwidth) is the roof; beside it the integer
+    co-bound of the same time from the kernel's recorded instruction counts
+    (instruction_co_bound), which is the one these launches run against: 8-bit
+    motion needs about 19 instructions per byte read."""
+    hbm = {"bound": "hbm", "achieved": alg_bytes / (ms * 1e-3) / 1e9, "peak": peak_gbs,
+           "unit": "GB/s", "frac": alg_bytes / (ms * 1e-3) / 1e9 / peak_gbs, "peak_kind": peak_kind,
            "algorithmic_bytes_per_step": alg_bytes}
-    alu = alu_co_bound(ops, ms, None)
-    hbm_roof_ms = alg_bytes / (peak_gbs * 1e9) * 1e3
-    alu_roof_ms = ops / (alu["peak"] * 1e12) * 1e3
-    if alu_roof_ms > hbm_roof_ms:
-        return dict({"bound": "alu"}, **{k: alu[k] for k in ("achieved", "peak", "unit", "frac")},
-                    peak_kind="derived: " + alu["peak_basis"], ops_per_step=ops, hbm=hbm)
-    return dict({"bound": "hbm"}, **hbm, alu=alu)
+    hbm["alu"] = instruction_co_bound(kernel, workload, ms, sm_mhz, units=frames, batch=batch)
+    return hbm
 
 
 def run_sequence_workload(args):
@@ -691,7 +756,6 @@ def run_sequence_workload(args):
         if not args.graph:
             launches = (iif.motion_kernel_launch_count() - l0) / args.steps
         alg = w * h * s * n
-        ops = (MOTION_OPS_PER_PIXEL + (1 if args.v2 else 0)) * w * h * n
         e2e = None
         if not args.v2 and not args.graph and not args.generic:
             # end to end: the same sequence from pinned host memory through
@@ -721,7 +785,8 @@ def run_sequence_workload(args):
                                  "frames_per_step": n, "batch": batch,
                                  "launches_per_step": launches, "cuda_graph": bool(args.graph),
                                  "kernel_path": "generic" if args.generic else "auto"},
-                      "roofline": seq_roofline(alg, ops, ms, peak, peak_kind), "e2e": e2e})
+                      "roofline": seq_roofline(alg, ms, peak, peak_kind, motion_kernel_name(bpc, args.v2),
+                                               args.workload, n, batch=batch), "e2e": e2e})
         ctx.close()
     for ln in lines:
         print(json.dumps(ln), flush=True)
@@ -849,6 +914,62 @@ def run_latency_workload(args):
     return 0
 
 
+def run_host_link(args):
+    """Host link ceiling by NUMA node: 1 GiB pinned buffers allocated under a
+    memory policy bound to each host node (and the default policy), host->device
+    and device->host copy rates (best of 5 and 3, CUDA events); one JSON line
+    with the GPU's node and where the pinned pages landed."""
+    import ctypes
+    import glob
+
+    import torch
+    libc = ctypes.CDLL(None, use_errno=True)
+    nr_set_mempolicy = 237 if os.uname().machine == "aarch64" else 238
+    nodes = sorted(int(p.rsplit("node", 1)[1]) for p in glob.glob("/sys/devices/system/node/node[0-9]*"))
+
+    def bind(node):
+        if node is None:
+            return libc.syscall(nr_set_mempolicy, 0, None, ctypes.c_ulong(0))
+        mask = ctypes.c_ulong(1 << node)
+        return libc.syscall(nr_set_mempolicy, 2, ctypes.byref(mask), ctypes.c_ulong(64))
+
+    torch.cuda.set_device(0)
+    s = torch.cuda.current_stream()
+    dev = torch.empty(1 << 30, dtype=torch.uint8, device="cuda")
+
+    def rate(copy, reps):
+        best = 0.0
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(s)
+            copy()
+            e1.record(s)
+            torch.cuda.synchronize()
+            best = max(best, (1 << 30) / (e0.elapsed_time(e1) * 1e-3) / 1e9)
+        return best
+
+    res = {}
+    for node in [None] + nodes:
+        if bind(node) != 0:
+            res["default" if node is None else str(node)] = {"error": "set_mempolicy refused"}
+            continue
+        try:
+            h = torch.empty(1 << 30, dtype=torch.uint8).pin_memory()
+            h.fill_(1)
+        finally:
+            bind(None)
+        dev.copy_(h, non_blocking=True)
+        torch.cuda.synchronize()
+        res["default" if node is None else str(node)] = {
+            "h2d_gbs": rate(lambda: dev.copy_(h, non_blocking=True), 5),
+            "d2h_gbs": rate(lambda: h.copy_(dev, non_blocking=True), 3),
+            "placement": numa_placement(h)}
+        del h
+    print(json.dumps({"metric": "pinned host link GB/s by NUMA node", "by_policy": res,
+                      "config": {"workload": "host_link", "bytes": 1 << 30}}), flush=True)
+    return 0
+
+
 def run_pipe_rates(args):
     """The instruction-throughput microbenchmark (libpipe_rates_gb300.so):
     lane-operations per SM clock per SM of each instruction class the motion
@@ -899,7 +1020,9 @@ def main(argv=None):
                     help="the headline 4:2:0 workload (default) or one of the motion-only "
                          "configurations: seq_3840x2160_u10, seq_1920x1080_u8_cuts, "
                          "seq_576x324_u8, pair_64x48_u8; or sse_yuv420_3840x2160_u8_pairs, "
-                         "moment_3840x2160_u8_pairs (stand-alone SSE / luma moment sums)")
+                         "moment_3840x2160_u8_pairs (stand-alone SSE / luma moment sums); "
+                         "pipe_rates (instruction throughput per SM), host_link (pinned copy "
+                         "rates by NUMA node)")
     ap.add_argument("--batch", type=int, default=0, help="frames per launch (sequence workloads)")
     ap.add_argument("--sweep", action="store_true", help="sweep batch sizes 1..32")
     ap.add_argument("--graph", action="store_true",
@@ -913,6 +1036,8 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.workload == "pipe_rates" and args.impl == "ours":
         return run_pipe_rates(args)
+    if args.workload == "host_link" and args.impl == "ours":
+        return run_host_link(args)
     if args.workload == "sse_yuv420_3840x2160_u8_pairs" and args.impl == "ours":
         return run_sse_workload(args)
     if args.workload == "moment_3840x2160_u8_pairs" and args.impl == "ours":
