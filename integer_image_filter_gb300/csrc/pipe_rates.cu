@@ -104,7 +104,7 @@ __global__ void __launch_bounds__(256) rate_kernel(int iters, uint32_t seed, Out
 #pragma unroll
     for (int c = 0; c < kChains; ++c) acc ^= v[c];
     if (threadIdx.x == 0) atomicMax(&out->max_cycles, (unsigned long long)(t1 - t0));
-    if (acc == 0x12345678u) atomicAdd(&out->sink, 1ull);   // keeps the chains live
+    if (acc == 0x12345678u) out->sink = acc;   // keeps the chains live
 }
 
 // Shared-memory loads of 32 or 128 bits per lane, consecutive across the warp.
@@ -136,7 +136,7 @@ __global__ void __launch_bounds__(256) lds_kernel(int iters, uint32_t seed, Out*
     const long long t1 = clock64();
     __syncthreads();
     if (threadIdx.x == 0) atomicMax(&out->max_cycles, (unsigned long long)(t1 - t0));
-    if (acc == 0x12345678u) atomicAdd(&out->sink, 1ull);
+    if (acc == 0x12345678u) out->sink = acc;
 }
 
 template <typename K>
