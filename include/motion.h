@@ -324,6 +324,24 @@ MOTION_API int motion_plan_chunks(int w, int h, int n, int resident_ctas, int* c
  * tile_out). */
 MOTION_API int motion_tile_order(int w, int h, int chunks, long long block, int* tile_out);
 
+/* Diagnostic, host only, no GPU: the blocks of a batched motion launch of n
+ * frames of w x h on a device where `resident_ctas` motion blocks run at once
+ * (4 per SM on GB300: 608).  The launch is sized by the SM count ("ADR-1226:
+ * Size the CUDA AIM CM launch by SM count, not by a fixed rows-per-thread"):
+ * the frames run in motion_plan_chunks chunks; a one-chunk launch of more than
+ * a wave whose last wave would be at most half full keeps the tiles of its full
+ * waves whole and splits the other tiles into chunks (of at least 4 frames but
+ * the last, at most 8 per tile), so that the blocks that start last are short.  A chunk that
+ * starts after frame 0 blurs the frame before it as well (no output for it).
+ * *blocks_out (host) receives the block count; for 0 <= block < that count,
+ * work_out (host int[4]) receives {tile column, tile row, first frame, end
+ * frame} of that block (block < 0: the count only).  Errors:
+ * MOTION_ERR_INVALID_ARGUMENT (w, h outside 1..32768, n < 1, resident_ctas <
+ * 1, NULL blocks_out, block past the launch or NULL work_out).  The
+ * allocation-free entry point, which continues in place, never splits. */
+MOTION_API int motion_launch_blocks(int w, int h, int n, int resident_ctas, long long block,
+                                    int* work_out, long long* blocks_out);
+
 /* Test hook for allocation failures (not part of the method): the nth
  * device or pinned-host allocation the library makes from now on (1 = the
  * next one) fails with MOTION_ERR_OUT_OF_MEMORY without reaching the driver;

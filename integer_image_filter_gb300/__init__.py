@@ -31,6 +31,7 @@ __all__ = [
     "moments_from_sums", "motion_v2_submit_batch", "motion_plan_chunks", "motion_tile_order",
     "motion_inject_alloc_failure", "motion_submit_batch_host", "motion_set_copy_limit",
     "motion_noalloc_device_error", "motion_noalloc_set_stall_injection", "MOTION_ERR_DEVICE",
+    "motion_launch_blocks",
 ]
 
 EXPORTED_SYMBOLS = (
@@ -42,7 +43,7 @@ EXPORTED_SYMBOLS = (
     "motion_set_stall_injection", "moment_sums_batch", "moments_from_sums",
     "motion_v2_submit_batch", "motion_plan_chunks", "motion_tile_order", "motion_inject_alloc_failure",
     "motion_submit_batch_host", "motion_set_copy_limit", "motion_noalloc_device_error",
-    "motion_noalloc_set_stall_injection",
+    "motion_noalloc_set_stall_injection", "motion_launch_blocks",
 )
 
 # Status of a call whose kernel set the device error word (include/motion.h).
@@ -96,6 +97,8 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
         "motion_set_copy_limit": ([P, Z], I),
         "motion_noalloc_device_error": ([P, ctypes.POINTER(I)], I),
         "motion_noalloc_set_stall_injection": ([I], I),
+        "motion_launch_blocks": ([I, I, I, I, ctypes.c_longlong, ctypes.POINTER(I),
+                                  ctypes.POINTER(ctypes.c_longlong)], I),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -430,6 +433,16 @@ def motion_tile_order(w: int, h: int, chunks: int, block: int) -> tuple[int, int
     t = (ctypes.c_int * 3)()
     _check(load_library().motion_tile_order(w, h, chunks, block, t), "motion_tile_order")
     return int(t[0]), int(t[1]), int(t[2])
+
+
+def motion_launch_blocks(w: int, h: int, n: int, resident_ctas: int, block: int = -1):
+    """Diagnostic: the block count of a batched motion launch and, for block
+    >= 0, that block's (tile column, tile row, first frame, end frame)."""
+    out = (ctypes.c_int * 4)()
+    cnt = ctypes.c_longlong()
+    _check(load_library().motion_launch_blocks(w, h, n, resident_ctas, block, out, ctypes.byref(cnt)),
+           "motion_launch_blocks")
+    return int(cnt.value), (tuple(out) if block >= 0 else None)
 
 
 def motion_plan_chunks(w: int, h: int, n: int, resident_ctas: int) -> int:

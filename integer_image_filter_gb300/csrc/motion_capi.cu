@@ -895,6 +895,29 @@ int motion_tile_order(int w, int h, int chunks, long long block, int* tile_out) 
     return MOTION_OK;
 }
 
+int motion_launch_blocks(int w, int h, int n, int resident_ctas, long long block, int* work_out,
+                         long long* blocks_out) {
+    if (w < 1 || h < 1 || w > 32768 || h > 32768 || n < 1 || resident_ctas < 1 || !blocks_out)
+        return MOTION_ERR_INVALID_ARGUMENT;
+    const int gx = (w + mg::kTileW - 1) / mg::kTileW, gy = (h + mg::kTileH - 1) / mg::kTileH;
+    const long long tiles = (long long)gx * gy;
+    const int c = mg::plan_frame_chunks(tiles, resident_ctas, n, 8);
+    const int chunk = (n + c - 1) / c;
+    const int gz = (n + chunk - 1) / chunk;
+    int tiles_a = 0, chunk_b = 0;
+    long long blocks = tiles * gz;
+    if (c == 1) {
+        const long long split = mg::plan_split_tail(tiles, resident_ctas, n, &tiles_a, &chunk_b);
+        if (split > 0) blocks = split;
+    }
+    *blocks_out = blocks;
+    if (block < 0) return MOTION_OK;   // the count only
+    if (block >= blocks || !work_out) return MOTION_ERR_INVALID_ARGUMENT;
+    mg::block_work(w, h, gx, gy, gz, n, chunk, tiles_a, chunk_b, (int)block, &work_out[0], &work_out[1],
+                   &work_out[2], &work_out[3]);
+    return MOTION_OK;
+}
+
 int motion_set_copy_limit(motion_ctx* c, size_t bytes) {
     if (!c) return MOTION_ERR_INVALID_ARGUMENT;
     c->rp_limit = bytes;

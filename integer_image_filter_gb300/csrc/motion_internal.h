@@ -33,6 +33,10 @@ struct TileArgs {
     unsigned long long* sse_out;  // [n][3], zeroed by the caller (fused only)
     int* err;                     // device error word (bit 0: a stage wait timed out)
     int chunk;                    // TMA kernel: frames per CTA (grid.z = ceil(n / chunk))
+    // TMA kernel, split tail (tiles_a > 0; see block_work): a one-dimensional
+    // grid whose first tiles_a blocks take tiles 0 .. tiles_a-1 whole and whose
+    // other blocks take the remaining tiles in chunks of chunk_b frames
+    int tiles_a, chunk_b;
     long long wait_cycles;        // bound of every mbarrier wait (0: about one second)
     int tx_extra;                 // test hook: bytes a stage expects beyond its boxes (0)
     // motion_v2 (blur of prev - cur): the last raw frame of the previous call
@@ -116,6 +120,43 @@ __host__ __device__ inline void tile_of_block(int w, int h, int gx, int gy, int 
         *tx = nfull + rr % per;
     }
 }
+// The work of block `lin` of a TMA launch over n frames of w x h: its tile
+// (tile_of_block order) and frames [*f_begin, *f_end).  Uniform launches
+// (tiles_a == 0) run gx x gy x gz blocks, each tile in gz chunks of `chunk`
+// frames.  Split-tail launches (tiles_a > 0) run tiles_a whole tiles first
+// and then the other tiles in chunks of chunk_b frames, chunk-major, so that
+// the last blocks to start are short.  A block whose chunk starts after frame
+// 0 also blurs the frame before it (no output for that frame).
+__host__ __device__ inline void block_work(int w, int h, int gx, int gy, int gz, int n, int chunk,
+                                           int tiles_a, int chunk_b, int lin, int* tx, int* ty,
+                                           int* f_begin, int* f_end) {
+    int cz = 0, len = chunk > 0 ? chunk : n;
+    if (tiles_a > 0) {
+        int t = lin, dz;
+        len = n;
+        if (lin >= tiles_a) {
+            const int tb = gx * gy - tiles_a;
+            const int r = lin - tiles_a;
+            cz = r / tb;
+            t = tiles_a + (r - cz * tb);
+            len = chunk_b;
+        }
+        tile_of_block(w, h, gx, gy, 1, t, tx, ty, &dz);
+    } else {
+        tile_of_block(w, h, gx, gy, gz, lin, tx, ty, &cz);
+    }
+    *f_begin = cz * len;
+    *f_end = *f_begin + len < n ? *f_begin + len : n;
+}
+// The split-tail plan of a one-chunk launch of `tiles` tiles over `slots`
+// resident blocks (host only): when the tiles fill more than one wave and
+// the last wave is at most half full, the tiles of the full waves stay whole
+// (*tiles_a) and the rest are split into chunks of *chunk_b frames (at least
+// 4, a tile's last chunk the remainder; at most 8 chunks, as many as the last
+// wave has room for);
+// returns the block count, or 0 (and *tiles_a = 0) for no split.
+long long plan_split_tail(long long tiles, long long slots, int n, int* tiles_a, int* chunk_b);
+
 // Chunks of a TMA launch (host only): n frames over `tiles` tiles with
 // `slots` CTAs resident on the device at once; 1 <= result <= max_c; v2
 // selects the motion_v2 kernel's constants.

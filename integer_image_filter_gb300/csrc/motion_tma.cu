@@ -209,9 +209,11 @@ __global__ void __launch_bounds__(Shape::NTK, Shape::MINB)
     [[maybe_unused]] const Span vrows{sV, 4 * SVW * sizeof(uint32_t)};   // this warp's V rows
     // border tiles of every chunk first, interior tiles after them in row-major
     // order (tile_of_block)
-    int tx, ty, cz;
-    tile_of_block(a.w, a.h, gridDim.x, gridDim.y, gridDim.z,
-                  blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z), &tx, &ty, &cz);
+    // this block's tile and frames (uniform chunks, or a split-tail launch)
+    int tx, ty, f_begin, f_end;
+    block_work(a.w, a.h, (a.w + TW - 1) / TW, (a.h + TH - 1) / TH, gridDim.z, a.n, a.chunk, a.tiles_a,
+               a.chunk_b, blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z), &tx, &ty, &f_begin,
+               &f_end);
     const int x0 = tx * TW, y0 = ty * TH;
     const bool full_tile = (x0 + TW <= a.w) && (y0 + TH <= a.h);
     const bool pl = x0 == 0, pt = y0 == 0;
@@ -254,15 +256,11 @@ __global__ void __launch_bounds__(Shape::NTK, Shape::MINB)
     }
     __syncthreads();
 
-    // this CTA's frames: chunk cz of the launch; a chunk after the
-    // first starts one frame early to rebuild B_prev (no outputs for it).
-    // motion_v2 continuing an earlier call starts from that call's last raw
-    // frame (the prev map) in the same way.
-    const int chunk = a.chunk > 0 ? a.chunk : a.n;
-    const int f_begin = cz * chunk;
-    const int f_end = min(a.n, f_begin + chunk);
-    const bool warm_prev = V2 && cz == 0 && a.has_prev;
-    const bool warm = cz > 0 || warm_prev;
+    // a chunk that starts after frame 0 starts one frame early to rebuild
+    // B_prev (no outputs for it).  motion_v2 continuing an earlier call starts
+    // from that call's last raw frame (the prev map) in the same way.
+    const bool warm_prev = V2 && f_begin == 0 && a.has_prev;
+    const bool warm = f_begin > 0 || warm_prev;
     const int first = f_begin - (warm ? 1 : 0);
     const int cnt = f_end - first;
     const bool use_prev = !V2 && !warm && a.has_prev;
@@ -707,6 +705,23 @@ int plan_frame_chunks(long long tiles, long long slots, int n, int max_c, bool v
     return best_c;
 }
 
+long long plan_split_tail(long long tiles, long long slots, int n, int* tiles_a, int* chunk_b) {
+    *tiles_a = 0;
+    *chunk_b = 0;
+    if (slots <= 0 || tiles <= slots) return 0;
+    const long long rest = tiles % slots;
+    if (rest == 0 || 2 * rest > slots) return 0;
+    long long cb = slots / rest;
+    if (cb > 8) cb = 8;
+    while (cb > 1 && (n + cb - 1) / cb < 4) --cb;
+    if (cb < 2) return 0;
+    const int len = (int)((n + cb - 1) / cb);
+    const long long chunks = (n + len - 1) / len;   // non-empty chunks
+    *tiles_a = (int)(tiles - rest);
+    *chunk_b = len;
+    return (tiles - rest) + rest * chunks;
+}
+
 namespace {
 
 // The driver's tensor-map encoder, looked up once (a function-local static is
@@ -779,6 +794,12 @@ cudaError_t launch_tma_one(const TmaMaps& maps, const TileArgs& a, cudaStream_t 
     const int best_c = plan_frame_chunks(tiles, spm, a.n, same_plane ? 1 : 8, V2);
     b.chunk = (a.n + best_c - 1) / best_c;
     dim3 grid((a.w + TW - 1) / TW, (a.h + TH - 1) / TH, (a.n + b.chunk - 1) / b.chunk);
+    b.tiles_a = 0;
+    b.chunk_b = 0;
+    if (best_c == 1 && !same_plane) {
+        const long long blocks = plan_split_tail(tiles, spm, a.n, &b.tiles_a, &b.chunk_b);
+        if (blocks > 0) grid = dim3((unsigned)blocks, 1, 1);
+    }
     motion_tma_kernel<Pix, FUSED, STAGES, V2><<<grid, Shape::NTK, SMEM, s>>>(maps, b);
     return cudaGetLastError();
 }

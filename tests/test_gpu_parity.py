@@ -139,6 +139,33 @@ def test_u10_batch_sizes_agree(iif, oracle, batch):
     assert np.array_equal(run_batches(iif, frames, 10, batch), want)
 
 
+@pytest.mark.parametrize("bpc", [8, 10])
+def test_split_tail_launch(iif, oracle, bpc):
+    """A launch shape that splits its tail: 2560x1440 frames in batches of 8
+    are 900 tiles, one full wave of 4 blocks per SM plus 292 tiles, which run
+    in chunks of 4 frames after the whole tiles (the plan checked through
+    motion_launch_blocks on this device's SM count); two calls of the sequence
+    against the oracle, motion and motion_v2."""
+    import torch
+    w, h, n, batch = 2560, 1440, 16, 8
+    slots = 4 * torch.cuda.get_device_properties(0).multi_processor_count
+    tiles = (w // 128) * (h // 32)
+    count, _ = iif.motion_launch_blocks(w, h, batch, slots)
+    if iif.motion_plan_chunks(w, h, batch, slots) == 1 and tiles > slots and 0 < 2 * (tiles % slots) <= slots:
+        assert count > tiles, "the launch splits its tail"
+    frames = synth.uniform_frames(77 + bpc, n, w, h, bpc)
+    want = oracle_sad(oracle, frames, bpc)
+    assert np.array_equal(run_batches(iif, frames, bpc, batch), want)
+    d = to_dev(frames)
+    out = dev_zeros(n)
+    with iif.MotionContext(w, h, bpc) as ctx:
+        for s0 in range(0, n, batch):
+            ctx.submit_batch_v2(d[s0:s0 + batch], out[s0:s0 + batch])
+        torch.cuda.synchronize()
+        assert ctx.device_error() == 0
+    assert np.array_equal(to_u64(out), oracle.motion_v2_sequence(frames, bpc))
+
+
 # --------------------------------------------------------------- shapes, layouts
 SIZES = [(w, h) for w in (3, 4, 5, 7, 9) for h in (3, 4, 6, 9)] + [
     (16, 16), (17, 33), (67, 35), (127, 31), (128, 32), (129, 33), (131, 70), (160, 36),

@@ -225,6 +225,49 @@ def test_frame_chunk_plan(lib):
         plan(10, 10, 4, 0)
 
 
+def test_launch_blocks_cover_every_frame_once(lib):
+    """The blocks of a batched launch (uniform chunks or a split tail) cover
+    every (tile, frame) exactly once; a split tail keeps the tiles of the full
+    waves whole, gives the last-wave tiles short chunks (at least 4 frames) and
+    puts them after the whole tiles."""
+    import numpy as np
+
+    import integer_image_filter_gb300 as iif
+    cases = [(3840, 2160, 32, 608), (3840, 2160, 16, 608), (3840, 2160, 50, 608), (1920, 1080, 16, 608),
+             (1920, 1080, 32, 608), (576, 324, 48, 608), (64, 48, 4, 608), (3840, 2160, 120, 608),
+             (4096, 2048, 9, 100), (1000, 700, 13, 7), (3, 3, 1, 1), (1366, 768, 8, 152)]
+    for (w, h, n, slots) in cases:
+        gx, gy = -(-w // 128), -(-h // 32)
+        count, _ = iif.motion_launch_blocks(w, h, n, slots)
+        seen = np.zeros((gy, gx, n), np.int32)
+        lens = []
+        for b in range(count):
+            _, (tx, ty, f0, f1) = iif.motion_launch_blocks(w, h, n, slots, b)
+            assert 0 <= tx < gx and 0 <= ty < gy and 0 <= f0 < f1 <= n, (w, h, n, b)
+            seen[ty, tx, f0:f1] += 1
+            lens.append(f1 - f0)
+        assert (seen == 1).all(), (w, h, n, slots)
+        tiles = gx * gy
+        if count != tiles * -(-n // -(-n // iif.motion_plan_chunks(w, h, n, slots))):
+            # a split tail: whole tiles first, then chunks of >= 4 frames
+            rest = tiles % slots
+            whole = tiles - rest
+            assert all(x == n for x in lens[:whole]), (w, h, n)
+            chunk = max(lens[whole:])
+            assert 4 <= chunk < n, (w, h, n)
+            # every chunk has that length but the one that ends at the last frame
+            for b in range(whole, count):
+                _, (tx, ty, f0, f1) = iif.motion_launch_blocks(w, h, n, slots, b)
+                assert f1 - f0 == chunk or f1 == n, (w, h, n, b)
+            assert 0 < 2 * rest <= slots
+    # the 10-bit 4K batch of 32: 1824 whole tiles and 216 tiles in two halves
+    assert iif.motion_launch_blocks(3840, 2160, 32, 608)[0] == 1824 + 2 * 216
+    assert iif.motion_launch_blocks(3840, 2160, 32, 608, 1824)[1][2:] == (0, 16)
+    assert iif.motion_launch_blocks(3840, 2160, 32, 608, 1824 + 216)[1][2:] == (16, 32)
+    with pytest.raises(iif.MotionError):
+        iif.motion_launch_blocks(3840, 2160, 32, 608, 1824 + 432)
+
+
 def test_tile_order(lib):
     """Block order of a batched launch: every (tile, chunk) exactly once; the
     tiles that run the border copy of the frame loop (top row, rows whose halo
