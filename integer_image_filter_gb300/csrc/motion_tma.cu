@@ -87,6 +87,49 @@ __device__ __forceinline__ void vertical_quad(const uint8_t* src, RowOff ro, uin
         MG_ST(reinterpret_cast<uint4*>(dst + j * SVW), o, vrows.p, vrows.n);
     }
 }
+// The vertical pass of all 8 of a warp's rows at once: 12 staged rows, each
+// loaded and interleaved (or unpacked) once, 8 V rows into the warp's V rows.
+template <typename RowOff>
+__device__ __forceinline__ void vertical_oct(const uint8_t* src, RowOff ro, uint32_t* dst, uint32_t rnd,
+                                             int sh, [[maybe_unused]] Span box, [[maybe_unused]] Span vrows) {
+    uint32_t wv[12];
+#pragma unroll
+    for (int i = 0; i < 12; ++i) wv[i] = MG_LD(reinterpret_cast<const uint32_t*>(src + ro(i)), box.p, box.n);
+    uint32_t lo[11], hi[11];
+#pragma unroll
+    for (int i = 0; i < 11; ++i) {
+        lo[i] = __byte_perm(wv[i], wv[i + 1], 0x5140);
+        hi[i] = __byte_perm(wv[i], wv[i + 1], 0x7362);
+    }
+    constexpr uint32_t T01 = kT0 | (kT1 << 16);
+    constexpr uint32_t T23 = kT2 | (kT1 << 16);
+    constexpr uint32_t T_4 = kT0 << 16;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        uint4 o;
+        o.x = __dp2a_lo(T01, lo[j], __dp2a_lo(T23, lo[j + 2], __dp2a_lo(T_4, lo[j + 3], rnd))) >> sh;
+        o.y = __dp2a_hi(T01, lo[j], __dp2a_hi(T23, lo[j + 2], __dp2a_hi(T_4, lo[j + 3], rnd))) >> sh;
+        o.z = __dp2a_lo(T01, hi[j], __dp2a_lo(T23, hi[j + 2], __dp2a_lo(T_4, hi[j + 3], rnd))) >> sh;
+        o.w = __dp2a_hi(T01, hi[j], __dp2a_hi(T23, hi[j + 2], __dp2a_hi(T_4, hi[j + 3], rnd))) >> sh;
+        MG_ST(reinterpret_cast<uint4*>(dst + j * SVW), o, vrows.p, vrows.n);
+    }
+}
+template <typename RowOff>
+__device__ __forceinline__ void vertical_oct(const uint16_t* src, RowOff ro, uint32_t* dst, uint32_t rnd,
+                                             int sh, [[maybe_unused]] Span box, [[maybe_unused]] Span vrows) {
+    uint32_t p[12][4];
+#pragma unroll
+    for (int i = 0; i < 12; ++i) unpack4_in(src + ro(i), box.p, box.n, p[i]);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        uint4 o;
+        o.x = vtap(p[j][0], p[j + 1][0], p[j + 2][0], p[j + 3][0], p[j + 4][0], rnd, sh);
+        o.y = vtap(p[j][1], p[j + 1][1], p[j + 2][1], p[j + 3][1], p[j + 4][1], rnd, sh);
+        o.z = vtap(p[j][2], p[j + 1][2], p[j + 2][2], p[j + 3][2], p[j + 4][2], rnd, sh);
+        o.w = vtap(p[j][3], p[j + 1][3], p[j + 2][3], p[j + 3][3], p[j + 4][3], rnd, sh);
+        MG_ST(reinterpret_cast<uint4*>(dst + j * SVW), o, vrows.p, vrows.n);
+    }
+}
 template <typename RowOff>
 __device__ __forceinline__ void vertical_quad(const uint16_t* src, RowOff ro, uint32_t* dst,
                                               uint32_t rnd, int sh, uint32_t (&center)[4],
@@ -161,17 +204,25 @@ __device__ __forceinline__ void vertical_sums(const uint16_t* src, RowOff ro, ui
         for (int i = 0; i < 4; ++i)
             x[j][i] = vsum(p[j][i], p[j + 1][i], p[j + 2][i], p[j + 3][i], p[j + 4][i]);
 }
-// Thread layout: each warp owns RPW = 8 output rows of the tile and runs them
-// in two halves of 4 rows through its own 4-row V buffer; 4 warps cover the
-// 32 rows.  Eight rows per warp halve the per-frame cost of stage waits,
-// reductions and loop control per pixel against four, and the 32 halo
-// values of a warp's rows then occupy every lane once.
+// Thread layout: each warp owns RPW = 8 output rows of the tile; 4 warps cover
+// the 32 rows.  The motion-only kernels run the vertical pass of all 8 rows at
+// once into the warp's 8-row V buffer (each of the 12 staged rows loaded and
+// interleaved once); the fused and motion_v2 kernels, whose stages fill more
+// shared memory, run two halves of 4 rows through a 4-row V buffer.  Eight
+// rows per warp halve the per-frame cost of stage waits, reductions and loop
+// control per pixel against four, and the 32 halo values of a warp's rows then
+// occupy every lane once.
 struct Shape {
     static constexpr int RPW = 8;                 // output rows per warp
     static constexpr int NWK = TH / RPW;          // warps per CTA
     static constexpr int NTK = NWK * 32;          // threads per CTA
     static constexpr int MINB = 4;                // resident CTAs per SM (<= 128 registers)
-    static constexpr int SV = NWK * 4 * SVW * 4;  // V buffers, bytes
+    // V rows per warp: the motion-only kernels run the vertical pass of all 8
+    // rows at once; the fused and motion_v2 kernels in two halves of 4
+    template <bool FUSED, bool V2>
+    static constexpr int VR = (!FUSED && !V2) ? 8 : 4;
+    template <bool FUSED, bool V2>
+    static constexpr int SV = NWK * VR<FUSED, V2> * SVW * 4;  // V buffers, bytes
     static constexpr int CRW = 16 / NWK;          // chroma rows per warp
     static constexpr int SPL = RPW;               // chroma samples per lane and plane
     static constexpr int LPR = 64 / SPL;          // lanes per chroma row
@@ -205,8 +256,9 @@ __global__ void __launch_bounds__(Shape::NTK, Shape::MINB)
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     // each warp owns output rows RPW w .. RPW w + RPW-1 of the tile; its V rows are private
-    uint32_t* sV = reinterpret_cast<uint32_t*>(smem + STAGES * STAGE) + warp * 4 * SVW;
-    [[maybe_unused]] const Span vrows{sV, 4 * SVW * sizeof(uint32_t)};   // this warp's V rows
+    constexpr int VR = SH::template VR<FUSED, V2>;   // V rows of one vertical pass
+    uint32_t* sV = reinterpret_cast<uint32_t*>(smem + STAGES * STAGE) + warp * VR * SVW;
+    [[maybe_unused]] const Span vrows{sV, VR * SVW * sizeof(uint32_t)};   // this warp's V rows
     // border tiles of every chunk first, interior tiles after them in row-major
     // order (tile_of_block)
     // this block's tile and frames (uniform chunks, or a split-tail launch)
@@ -441,11 +493,20 @@ __global__ void __launch_bounds__(Shape::NTK, Shape::MINB)
             uint32_t sad = 0;
             [[maybe_unused]] Acc sse_y = 0, sse_u = 0, sse_v = 0;
 #pragma unroll
-            for (int h = 0; h < RPW / 4; ++h) {
+            for (int h = 0; h < RPW / VR; ++h) {
                 if (h > 0) __syncwarp();   // the previous half has read the V rows
-                // ---- vertical pass of 4 rows (staged row r <-> y0 - 2 + r)
+                // ---- vertical pass of VR rows (staged row r <-> y0 - 2 + r)
                 [[maybe_unused]] uint32_t center[4];
-                if constexpr (V2) {
+                if constexpr (VR == 8) {
+                    const Pix* colv = reinterpret_cast<const Pix*>(st + off_vcol);
+                    const int r0 = RPW * warp;
+                    if (remap)
+                        vertical_oct(colv, [&](int i) { return MG_LD(&rowsrc[r0 + i], rowsrc, sizeof(rowsrc)); },
+                                     sV + 4 + 4 * lane, rnd, sh, box, vrows);
+                    else
+                        vertical_oct(colv, [=](int i) { return (r0 + i) * G::RAW_W; }, sV + 4 + 4 * lane, rnd, sh,
+                                     box, vrows);
+                } else if constexpr (V2) {
                     // V of prev - cur from this frame's sums and the previous frame's
                     uint32_t x[4][4];
                     const Pix* colv = reinterpret_cast<const Pix*>(st + off_vcol);
@@ -475,14 +536,14 @@ __global__ void __launch_bounds__(Shape::NTK, Shape::MINB)
                         vertical_quad(colv, [=](int i) { return (r0 + i) * G::RAW_W; },
                                       sV + 4 + 4 * lane, rnd, sh, center, box, vrows);
                 }
-                if ((halo_r >> 2) == h)
-                    MG_ST(&sV[(halo_r & 3) * SVW + 4 + halo_off], hv, vrows.p, vrows.n);
+                if (VR == 8 || (halo_r >> 2) == h)
+                    MG_ST(&sV[(VR == 8 ? halo_r : (halo_r & 3)) * SVW + 4 + halo_off], hv, vrows.p, vrows.n);
                 __syncwarp();
                 if (!INTERIOR && (pl || pr)) {
                     // the column mirror on V (the vertical pass works per column):
                     // x = -1, -2 <- 1, 2 on the left edge, x = w + k <- w - 2 - k on
-                    // the right edge, in this warp's 4 V rows; no source is a target
-                    if (lane < 16) {
+                    // the right edge, in this warp's VR V rows; no source is a target
+                    if (lane < 4 * VR) {
                         const int row = lane >> 2, which = lane & 3;
                         int dc = -3, sc = 0;
                         if (which < 2) {
@@ -501,8 +562,8 @@ __global__ void __launch_bounds__(Shape::NTK, Shape::MINB)
 
                 // ---- horizontal pass, SAD against B_prev, squared errors
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
-                    const int k = 4 * h + kk;
+                for (int kk = 0; kk < VR; ++kk) {
+                    const int k = VR * h + kk;
                     const uint32_t* v = sV + kk * SVW + 4 * q;
                     const uint4 A = MG_LD(reinterpret_cast<const uint4*>(v), vrows.p, vrows.n);
                     const uint4 Bq = MG_LD(reinterpret_cast<const uint4*>(v + 4), vrows.p, vrows.n);
@@ -759,7 +820,7 @@ template <typename Pix, bool FUSED, int STAGES, bool V2 = false>
 cudaError_t launch_tma_one(const TmaMaps& maps, const TileArgs& a, cudaStream_t s) {
     using G = Geo<Pix>;
     constexpr int STAGE = FUSED ? G::STAGE_FUSED : G::STAGE_MOTION;
-    constexpr int SMEM = STAGES * STAGE + Shape::SV + 128;
+    constexpr int SMEM = STAGES * STAGE + Shape::SV<FUSED, V2> + 128;
     static unsigned long long configured = 0;  // per device bit
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -837,12 +898,14 @@ cudaError_t launch_motion_tma(const TileArgs& a, bool fused, cudaStream_t s, int
     if (!ok) return cudaSuccess;  // the caller falls back to the generic kernel
     *used = true;
     *launches += 1;
-    // stages per CTA: as many as keep 4 CTAs (3 for 16-bit pairs) resident
+    // stages per CTA: as many as keep 4 CTAs resident beside the V buffers
+    // (3 for 8-bit pairs and 16-bit motion, 2 for 16-bit pairs, 4 for 8-bit
+    // motion)
     if (S == 1)
         return fused ? launch_tma_one<uint8_t, true, 3>(maps, a, s)
                      : launch_tma_one<uint8_t, false, 4>(maps, a, s);
     return fused ? launch_tma_one<uint16_t, true, 2>(maps, a, s)
-                 : launch_tma_one<uint16_t, false, 4>(maps, a, s);
+                 : launch_tma_one<uint16_t, false, 3>(maps, a, s);
 }
 
 cudaError_t launch_motion_v2_tma(const TileArgs& a, cudaStream_t s, int* launches, bool* used) {

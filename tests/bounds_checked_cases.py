@@ -25,6 +25,9 @@ FUSED_SIZES = [(4, 4), (67, 35), (130, 70), (258, 66)]
 # the allocation-free entry point: packed odd rows take the generic kernel,
 # 16-byte rows the TMA kernel
 NOALLOC_SIZES = [(67, 35), (256, 70), (130, 34)]
+# a launch shape whose tail is split (900 tiles of 128 x 32 over 608 resident
+# blocks: the last 292 tiles run in chunks of 4 frames), 8 frames per call
+SPLIT_SIZES = [(2560, 1440)]
 
 
 def _dev(a: np.ndarray, pad: bool):
@@ -118,6 +121,20 @@ def main() -> int:
                 if err != 0 or not np.array_equal(u64(out), want):
                     failures.append({"kind": "noalloc", "w": w, "h": h, "bpc": bpc, "pad": pad,
                                      "err": err, "got": u64(out).tolist(), "want": want.tolist()})
+    for (w, h) in SPLIT_SIZES:
+        for bpc in (8, 10):
+            fr = _frames(rng, 16, h, w, bpc)
+            d = _dev(fr, False)
+            want = o.motion_sad_sequence(fr, bpc).astype(np.uint64)
+            out = torch.zeros(16, dtype=torch.int64, device="cuda")
+            with iif.MotionContext(w, h, bpc) as ctx:
+                ctx.submit_batch(d[:8], out[:8])
+                ctx.submit_batch(d[8:], out[8:])
+                torch.cuda.synchronize()
+                err = ctx.device_error()
+            cases += 1
+            if err != 0 or not np.array_equal(u64(out), want):
+                failures.append({"kind": "split", "w": w, "h": h, "bpc": bpc, "err": err})
     print(json.dumps({"cases": cases, "failures": failures[:20], "n_failures": len(failures)}))
     return 0
 

@@ -4,8 +4,8 @@ buffer (a failed check skips the access and sets bit 1 of the device error
 word).  A child process loads that library and runs the cases of
 tests/bounds_checked_cases.py -- both kernel paths, odd, ragged and padded
 frames, 8/10/16 bits, motion, motion_v2 and the fused 4:2:0 form, each over
-two calls, and the allocation-free entry point -- and every result must match
-the oracle with the error word 0.
+two calls, the allocation-free entry point and a launch whose tail is split --
+and every result must match the oracle with the error word 0.
 This is the memory checker the tests use in place of a sanitizer."""
 import json
 import os
@@ -31,5 +31,5 @@ def test_bounds_checked_kernels_match_the_oracle():
     res = json.loads(r.stdout.strip().splitlines()[-1])
     from tests import bounds_checked_cases as bc
     assert res["cases"] == (2 * (len(bc.SIZES) * 3 * 2 * 2 + len(bc.FUSED_SIZES) * 2 * 2) +
-                            len(bc.NOALLOC_SIZES) * 2 * 2), res["cases"]
+                            len(bc.NOALLOC_SIZES) * 2 * 2 + len(bc.SPLIT_SIZES) * 2), res["cases"]
     assert res["n_failures"] == 0, res["failures"]
