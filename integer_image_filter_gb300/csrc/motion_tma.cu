@@ -91,10 +91,13 @@ __device__ __forceinline__ void vertical_quad(const uint8_t* src, RowOff ro, uin
 // loaded and interleaved (or unpacked) once, 8 V rows into the warp's V rows.
 template <typename RowOff>
 __device__ __forceinline__ void vertical_oct(const uint8_t* src, RowOff ro, uint32_t* dst, uint32_t rnd,
-                                             int sh, [[maybe_unused]] Span box, [[maybe_unused]] Span vrows) {
+                                             int sh, uint32_t (&center)[8], [[maybe_unused]] Span box,
+                                             [[maybe_unused]] Span vrows) {
     uint32_t wv[12];
 #pragma unroll
     for (int i = 0; i < 12; ++i) wv[i] = MG_LD(reinterpret_cast<const uint32_t*>(src + ro(i)), box.p, box.n);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) center[i] = wv[i + 2];
     uint32_t lo[11], hi[11];
 #pragma unroll
     for (int i = 0; i < 11; ++i) {
@@ -116,8 +119,11 @@ __device__ __forceinline__ void vertical_oct(const uint8_t* src, RowOff ro, uint
 }
 template <typename RowOff>
 __device__ __forceinline__ void vertical_oct(const uint16_t* src, RowOff ro, uint32_t* dst, uint32_t rnd,
-                                             int sh, [[maybe_unused]] Span box, [[maybe_unused]] Span vrows) {
+                                             int sh, uint32_t (&center)[8], [[maybe_unused]] Span box,
+                                             [[maybe_unused]] Span vrows) {
     uint32_t p[12][4];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) center[i] = 0;   // 16-bit SSE reloads its samples
 #pragma unroll
     for (int i = 0; i < 12; ++i) unpack4_in(src + ro(i), box.p, box.n, p[i]);
 #pragma unroll
@@ -207,22 +213,23 @@ __device__ __forceinline__ void vertical_sums(const uint16_t* src, RowOff ro, ui
 // Thread layout: each warp owns RPW = 8 output rows of the tile; 4 warps cover
 // the 32 rows.  The motion-only kernels run the vertical pass of all 8 rows at
 // once into the warp's 8-row V buffer (each of the 12 staged rows loaded and
-// interleaved once); the fused and motion_v2 kernels, whose stages fill more
-// shared memory, run two halves of 4 rows through a 4-row V buffer.  Eight
-// rows per warp halve the per-frame cost of stage waits, reductions and loop
-// control per pixel against four, and the 32 halo values of a warp's rows then
-// occupy every lane once.
+// interleaved once), and so does the 8-bit fused kernel with 2 stages; the
+// 16-bit fused and the motion_v2 kernels run two halves of 4 rows through a
+// 4-row V buffer.  Eight rows per warp halve the per-frame cost of stage
+// waits, reductions and loop control per pixel against four, and the 32 halo
+// values of a warp's rows then occupy every lane once.
 struct Shape {
     static constexpr int RPW = 8;                 // output rows per warp
     static constexpr int NWK = TH / RPW;          // warps per CTA
     static constexpr int NTK = NWK * 32;          // threads per CTA
     static constexpr int MINB = 4;                // resident CTAs per SM (<= 128 registers)
-    // V rows per warp: the motion-only kernels run the vertical pass of all 8
-    // rows at once; the fused and motion_v2 kernels in two halves of 4
-    template <bool FUSED, bool V2>
-    static constexpr int VR = (!FUSED && !V2) ? 8 : 4;
-    template <bool FUSED, bool V2>
-    static constexpr int SV = NWK * VR<FUSED, V2> * SVW * 4;  // V buffers, bytes
+    // V rows per warp: the motion-only and 8-bit fused kernels run the vertical
+    // pass of all 8 rows at once; the 16-bit fused and motion_v2 kernels in two
+    // halves of 4
+    template <typename Pix, bool FUSED, bool V2>
+    static constexpr int VR = (!V2 && !(FUSED && sizeof(Pix) == 2)) ? 8 : 4;
+    template <typename Pix, bool FUSED, bool V2>
+    static constexpr int SV = NWK * VR<Pix, FUSED, V2> * SVW * 4;  // V buffers, bytes
     static constexpr int CRW = 16 / NWK;          // chroma rows per warp
     static constexpr int SPL = RPW;               // chroma samples per lane and plane
     static constexpr int LPR = 64 / SPL;          // lanes per chroma row
@@ -256,7 +263,7 @@ __global__ void __launch_bounds__(Shape::NTK, Shape::MINB)
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     // each warp owns output rows RPW w .. RPW w + RPW-1 of the tile; its V rows are private
-    constexpr int VR = SH::template VR<FUSED, V2>;   // V rows of one vertical pass
+    constexpr int VR = SH::template VR<Pix, FUSED, V2>;   // V rows of one vertical pass
     uint32_t* sV = reinterpret_cast<uint32_t*>(smem + STAGES * STAGE) + warp * VR * SVW;
     [[maybe_unused]] const Span vrows{sV, VR * SVW * sizeof(uint32_t)};   // this warp's V rows
     // border tiles of every chunk first, interior tiles after them in row-major
@@ -496,16 +503,16 @@ __global__ void __launch_bounds__(Shape::NTK, Shape::MINB)
             for (int h = 0; h < RPW / VR; ++h) {
                 if (h > 0) __syncwarp();   // the previous half has read the V rows
                 // ---- vertical pass of VR rows (staged row r <-> y0 - 2 + r)
-                [[maybe_unused]] uint32_t center[4];
+                [[maybe_unused]] uint32_t center[VR];
                 if constexpr (VR == 8) {
                     const Pix* colv = reinterpret_cast<const Pix*>(st + off_vcol);
                     const int r0 = RPW * warp;
                     if (remap)
                         vertical_oct(colv, [&](int i) { return MG_LD(&rowsrc[r0 + i], rowsrc, sizeof(rowsrc)); },
-                                     sV + 4 + 4 * lane, rnd, sh, box, vrows);
+                                     sV + 4 + 4 * lane, rnd, sh, center, box, vrows);
                     else
                         vertical_oct(colv, [=](int i) { return (r0 + i) * G::RAW_W; }, sV + 4 + 4 * lane, rnd, sh,
-                                     box, vrows);
+                                     center, box, vrows);
                 } else if constexpr (V2) {
                     // V of prev - cur from this frame's sums and the previous frame's
                     uint32_t x[4][4];
@@ -820,7 +827,7 @@ template <typename Pix, bool FUSED, int STAGES, bool V2 = false>
 cudaError_t launch_tma_one(const TmaMaps& maps, const TileArgs& a, cudaStream_t s) {
     using G = Geo<Pix>;
     constexpr int STAGE = FUSED ? G::STAGE_FUSED : G::STAGE_MOTION;
-    constexpr int SMEM = STAGES * STAGE + Shape::SV<FUSED, V2> + 128;
+    constexpr int SMEM = STAGES * STAGE + Shape::SV<Pix, FUSED, V2> + 128;
     static unsigned long long configured = 0;  // per device bit
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -899,10 +906,9 @@ cudaError_t launch_motion_tma(const TileArgs& a, bool fused, cudaStream_t s, int
     *used = true;
     *launches += 1;
     // stages per CTA: as many as keep 4 CTAs resident beside the V buffers
-    // (3 for 8-bit pairs and 16-bit motion, 2 for 16-bit pairs, 4 for 8-bit
-    // motion)
+    // (4 for 8-bit motion, 3 for 16-bit motion, 2 for pairs)
     if (S == 1)
-        return fused ? launch_tma_one<uint8_t, true, 3>(maps, a, s)
+        return fused ? launch_tma_one<uint8_t, true, 2>(maps, a, s)
                      : launch_tma_one<uint8_t, false, 4>(maps, a, s);
     return fused ? launch_tma_one<uint16_t, true, 2>(maps, a, s)
                  : launch_tma_one<uint16_t, false, 3>(maps, a, s);
