@@ -46,10 +46,21 @@ def algorithmic_bytes_per_pair(w: int, h: int, bpc: int) -> int:
     return 2 * (w * h + 2 * cw * ch) * s
 
 
-def motion_kernel_name(bpc: int, v2: bool = False) -> str:
+def motion_tile_rows(w: int, h: int, batch: int, v2: bool = False) -> int:
+    """Tile height (32 or 16) of a batched motion-only launch on this device:
+    128 x 16 tiles when the 128 x 32 tiles fit in one wave of 4 per SM."""
+    import torch
+
+    import integer_image_filter_gb300 as iif
+    slots = 4 * torch.cuda.get_device_properties(0).multi_processor_count
+    return iif.motion_launch_shape(w, h, batch, slots, v2=v2)
+
+
+def motion_kernel_name(bpc: int, v2: bool = False, tile_rows: int = 32) -> str:
     """The key of a motion-only launch in the recorded profiles."""
-    return "motion_tma_kernel<%s, %s>" % ("uint8_t" if bpc == 8 else "uint16_t",
-                                            "motion_v2" if v2 else "motion")
+    return "motion_tma_kernel<%s, %s%s>" % ("uint8_t" if bpc == 8 else "uint16_t",
+                                              "motion_v2" if v2 else "motion",
+                                              "" if tile_rows == 32 else ", 16-row tiles")
 
 
 def numa_placement(host_tensor) -> dict:
@@ -456,7 +467,10 @@ def secondary_measurements(dev, stream, planes, n_pairs: int, w420: int, h420: i
                               "frames_per_step": n, "steps_timed": r["launches"],
                               "cuda_graph": graph,
                               "clocks": clocks.summary(r["t0"], r["t1"])}
-                res[batch]["roofline"] = seq_roofline(alg, ms, peak, peak_kind, motion_kernel_name(bpc), name,
+                rows = motion_tile_rows(w, h, batch)
+                res[batch]["tile_rows"] = rows
+                res[batch]["roofline"] = seq_roofline(alg, ms, peak, peak_kind,
+                                                      motion_kernel_name(bpc, tile_rows=rows), name,
                                                       n, res[batch]["clocks"].get("sm_mhz"), batch)
         return res
 
@@ -755,6 +769,7 @@ def run_sequence_workload(args):
         ms = e0.elapsed_time(e1) / args.steps
         if not args.graph:
             launches = (iif.motion_kernel_launch_count() - l0) / args.steps
+        rows = 32 if args.generic else motion_tile_rows(w, h, batch, args.v2)
         alg = w * h * s * n
         e2e = None
         if not args.v2 and not args.graph and not args.generic:
@@ -784,8 +799,10 @@ def run_sequence_workload(args):
                                  "w": w, "h": h, "bpc": bpc,
                                  "frames_per_step": n, "batch": batch,
                                  "launches_per_step": launches, "cuda_graph": bool(args.graph),
-                                 "kernel_path": "generic" if args.generic else "auto"},
-                      "roofline": seq_roofline(alg, ms, peak, peak_kind, motion_kernel_name(bpc, args.v2),
+                                 "kernel_path": "generic" if args.generic else "auto",
+                                 "tile_rows": rows},
+                      "roofline": seq_roofline(alg, ms, peak, peak_kind,
+                                               motion_kernel_name(bpc, args.v2, rows),
                                                args.workload, n, batch=batch), "e2e": e2e})
         ctx.close()
     for ln in lines:

@@ -283,10 +283,15 @@ MOTION_API int psnr_from_sse(uint64_t sse, uint64_t n_samples, int bpc, double* 
  * scratch the context owns with 16-byte-aligned rows (allocated by the first
  * such call, n frames' or pairs' worth up to motion_set_copy_limit, grown
  * when a call needs more, freed by motion_destroy); MOTION_PATH_GENERIC
- * always uses the generic kernel, which reads any layout in place.  Results
- * are identical on both paths. */
+ * always uses the generic kernel, which reads any layout in place;
+ * MOTION_PATH_TMA_32 and MOTION_PATH_TMA_16 are MOTION_PATH_AUTO with the
+ * tile height of the motion-only launches (motion and motion_v2) fixed at
+ * 128 x 32 or 128 x 16 instead of chosen per launch (motion_launch_shape).
+ * Results are identical on every path. */
 #define MOTION_PATH_AUTO 0
 #define MOTION_PATH_GENERIC 1
+#define MOTION_PATH_TMA_32 2
+#define MOTION_PATH_TMA_16 3
 MOTION_API int motion_set_kernel_path(motion_ctx* ctx, int path);
 
 /* The most scratch the copy of MOTION_PATH_AUTO may use for one launch, in
@@ -296,8 +301,8 @@ MOTION_API int motion_set_kernel_path(motion_ctx* ctx, int path);
 MOTION_API int motion_set_copy_limit(motion_ctx* ctx, size_t bytes);
 
 /* Diagnostic, host only, no GPU: the number of frame chunks (1..8) a batched
- * launch of n frames of w x h splits into on a device where `resident_ctas`
- * motion CTAs run at once (4 per SM on GB300: 608).  The launch sizing
+ * launch of n frames of w x h in 128 x 32 tiles splits into on a device where
+ * `resident_ctas` motion CTAs run at once (4 per SM on GB300: 608).  The launch sizing
  * follows "ADR-1226: Size the CUDA AIM CM launch by SM count, not by a fixed
  * rows-per-thread": chunks after the first re-blur one warm-up frame, and
  * the count balances that work against the idle part of the last wave.  This
@@ -324,22 +329,36 @@ MOTION_API int motion_plan_chunks(int w, int h, int n, int resident_ctas, int* c
  * tile_out). */
 MOTION_API int motion_tile_order(int w, int h, int chunks, long long block, int* tile_out);
 
+/* Diagnostic, host only, no GPU: the tile height of a batched motion-only
+ * launch (motion_v2 when v2 != 0; the fused 4:2:0 launches always take 32):
+ * 16 when its 128 x 32 tiles, in their motion_plan_chunks chunks, fit in one
+ * wave of `resident_ctas` resident CTAs (608 on GB300), else 32.  Under one
+ * wave each block runs a long serial chain of frames on SMs that are not
+ * full; 128 x 16 tiles give twice the blocks, each warp 4 output rows instead
+ * of 8, and 7 CTAs per SM instead of 4 (1080p x 16 frames: 1020 blocks of 16
+ * rows instead of 510 of 32).  *tile_rows (host int) receives 16 or 32.
+ * Errors: MOTION_ERR_INVALID_ARGUMENT (w, h outside 1..32768, n < 1,
+ * resident_ctas < 1, NULL tile_rows). */
+MOTION_API int motion_launch_shape(int w, int h, int n, int v2, int resident_ctas, int* tile_rows);
+
 /* Diagnostic, host only, no GPU: the blocks of a batched motion launch of n
- * frames of w x h on a device where `resident_ctas` motion blocks run at once
- * (4 per SM on GB300: 608).  The launch is sized by the SM count ("ADR-1226:
- * Size the CUDA AIM CM launch by SM count, not by a fixed rows-per-thread"):
- * the frames run in motion_plan_chunks chunks; a one-chunk launch of more than
- * a wave whose last wave would be at most half full keeps the tiles of its full
- * waves whole and splits the other tiles into chunks (of at least 4 frames but
- * the last, at most 8 per tile), so that the blocks that start last are short.  A chunk that
- * starts after frame 0 blurs the frame before it as well (no output for it).
- * *blocks_out (host) receives the block count; for 0 <= block < that count,
- * work_out (host int[4]) receives {tile column, tile row, first frame, end
- * frame} of that block (block < 0: the count only).  Errors:
- * MOTION_ERR_INVALID_ARGUMENT (w, h outside 1..32768, n < 1, resident_ctas <
- * 1, NULL blocks_out, block past the launch or NULL work_out).  The
- * allocation-free entry point, which continues in place, never splits. */
-MOTION_API int motion_launch_blocks(int w, int h, int n, int resident_ctas, long long block,
+ * frames of w x h in tiles of 128 x tile_rows (32 or 16, see
+ * motion_launch_shape) on a device where `resident_ctas` blocks of that tile
+ * run at once (GB300: 608 of 32 rows, 1064 of 16).  The launch is sized by
+ * the SM count ("ADR-1226: Size the CUDA AIM CM launch by SM count, not by a
+ * fixed rows-per-thread"): the frames run in motion_plan_chunks chunks; a
+ * one-chunk launch of more than a wave whose last wave would be at most half
+ * full keeps the tiles of its full waves whole and splits the other tiles
+ * into chunks (of at least 4 frames but the last, at most 8 per tile), so
+ * that the blocks that start last are short.  A chunk that starts after frame
+ * 0 blurs the frame before it as well (no output for it).  *blocks_out (host)
+ * receives the block count; for 0 <= block < that count, work_out (host
+ * int[4]) receives {tile column, tile row, first frame, end frame} of that
+ * block (block < 0: the count only).  Errors: MOTION_ERR_INVALID_ARGUMENT (w,
+ * h outside 1..32768, n < 1, tile_rows not 16 or 32, resident_ctas < 1, NULL
+ * blocks_out, block past the launch or NULL work_out).  The allocation-free
+ * entry point, which continues in place, never splits. */
+MOTION_API int motion_launch_blocks(int w, int h, int n, int tile_rows, int resident_ctas, long long block,
                                     int* work_out, long long* blocks_out);
 
 /* Test hook for allocation failures (not part of the method): the nth

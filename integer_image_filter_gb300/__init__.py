@@ -27,11 +27,12 @@ __all__ = [
     "psnr_sse_yuv420_batch", "motion_scores_from_sad", "psnr_from_sse",
     "motion_kernel_launch_count", "motion_strerror", "MotionContext", "EXPORTED_SYMBOLS",
     "motion_set_kernel_path", "motion_device_error", "MOTION_PATH_AUTO", "MOTION_PATH_GENERIC",
+    "MOTION_PATH_TMA_32", "MOTION_PATH_TMA_16",
     "motion_submit_batch_noalloc", "motion_set_stall_injection", "moment_sums_batch",
     "moments_from_sums", "motion_v2_submit_batch", "motion_plan_chunks", "motion_tile_order",
     "motion_inject_alloc_failure", "motion_submit_batch_host", "motion_set_copy_limit",
     "motion_noalloc_device_error", "motion_noalloc_set_stall_injection", "MOTION_ERR_DEVICE",
-    "motion_launch_blocks",
+    "motion_launch_blocks", "motion_launch_shape",
 ]
 
 EXPORTED_SYMBOLS = (
@@ -43,7 +44,7 @@ EXPORTED_SYMBOLS = (
     "motion_set_stall_injection", "moment_sums_batch", "moments_from_sums",
     "motion_v2_submit_batch", "motion_plan_chunks", "motion_tile_order", "motion_inject_alloc_failure",
     "motion_submit_batch_host", "motion_set_copy_limit", "motion_noalloc_device_error",
-    "motion_noalloc_set_stall_injection", "motion_launch_blocks",
+    "motion_noalloc_set_stall_injection", "motion_launch_blocks", "motion_launch_shape",
 )
 
 # Status of a call whose kernel set the device error word (include/motion.h).
@@ -97,8 +98,9 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
         "motion_set_copy_limit": ([P, Z], I),
         "motion_noalloc_device_error": ([P, ctypes.POINTER(I)], I),
         "motion_noalloc_set_stall_injection": ([I], I),
-        "motion_launch_blocks": ([I, I, I, I, ctypes.c_longlong, ctypes.POINTER(I),
+        "motion_launch_blocks": ([I, I, I, I, I, ctypes.c_longlong, ctypes.POINTER(I),
                                   ctypes.POINTER(ctypes.c_longlong)], I),
+        "motion_launch_shape": ([I, I, I, I, I, ctypes.POINTER(I)], I),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -435,14 +437,24 @@ def motion_tile_order(w: int, h: int, chunks: int, block: int) -> tuple[int, int
     return int(t[0]), int(t[1]), int(t[2])
 
 
-def motion_launch_blocks(w: int, h: int, n: int, resident_ctas: int, block: int = -1):
-    """Diagnostic: the block count of a batched motion launch and, for block
-    >= 0, that block's (tile column, tile row, first frame, end frame)."""
+def motion_launch_blocks(w: int, h: int, n: int, resident_ctas: int, block: int = -1, tile_rows: int = 32):
+    """Diagnostic: the block count of a batched motion launch in 128 x
+    tile_rows tiles and, for block >= 0, that block's (tile column, tile row,
+    first frame, end frame)."""
     out = (ctypes.c_int * 4)()
     cnt = ctypes.c_longlong()
-    _check(load_library().motion_launch_blocks(w, h, n, resident_ctas, block, out, ctypes.byref(cnt)),
+    _check(load_library().motion_launch_blocks(w, h, n, tile_rows, resident_ctas, block, out,
+                                               ctypes.byref(cnt)),
            "motion_launch_blocks")
     return int(cnt.value), (tuple(out) if block >= 0 else None)
+
+
+def motion_launch_shape(w: int, h: int, n: int, resident_ctas: int, v2: bool = False) -> int:
+    """Diagnostic: the tile height (16 or 32) of a batched motion-only launch."""
+    rows = ctypes.c_int()
+    _check(load_library().motion_launch_shape(w, h, n, int(bool(v2)), resident_ctas, ctypes.byref(rows)),
+           "motion_launch_shape")
+    return int(rows.value)
 
 
 def motion_plan_chunks(w: int, h: int, n: int, resident_ctas: int) -> int:
@@ -501,6 +513,8 @@ def motion_noalloc_set_stall_injection(on: bool) -> None:
 
 MOTION_PATH_AUTO = 0
 MOTION_PATH_GENERIC = 1
+MOTION_PATH_TMA_32 = 2      # the TMA kernel with 128 x 32 tiles for motion-only launches
+MOTION_PATH_TMA_16 = 3      # ... with 128 x 16 tiles
 
 
 def motion_set_kernel_path(ctx: int, path: int) -> None:

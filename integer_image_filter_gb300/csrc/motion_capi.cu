@@ -108,6 +108,7 @@ struct motion_ctx {
     // copy reads a frame's SAD and the word together
     int* d_err = nullptr;
     int force_generic = 0;          // diagnostics: always use the generic kernel
+    int force_rows = 0;             // diagnostics: TMA tile height of motion-only launches (0: chosen)
     int stall_injection = 0;        // test hook: stage waits that can never complete
     unsigned long long* d_slot = nullptr;   // [0]: single-submit SAD, [1]: error word
     unsigned long long* h_slot = nullptr;   // pinned readback of d_slot (16 bytes)
@@ -334,6 +335,7 @@ mg::TileArgs motion_args(motion_ctx* c, int n) {
     a.bprev_out = c->d_bprev[c->cur ^ 1];
     a.bprev_pitch = c->bprev_pitch;
     a.err = c->d_err;
+    a.force_rows = c->force_rows;
     if (c->stall_injection) {
         a.tx_extra = 16;               // the stage expects 16 bytes that never arrive
         a.wait_cycles = 1LL << 22;     // and gives up after about 2 ms
@@ -871,9 +873,10 @@ int psnr_from_sse(uint64_t sse, uint64_t n_samples, int bpc, double* mse, double
 }
 
 int motion_set_kernel_path(motion_ctx* c, int path) {
-    if (!c || (path != MOTION_PATH_AUTO && path != MOTION_PATH_GENERIC))
+    if (!c || path < MOTION_PATH_AUTO || path > MOTION_PATH_TMA_16)
         return MOTION_ERR_INVALID_ARGUMENT;
     c->force_generic = path == MOTION_PATH_GENERIC;
+    c->force_rows = path == MOTION_PATH_TMA_32 ? mg::kTileH : path == MOTION_PATH_TMA_16 ? mg::kShortTileH : 0;
     return MOTION_OK;
 }
 
@@ -895,11 +898,12 @@ int motion_tile_order(int w, int h, int chunks, long long block, int* tile_out) 
     return MOTION_OK;
 }
 
-int motion_launch_blocks(int w, int h, int n, int resident_ctas, long long block, int* work_out,
+int motion_launch_blocks(int w, int h, int n, int tile_rows, int resident_ctas, long long block, int* work_out,
                          long long* blocks_out) {
-    if (w < 1 || h < 1 || w > 32768 || h > 32768 || n < 1 || resident_ctas < 1 || !blocks_out)
+    if (w < 1 || h < 1 || w > 32768 || h > 32768 || n < 1 || resident_ctas < 1 || !blocks_out ||
+        (tile_rows != mg::kTileH && tile_rows != mg::kShortTileH))
         return MOTION_ERR_INVALID_ARGUMENT;
-    const int gx = (w + mg::kTileW - 1) / mg::kTileW, gy = (h + mg::kTileH - 1) / mg::kTileH;
+    const int gx = (w + mg::kTileW - 1) / mg::kTileW, gy = (h + tile_rows - 1) / tile_rows;
     const long long tiles = (long long)gx * gy;
     const int c = mg::plan_frame_chunks(tiles, resident_ctas, n, 8);
     const int chunk = (n + c - 1) / c;
@@ -914,7 +918,15 @@ int motion_launch_blocks(int w, int h, int n, int resident_ctas, long long block
     if (block < 0) return MOTION_OK;   // the count only
     if (block >= blocks || !work_out) return MOTION_ERR_INVALID_ARGUMENT;
     mg::block_work(w, h, gx, gy, gz, n, chunk, tiles_a, chunk_b, (int)block, &work_out[0], &work_out[1],
-                   &work_out[2], &work_out[3]);
+                   &work_out[2], &work_out[3], tile_rows);
+    return MOTION_OK;
+}
+
+int motion_launch_shape(int w, int h, int n, int v2, int resident_ctas, int* tile_rows) {
+    if (w < 1 || h < 1 || w > 32768 || h > 32768 || n < 1 || resident_ctas < 1 || !tile_rows)
+        return MOTION_ERR_INVALID_ARGUMENT;
+    const long long tiles = (long long)((w + mg::kTileW - 1) / mg::kTileW) * ((h + mg::kTileH - 1) / mg::kTileH);
+    *tile_rows = mg::prefer_short_tiles(tiles, resident_ctas, n, 8, v2 != 0) ? mg::kShortTileH : mg::kTileH;
     return MOTION_OK;
 }
 

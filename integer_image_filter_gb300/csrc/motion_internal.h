@@ -37,6 +37,7 @@ struct TileArgs {
     // grid whose first tiles_a blocks take tiles 0 .. tiles_a-1 whole and whose
     // other blocks take the remaining tiles in chunks of chunk_b frames
     int tiles_a, chunk_b;
+    int force_rows;               // motion-only TMA tile height: 0 chosen per launch, 32 or 16 forced
     long long wait_cycles;        // bound of every mbarrier wait (0: about one second)
     int tx_extra;                 // test hook: bytes a stage expects beyond its boxes (0)
     // motion_v2 (blur of prev - cur): the last raw frame of the previous call
@@ -81,10 +82,11 @@ cudaError_t launch_motion_v2_tile(const TileArgs& a, cudaStream_t s, int* launch
 // Whether the TMA kernel can take a's planes (16-byte strides and bases; the
 // driver's tensor-map encoder available).
 bool tma_usable(const TileArgs& a, bool fused);
-// The output tile of the motion kernels (the TMA kernel's TW x TH).
-constexpr int kTileW = 128, kTileH = 32;
+// The output tile of the motion kernels (the TMA kernel's TW x TH); the TMA
+// kernel's motion-only launches under one wave take tiles of kShortTileH rows.
+constexpr int kTileW = 128, kTileH = 32, kShortTileH = 16;
 // The tile and frame chunk of block `lin` (x fastest, then y, then chunk) of a
-// TMA launch over gx x gy tiles and gz chunks.  Tiles whose staged rows reach
+// TMA launch over gx x gy tiles of th rows and gz chunks.  Tiles whose staged rows reach
 // past the top or bottom frame edge (tile row 0 and the rows after niy), and
 // a partial last tile column, run the border copy of the frame loop; all other
 // tiles run the interior copy -- the left and right edge columns included,
@@ -95,8 +97,8 @@ constexpr int kTileW = 128, kTileH = 32;
 // copies of the loop at once would miss in its instruction cache, and in this
 // order only the first wave mixes them.  A bijection of [0, gx gy gz).
 __host__ __device__ inline void tile_of_block(int w, int h, int gx, int gy, int gz, int lin,
-                                              int* tx, int* ty, int* cz) {
-    const int niy = h >= kTileH + 2 ? (h - kTileH - 2) / kTileH : 0;   // interior rows 1..niy
+                                              int* tx, int* ty, int* cz, int th = kTileH) {
+    const int niy = h >= th + 2 ? (h - th - 2) / th : 0;   // interior rows 1..niy
     const int nfull = w / kTileW;                                       // full columns 0..nfull-1
     const int ni = nfull * niy, nb = gx * gy - ni;
     if (lin >= nb * gz) {
@@ -120,8 +122,8 @@ __host__ __device__ inline void tile_of_block(int w, int h, int gx, int gy, int 
         *tx = nfull + rr % per;
     }
 }
-// The work of block `lin` of a TMA launch over n frames of w x h: its tile
-// (tile_of_block order) and frames [*f_begin, *f_end).  Uniform launches
+// The work of block `lin` of a TMA launch over n frames of w x h in tiles of
+// th rows: its tile (tile_of_block order) and frames [*f_begin, *f_end).  Uniform launches
 // (tiles_a == 0) run gx x gy x gz blocks, each tile in gz chunks of `chunk`
 // frames.  Split-tail launches (tiles_a > 0) run tiles_a whole tiles first
 // and then the other tiles in chunks of chunk_b frames, chunk-major, so that
@@ -129,7 +131,7 @@ __host__ __device__ inline void tile_of_block(int w, int h, int gx, int gy, int 
 // 0 also blurs the frame before it (no output for that frame).
 __host__ __device__ inline void block_work(int w, int h, int gx, int gy, int gz, int n, int chunk,
                                            int tiles_a, int chunk_b, int lin, int* tx, int* ty,
-                                           int* f_begin, int* f_end) {
+                                           int* f_begin, int* f_end, int th = kTileH) {
     int cz = 0, len = chunk > 0 ? chunk : n;
     if (tiles_a > 0) {
         int t = lin, dz;
@@ -141,9 +143,9 @@ __host__ __device__ inline void block_work(int w, int h, int gx, int gy, int gz,
             t = tiles_a + (r - cz * tb);
             len = chunk_b;
         }
-        tile_of_block(w, h, gx, gy, 1, t, tx, ty, &dz);
+        tile_of_block(w, h, gx, gy, 1, t, tx, ty, &dz, th);
     } else {
-        tile_of_block(w, h, gx, gy, gz, lin, tx, ty, &cz);
+        tile_of_block(w, h, gx, gy, gz, lin, tx, ty, &cz, th);
     }
     *f_begin = cz * len;
     *f_end = *f_begin + len < n ? *f_begin + len : n;
@@ -161,6 +163,12 @@ long long plan_split_tail(long long tiles, long long slots, int n, int* tiles_a,
 // `slots` CTAs resident on the device at once; 1 <= result <= max_c; v2
 // selects the motion_v2 kernel's constants.
 int plan_frame_chunks(long long tiles, long long slots, int n, int max_c, bool v2 = false);
+// Whether a motion-only TMA launch takes tiles of kShortTileH rows (host
+// only): its tiles32 tiles of kTileH rows, in their planned chunks, fit in
+// one wave of slots32 resident CTAs.
+inline bool prefer_short_tiles(long long tiles32, long long slots32, int n, int max_c, bool v2) {
+    return tiles32 * plan_frame_chunks(tiles32, slots32, n, max_c, v2) <= slots32;
+}
 cudaError_t launch_sse(const SseArgs& a, cudaStream_t s, int sm_count, int* launches);
 
 // Copies of planes into rows the TMA can address (repitch.cu): n frames of

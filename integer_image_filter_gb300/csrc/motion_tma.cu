@@ -3,7 +3,8 @@
 // Tensor Memory Accelerator.
 //
 // Structure (GB300 / sm_103a):
-//  * One CTA owns a TW x TH output tile and walks the batch of frames (or one
+//  * One CTA owns a TW x TH output tile (128 x 32; 128 x 16 for motion-only
+//    launches that fit in one wave) and walks the batch of frames (or one
 //    chunk of it) in time order; B_prev of its tile stays in registers, so
 //    every frame is read from HBM once ("Making it fast: three rounds on one
 //    pipeline", Round 1 -- one kernel over all frames).
@@ -210,38 +211,48 @@ __device__ __forceinline__ void vertical_sums(const uint16_t* src, RowOff ro, ui
         for (int i = 0; i < 4; ++i)
             x[j][i] = vsum(p[j][i], p[j + 1][i], p[j + 2][i], p[j + 3][i], p[j + 4][i]);
 }
-// Thread layout: each warp owns RPW = 8 output rows of the tile; 4 warps cover
-// the 32 rows.  The motion-only kernels run the vertical pass of all 8 rows at
-// once into the warp's 8-row V buffer (each of the 12 staged rows loaded and
-// interleaved once), and so does the 8-bit fused kernel with 2 stages; the
-// 16-bit fused and the motion_v2 kernels run two halves of 4 rows through a
-// 4-row V buffer.  Eight rows per warp halve the per-frame cost of stage
-// waits, reductions and loop control per pixel against four, and the 32 halo
-// values of a warp's rows then occupy every lane once.
-struct Shape {
-    static constexpr int RPW = 8;                 // output rows per warp
-    static constexpr int NWK = TH / RPW;          // warps per CTA
+// Thread layout: 4 warps per CTA; on a tile of THT = 32 rows each warp owns
+// RPW = 8 output rows.  The motion-only kernels run the vertical pass of all
+// 8 rows at once into the warp's 8-row V buffer (each of the 12 staged rows
+// loaded and interleaved once), and so does the 8-bit fused kernel with 2
+// stages; the 16-bit fused and the motion_v2 kernels run two halves of 4 rows
+// through a 4-row V buffer.  Eight rows per warp halve the per-frame cost of
+// stage waits, reductions and loop control per pixel against four, and the 32
+// halo values of a warp's rows then occupy every lane once.  Motion-only
+// launches that fit in one wave of 32-row tiles run tiles of THT = 16 rows
+// instead (4 rows per warp, at most 72 registers, 7 CTAs per SM): twice the
+// blocks, each warp with half the work per frame.
+template <int THT>
+struct ShapeT {
+    static_assert(THT == 32 || THT == 16, "tiles are 32 or 16 rows high");
+    static constexpr int RPW = THT / 4;           // output rows per warp
+    static constexpr int NWK = THT / RPW;         // warps per CTA
     static constexpr int NTK = NWK * 32;          // threads per CTA
-    static constexpr int MINB = 4;                // resident CTAs per SM (<= 128 registers)
-    // V rows per warp: the motion-only and 8-bit fused kernels run the vertical
-    // pass of all 8 rows at once; the 16-bit fused and motion_v2 kernels in two
-    // halves of 4
+    // resident CTAs per SM: 4 (<= 128 registers) for 32-row tiles, 7 (<= 72) for 16
+    static constexpr int MINB = THT == 32 ? 4 : 7;
+    // V rows of one vertical pass: 8 for the motion-only and 8-bit fused
+    // kernels on 32-row tiles; 4 (two halves of a warp's 8 rows, or all of its
+    // 4) otherwise
     template <typename Pix, bool FUSED, bool V2>
-    static constexpr int VR = (!V2 && !(FUSED && sizeof(Pix) == 2)) ? 8 : 4;
+    static constexpr int VR = (RPW == 8 && !V2 && !(FUSED && sizeof(Pix) == 2)) ? 8 : 4;
     template <typename Pix, bool FUSED, bool V2>
     static constexpr int SV = NWK * VR<Pix, FUSED, V2> * SVW * 4;  // V buffers, bytes
     static constexpr int CRW = 16 / NWK;          // chroma rows per warp
     static constexpr int SPL = RPW;               // chroma samples per lane and plane
     static constexpr int LPR = 64 / SPL;          // lanes per chroma row
 };
+using Shape = ShapeT<32>;
 
 // V2: motion_v2, the blur of prev - cur (see vsum / vdiff); FUSED is false then.
-template <typename Pix, bool FUSED, int STAGES, bool V2>
-__global__ void __launch_bounds__(Shape::NTK, Shape::MINB)
+// THT: tile rows (32, or 16 for motion-only launches under one wave).
+template <typename Pix, bool FUSED, int STAGES, bool V2, int THT>
+__global__ void __launch_bounds__(ShapeT<THT>::NTK, ShapeT<THT>::MINB)
     motion_tma_kernel(const __grid_constant__ TmaMaps maps, const TileArgs a) {
     static_assert(!(FUSED && V2), "motion_v2 has no fused form");
-    using G = Geo<Pix>;
-    using SH = Shape;
+    static_assert(!FUSED || THT == 32, "the fused form runs 32-row tiles");
+    constexpr int TH = THT;
+    using G = Geo<Pix, THT>;
+    using SH = ShapeT<THT>;
     constexpr int NWK = SH::NWK, NTK = SH::NTK, RPW = SH::RPW;
     using Acc = typename SseAcc<Pix>::T;
     constexpr int STAGE = FUSED ? G::STAGE_FUSED : G::STAGE_MOTION;
@@ -259,7 +270,7 @@ __global__ void __launch_bounds__(Shape::NTK, Shape::MINB)
     __shared__ int wcount[2];
     // border tiles: element offset of the staged row that holds each staged
     // row after the mirror rule (frame-invariant, filled once)
-    __shared__ int rowsrc[Geo<Pix>::RAW_ROWS];
+    __shared__ int rowsrc[G::RAW_ROWS];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     // each warp owns output rows RPW w .. RPW w + RPW-1 of the tile; its V rows are private
@@ -272,7 +283,7 @@ __global__ void __launch_bounds__(Shape::NTK, Shape::MINB)
     int tx, ty, f_begin, f_end;
     block_work(a.w, a.h, (a.w + TW - 1) / TW, (a.h + TH - 1) / TH, gridDim.z, a.n, a.chunk, a.tiles_a,
                a.chunk_b, blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z), &tx, &ty, &f_begin,
-               &f_end);
+               &f_end, TH);
     const int x0 = tx * TW, y0 = ty * TH;
     const bool full_tile = (x0 + TW <= a.w) && (y0 + TH <= a.h);
     const bool pl = x0 == 0, pt = y0 == 0;
@@ -378,7 +389,8 @@ __global__ void __launch_bounds__(Shape::NTK, Shape::MINB)
     }
     // per-thread byte offsets inside a stage (the same for every stage)
     const int off_vcol = (G::HX + 4 * lane) * G::S;   // this lane's columns in staged row 0
-    const int halo_r = lane >> 2, halo_which = lane & 3;   // halo row 0..7, column
+    // halo row 0..RPW-1 and column; with 4-row warps lanes 16..31 repeat lanes 0..15
+    const int halo_r = (lane >> 2) % RPW, halo_which = lane & 3;
     const int halo_off = halo_which == 0 ? -2 : halo_which == 1 ? -1 : halo_which == 2 ? TW : TW + 1;
     // an interior tile on the left or right frame edge reads a halo column
     // outside the frame from its mirror inside it (x < 0 -> -x, x >= w ->
@@ -543,8 +555,8 @@ __global__ void __launch_bounds__(Shape::NTK, Shape::MINB)
                         vertical_quad(colv, [=](int i) { return (r0 + i) * G::RAW_W; },
                                       sV + 4 + 4 * lane, rnd, sh, center, box, vrows);
                 }
-                if (VR == 8 || (halo_r >> 2) == h)
-                    MG_ST(&sV[(VR == 8 ? halo_r : (halo_r & 3)) * SVW + 4 + halo_off], hv, vrows.p, vrows.n);
+                if ((lane >> 2) < RPW && halo_r / VR == h)
+                    MG_ST(&sV[(halo_r % VR) * SVW + 4 + halo_off], hv, vrows.p, vrows.n);
                 __syncwarp();
                 if (!INTERIOR && (pl || pr)) {
                     // the column mirror on V (the vertical pass works per column):
@@ -823,38 +835,54 @@ bool encode(CUtensorMap* m, int bytes_per_sample, const void* base, int w, int h
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <typename Pix, bool FUSED, int STAGES, bool V2 = false>
-cudaError_t launch_tma_one(const TmaMaps& maps, const TileArgs& a, cudaStream_t s) {
-    using G = Geo<Pix>;
+// Resident CTAs of one kernel instance on the current device (all SMs), with
+// its dynamic shared memory configured; cached per device (threads racing
+// here compute and store the same value).
+template <typename Pix, bool FUSED, int STAGES, bool V2, int THT>
+cudaError_t resident_slots(int* slots) {
+    using G = Geo<Pix, THT>;
+    using SH = ShapeT<THT>;
     constexpr int STAGE = FUSED ? G::STAGE_FUSED : G::STAGE_MOTION;
-    constexpr int SMEM = STAGES * STAGE + Shape::SV<Pix, FUSED, V2> + 128;
+    constexpr int SMEM = STAGES * STAGE + SH::template SV<Pix, FUSED, V2> + 128;
     static unsigned long long configured = 0;  // per device bit
+    static int slots_per_dev[64] = {0};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     const unsigned long long bit = 1ull << (dev & 63);
     if (!(__atomic_load_n(&configured, __ATOMIC_ACQUIRE) & bit)) {
-        e = cudaFuncSetAttribute(motion_tma_kernel<Pix, FUSED, STAGES, V2>,
+        e = cudaFuncSetAttribute(motion_tma_kernel<Pix, FUSED, STAGES, V2, THT>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
         if (e != cudaSuccess) return e;
         __atomic_fetch_or(&configured, bit, __ATOMIC_RELEASE);
     }
-    // Size the launch by the SM count (ADR-1226): plan_frame_chunks.
-    // resident CTAs on the whole device, per device (threads racing here
-    // compute and store the same value)
-    static int slots_per_sm[64] = {0};
-    int spm = __atomic_load_n(&slots_per_sm[dev & 63], __ATOMIC_RELAXED);
+    int spm = __atomic_load_n(&slots_per_dev[dev & 63], __ATOMIC_RELAXED);
     if (spm == 0) {
         int per_sm = 0, sms = 0;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, motion_tma_kernel<Pix, FUSED, STAGES, V2>,
-                                                          Shape::NTK, SMEM);
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, motion_tma_kernel<Pix, FUSED, STAGES, V2, THT>,
+                                                          SH::NTK, SMEM);
         if (e != cudaSuccess) return e;
         e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return e;
         spm = (per_sm > 0 ? per_sm : 1) * sms;
-        __atomic_store_n(&slots_per_sm[dev & 63], spm, __ATOMIC_RELAXED);
+        __atomic_store_n(&slots_per_dev[dev & 63], spm, __ATOMIC_RELAXED);
     }
+    *slots = spm;
+    return cudaSuccess;
+}
+
+template <typename Pix, bool FUSED, int STAGES, bool V2 = false, int THT = 32>
+cudaError_t launch_tma_one(const TmaMaps& maps, const TileArgs& a, cudaStream_t s) {
+    using G = Geo<Pix, THT>;
+    using SH = ShapeT<THT>;
+    constexpr int STAGE = FUSED ? G::STAGE_FUSED : G::STAGE_MOTION;
+    constexpr int SMEM = STAGES * STAGE + SH::template SV<Pix, FUSED, V2> + 128;
+    // Size the launch by the SM count (ADR-1226): plan_frame_chunks.
+    int spm = 0;
+    cudaError_t e = resident_slots<Pix, FUSED, STAGES, V2, THT>(&spm);
+    if (e != cudaSuccess) return e;
     TileArgs b = a;
+    constexpr int TH = THT;
     const long long tiles = (long long)((a.w + TW - 1) / TW) * ((a.h + TH - 1) / TH);
     // a launch that reads and writes the same resident plane keeps one chunk:
     // the last chunk's store must not overtake the first chunk's read
@@ -868,8 +896,23 @@ cudaError_t launch_tma_one(const TmaMaps& maps, const TileArgs& a, cudaStream_t 
         const long long blocks = plan_split_tail(tiles, spm, a.n, &b.tiles_a, &b.chunk_b);
         if (blocks > 0) grid = dim3((unsigned)blocks, 1, 1);
     }
-    motion_tma_kernel<Pix, FUSED, STAGES, V2><<<grid, Shape::NTK, SMEM, s>>>(maps, b);
+    motion_tma_kernel<Pix, FUSED, STAGES, V2, THT><<<grid, SH::NTK, SMEM, s>>>(maps, b);
     return cudaGetLastError();
+}
+
+// A motion-only launch whose 32-row tiles (in their planned chunks) fit in
+// one wave leaves every block a long serial chain of frames at a fraction of
+// the SMs' issue capacity; 16-row tiles with 4-row warps halve each warp's
+// work per frame and run twice the blocks, more of them resident per SM.
+template <typename Pix, int STAGES, bool V2>
+cudaError_t choose_short_tiles(const TileArgs& a, bool* out) {
+    int spm = 0;
+    const cudaError_t e = resident_slots<Pix, false, STAGES, V2, TH>(&spm);
+    if (e != cudaSuccess) return e;
+    const long long tiles = (long long)((a.w + TW - 1) / TW) * ((a.h + TH - 1) / TH);
+    const bool same_plane = !V2 && a.has_prev && a.bprev == a.bprev_out;
+    *out = prefer_short_tiles(tiles, spm, a.n, same_plane ? 1 : 8, V2);
+    return cudaSuccess;
 }
 
 }  // namespace
@@ -891,9 +934,16 @@ cudaError_t launch_motion_tma(const TileArgs& a, bool fused, cudaStream_t s, int
     if (a.n <= 0) return cudaSuccess;
     if (!tma_usable(a, fused)) return cudaSuccess;
     const int S = a.bpc == 8 ? 1 : 2;
+    // tile height first: the luma box of the tensor map is (tile rows + 4) high
+    bool short_tiles = !fused && a.force_rows == kShortTileH;
+    if (!fused && a.force_rows == 0) {
+        const cudaError_t e = S == 1 ? choose_short_tiles<uint8_t, 4, false>(a, &short_tiles)
+                                     : choose_short_tiles<uint16_t, 3, false>(a, &short_tiles);
+        if (e != cudaSuccess) return e;
+    }
     TmaMaps maps;
     std::memset(&maps, 0, sizeof(maps));
-    const int rawW = TW + 2 * (16 / S), rawH = TH + 4;
+    const int rawW = TW + 2 * (16 / S), rawH = (short_tiles ? kShortTileH : TH) + 4;
     bool ok = encode(&maps.raw, S, a.ref_y, a.w, a.h, a.n, a.pitch_y, a.stride_y, rawW, rawH);
     if (fused) {
         ok = ok && encode(&maps.dist, S, a.dist_y, a.w, a.h, a.n, a.pitch_y, a.stride_y, TW, TH);
@@ -905,13 +955,15 @@ cudaError_t launch_motion_tma(const TileArgs& a, bool fused, cudaStream_t s, int
     if (!ok) return cudaSuccess;  // the caller falls back to the generic kernel
     *used = true;
     *launches += 1;
-    // stages per CTA: as many as keep 4 CTAs resident beside the V buffers
+    // stages per CTA: as many as keep the CTAs resident beside the V buffers
     // (4 for 8-bit motion, 3 for 16-bit motion, 2 for pairs)
+    if (fused)
+        return S == 1 ? launch_tma_one<uint8_t, true, 2>(maps, a, s) : launch_tma_one<uint16_t, true, 2>(maps, a, s);
     if (S == 1)
-        return fused ? launch_tma_one<uint8_t, true, 2>(maps, a, s)
-                     : launch_tma_one<uint8_t, false, 4>(maps, a, s);
-    return fused ? launch_tma_one<uint16_t, true, 2>(maps, a, s)
-                 : launch_tma_one<uint16_t, false, 3>(maps, a, s);
+        return short_tiles ? launch_tma_one<uint8_t, false, 4, false, kShortTileH>(maps, a, s)
+                           : launch_tma_one<uint8_t, false, 4>(maps, a, s);
+    return short_tiles ? launch_tma_one<uint16_t, false, 3, false, kShortTileH>(maps, a, s)
+                       : launch_tma_one<uint16_t, false, 3>(maps, a, s);
 }
 
 cudaError_t launch_motion_v2_tma(const TileArgs& a, cudaStream_t s, int* launches, bool* used) {
@@ -920,17 +972,26 @@ cudaError_t launch_motion_v2_tma(const TileArgs& a, cudaStream_t s, int* launche
     if (!tma_usable(a, false)) return cudaSuccess;
     if (a.has_prev && (a.raw_pitch % 16 || ((uintptr_t)a.raw_prev & 15))) return cudaSuccess;
     const int S = a.bpc == 8 ? 1 : 2;
+    bool short_tiles = a.force_rows == kShortTileH;
+    if (a.force_rows == 0) {
+        const cudaError_t e = S == 1 ? choose_short_tiles<uint8_t, 4, true>(a, &short_tiles)
+                                     : choose_short_tiles<uint16_t, 4, true>(a, &short_tiles);
+        if (e != cudaSuccess) return e;
+    }
     TmaMaps maps;
     std::memset(&maps, 0, sizeof(maps));
-    const int rawW = TW + 2 * (16 / S), rawH = TH + 4;
+    const int rawW = TW + 2 * (16 / S), rawH = (short_tiles ? kShortTileH : TH) + 4;
     bool ok = encode(&maps.raw, S, a.ref_y, a.w, a.h, a.n, a.pitch_y, a.stride_y, rawW, rawH);
     if (a.has_prev)
         ok = ok && encode(&maps.prev, S, a.raw_prev, a.w, a.h, 1, a.raw_pitch, 0, rawW, rawH);
     if (!ok) return cudaSuccess;  // the caller falls back to the generic kernel
     *used = true;
     *launches += 1;
-    if (S == 1) return launch_tma_one<uint8_t, false, 4, true>(maps, a, s);
-    return launch_tma_one<uint16_t, false, 4, true>(maps, a, s);
+    if (S == 1)
+        return short_tiles ? launch_tma_one<uint8_t, false, 4, true, kShortTileH>(maps, a, s)
+                           : launch_tma_one<uint8_t, false, 4, true>(maps, a, s);
+    return short_tiles ? launch_tma_one<uint16_t, false, 3, true, kShortTileH>(maps, a, s)
+                       : launch_tma_one<uint16_t, false, 4, true>(maps, a, s);
 }
 
 }  // namespace mg

@@ -19,19 +19,19 @@ constexpr int SVW = TW + 8;        // V tile row pitch (uint32); col j <-> x = x
 // samples, so every box starts on a 16-byte boundary); the fused form adds the
 // distorted luma tile and the four 4:2:0 chroma tiles (ref U, dist U, ref V,
 // dist V).  Every region is a multiple of 128 bytes.
-template <typename Pix>
+template <typename Pix, int THT = TH>
 struct Geo {
     static constexpr int S = sizeof(Pix);
     static constexpr int HX = 16 / S;
     static constexpr int RAW_W = TW + 2 * HX;
-    static constexpr int RAW_ROWS = TH + 4;
+    static constexpr int RAW_ROWS = THT + 4;
     static constexpr int RAW_BYTES = RAW_ROWS * RAW_W * S;
-    static constexpr int DIST_BYTES = TH * TW * S;
-    static constexpr int CW = TW / 2, CH = TH / 2;
+    static constexpr int DIST_BYTES = THT * TW * S;
+    static constexpr int CW = TW / 2, CH = THT / 2;
     static constexpr int C_BYTES = CH * CW * S;
     static constexpr int STAGE_MOTION = RAW_BYTES;
     static constexpr int STAGE_FUSED = RAW_BYTES + DIST_BYTES + 4 * C_BYTES;
-    static constexpr int SV_BYTES = TH * SVW * 4;
+    static constexpr int SV_BYTES = THT * SVW * 4;
     static_assert(RAW_BYTES % 128 == 0 && DIST_BYTES % 128 == 0 && C_BYTES % 128 == 0,
                   "regions must keep 128-byte alignment");
 };

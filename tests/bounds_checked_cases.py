@@ -8,7 +8,9 @@ context's device error word.  Each case below runs both kernel paths (TMA and
 generic) on frames of odd, ragged and tile-straddling sizes, contiguous and
 with padded rows, at 8, 10 and 16 bits, over two calls (the second continues
 the sequence), and records a failure when a result differs from the oracle or
-the error word is not 0.  The allocation-free entry point runs the same way
+the error word is not 0; the motion cases also run with the tile height
+forced to 128 x 32 (the small frames here otherwise take 128 x 16 tiles).
+The allocation-free entry point runs the same way
 (start, then continue) with its own error word read after each case.  Prints
 one JSON line: {"cases": N, "failures": [...]}.
 """
@@ -60,7 +62,9 @@ def main() -> int:
     def u64(t):
         return t.cpu().numpy().astype(np.uint64)
 
-    for path in (iif.MOTION_PATH_AUTO, iif.MOTION_PATH_GENERIC):
+    # AUTO runs these small frames in 128 x 16 tiles (they fit in one wave of
+    # 128 x 32 tiles); TMA_32 runs the motion cases in 128 x 32 tiles as well
+    for path in (iif.MOTION_PATH_AUTO, iif.MOTION_PATH_GENERIC, iif.MOTION_PATH_TMA_32):
         for (w, h) in SIZES:
             for bpc in (8, 10, 16):
                 for pad in (False, True):
@@ -84,7 +88,7 @@ def main() -> int:
                             failures.append({"kind": "motion_v2" if v2 else "motion", "w": w, "h": h,
                                              "bpc": bpc, "pad": pad, "path": path, "err": err,
                                              "got": got.tolist(), "want": exp.tolist()})
-        for (w, h) in FUSED_SIZES:
+        for (w, h) in (FUSED_SIZES if path != iif.MOTION_PATH_TMA_32 else ()):
             for bpc in (8, 10):
                 for pad in (False, True):
                     n = 5

@@ -30,6 +30,6 @@ def test_bounds_checked_kernels_match_the_oracle():
     assert r.returncode == 0, r.stderr[-3000:]
     res = json.loads(r.stdout.strip().splitlines()[-1])
     from tests import bounds_checked_cases as bc
-    assert res["cases"] == (2 * (len(bc.SIZES) * 3 * 2 * 2 + len(bc.FUSED_SIZES) * 2 * 2) +
+    assert res["cases"] == (3 * len(bc.SIZES) * 3 * 2 * 2 + 2 * len(bc.FUSED_SIZES) * 2 * 2 +
                             len(bc.NOALLOC_SIZES) * 2 * 2 + len(bc.SPLIT_SIZES) * 2), res["cases"]
     assert res["n_failures"] == 0, res["failures"]

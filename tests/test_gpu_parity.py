@@ -166,6 +166,35 @@ def test_split_tail_launch(iif, oracle, bpc):
     assert np.array_equal(to_u64(out), oracle.motion_v2_sequence(frames, bpc))
 
 
+@pytest.mark.parametrize("bpc", [8, 10])
+def test_short_and_full_tiles_agree(iif, oracle, bpc):
+    """1080p frames in batches of 16 fit in one wave of 128 x 32 tiles, so
+    they run 128 x 16 tiles; batches of 32 (three chunks) run 128 x 32.  The
+    shape chosen is checked through motion_launch_shape on this device's SM
+    count, and both tile heights, chosen or forced, equal the oracle, for
+    motion and motion_v2 (ragged last tile row: 1080 = 67.5 x 16)."""
+    import torch
+    w, h, n = 1920, 1080, 32
+    slots = 4 * torch.cuda.get_device_properties(0).multi_processor_count
+    assert iif.motion_launch_shape(w, h, 16, slots) == 16
+    assert iif.motion_launch_shape(w, h, 32, slots) == 32
+    frames = synth.smooth_sequence(31 + bpc, n, w, h, 5, bpc=bpc)
+    want = oracle_sad(oracle, frames, bpc)
+    for batch, path in ((16, None), (32, None), (16, iif.MOTION_PATH_TMA_32), (32, iif.MOTION_PATH_TMA_16)):
+        assert np.array_equal(run_batches(iif, frames, bpc, batch, path=path), want), (batch, path)
+    want_v2 = oracle.motion_v2_sequence(frames, bpc)
+    d = to_dev(frames)
+    for path in (iif.MOTION_PATH_TMA_32, iif.MOTION_PATH_TMA_16):
+        out = dev_zeros(n)
+        with iif.MotionContext(w, h, bpc) as ctx:
+            ctx.set_kernel_path(path)
+            for s0 in range(0, n, 16):
+                ctx.submit_batch_v2(d[s0:s0 + 16], out[s0:s0 + 16])
+            torch.cuda.synchronize()
+            assert ctx.device_error() == 0
+        assert np.array_equal(to_u64(out), want_v2), path
+
+
 # --------------------------------------------------------------- shapes, layouts
 SIZES = [(w, h) for w in (3, 4, 5, 7, 9) for h in (3, 4, 6, 9)] + [
     (16, 16), (17, 33), (67, 35), (127, 31), (128, 32), (129, 33), (131, 70), (160, 36),
@@ -188,12 +217,14 @@ def test_tiny_and_ragged_frames(iif, oracle, bpc):
 @pytest.mark.parametrize("bpc", [8, 10, 16])
 def test_tma_and_generic_paths_on_aligned_layouts(iif, oracle, bpc):
     """16-byte-aligned pitches: the TMA kernel (mirrored reads on border tiles)
-    and the generic kernel (mirror applied at load) both equal the oracle."""
+    with 128 x 32 and with 128 x 16 tiles, and the generic kernel (mirror
+    applied at load), all equal the oracle."""
     rng = np.random.default_rng(100 + bpc)
     for (w, h) in SIZES:
         frames = synth.uniform_frames(int(rng.integers(1 << 30)), 4, w, h, bpc)
         want = oracle.motion_sad_sequence(frames, bpc)
-        for path in (iif.MOTION_PATH_AUTO, iif.MOTION_PATH_GENERIC):
+        for path in (iif.MOTION_PATH_AUTO, iif.MOTION_PATH_GENERIC, iif.MOTION_PATH_TMA_32,
+                     iif.MOTION_PATH_TMA_16):
             got = run_batches(iif, frames, bpc, 3, path=path, padded=True)
             assert np.array_equal(got, want), (w, h, bpc, path)
 

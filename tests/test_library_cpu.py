@@ -233,22 +233,30 @@ def test_launch_blocks_cover_every_frame_once(lib):
     import numpy as np
 
     import integer_image_filter_gb300 as iif
-    cases = [(3840, 2160, 32, 608), (3840, 2160, 16, 608), (3840, 2160, 50, 608), (1920, 1080, 16, 608),
-             (1920, 1080, 32, 608), (576, 324, 48, 608), (64, 48, 4, 608), (3840, 2160, 120, 608),
-             (4096, 2048, 9, 100), (1000, 700, 13, 7), (3, 3, 1, 1), (1366, 768, 8, 152)]
-    for (w, h, n, slots) in cases:
-        gx, gy = -(-w // 128), -(-h // 32)
-        count, _ = iif.motion_launch_blocks(w, h, n, slots)
+    cases = [(3840, 2160, 32, 608, 32), (3840, 2160, 16, 608, 32), (3840, 2160, 50, 608, 32),
+             (1920, 1080, 16, 608, 32), (1920, 1080, 32, 608, 32), (576, 324, 48, 608, 32),
+             (64, 48, 4, 608, 32), (3840, 2160, 120, 608, 32), (4096, 2048, 9, 100, 32),
+             (1000, 700, 13, 7, 32), (3, 3, 1, 1, 32), (1366, 768, 8, 152, 32),
+             # 128 x 16 tiles (1064 resident on GB300): 1080p x 16 in one wave, a split
+             # tail past one wave, ragged last tile rows
+             (1920, 1080, 16, 1064, 16), (576, 324, 48, 1064, 16), (1920, 1080, 32, 900, 16),
+             (1000, 700, 13, 7, 16), (3, 3, 1, 1, 16), (130, 17, 5, 1064, 16)]
+    for (w, h, n, slots, rows) in cases:
+        gx, gy = -(-w // 128), -(-h // rows)
+        count, _ = iif.motion_launch_blocks(w, h, n, slots, tile_rows=rows)
         seen = np.zeros((gy, gx, n), np.int32)
         lens = []
         for b in range(count):
-            _, (tx, ty, f0, f1) = iif.motion_launch_blocks(w, h, n, slots, b)
+            _, (tx, ty, f0, f1) = iif.motion_launch_blocks(w, h, n, slots, b, tile_rows=rows)
             assert 0 <= tx < gx and 0 <= ty < gy and 0 <= f0 < f1 <= n, (w, h, n, b)
             seen[ty, tx, f0:f1] += 1
             lens.append(f1 - f0)
         assert (seen == 1).all(), (w, h, n, slots)
         tiles = gx * gy
-        if count != tiles * -(-n // -(-n // iif.motion_plan_chunks(w, h, n, slots))):
+        if rows == 32:
+            c = iif.motion_plan_chunks(w, h, n, slots)
+            assert (count != tiles * -(-n // -(-n // c))) == (count > tiles and lens[0] == n)
+        if count > tiles and lens[0] == n:
             # a split tail: whole tiles first, then chunks of >= 4 frames
             rest = tiles % slots
             whole = tiles - rest
@@ -257,7 +265,7 @@ def test_launch_blocks_cover_every_frame_once(lib):
             assert 4 <= chunk < n, (w, h, n)
             # every chunk has that length but the one that ends at the last frame
             for b in range(whole, count):
-                _, (tx, ty, f0, f1) = iif.motion_launch_blocks(w, h, n, slots, b)
+                _, (tx, ty, f0, f1) = iif.motion_launch_blocks(w, h, n, slots, b, tile_rows=rows)
                 assert f1 - f0 == chunk or f1 == n, (w, h, n, b)
             assert 0 < 2 * rest <= slots
     # the 10-bit 4K batch of 32: 1824 whole tiles and 216 tiles in two halves
@@ -266,6 +274,34 @@ def test_launch_blocks_cover_every_frame_once(lib):
     assert iif.motion_launch_blocks(3840, 2160, 32, 608, 1824 + 216)[1][2:] == (16, 32)
     with pytest.raises(iif.MotionError):
         iif.motion_launch_blocks(3840, 2160, 32, 608, 1824 + 432)
+    with pytest.raises(iif.MotionError):
+        iif.motion_launch_blocks(1920, 1080, 16, 608, tile_rows=24)
+    # 1080p x 16 in 128 x 16 tiles: 1020 blocks of all 16 frames, one wave of 1064; the
+    # last block takes the last interior tile (rows 1..66 interior, 67 on the border)
+    assert iif.motion_launch_blocks(1920, 1080, 16, 1064, tile_rows=16)[0] == 1020
+    assert iif.motion_launch_blocks(1920, 1080, 16, 1064, 1019, tile_rows=16)[1] == (14, 66, 0, 16)
+
+
+def test_launch_shape(lib):
+    """Motion-only launches whose 128 x 32 tiles, in their planned chunks, fit in
+    one wave (608 resident blocks on GB300) take 128 x 16 tiles; the others,
+    motion_v2's two-chunk 1080p plan among them, keep 128 x 32."""
+    import integer_image_filter_gb300 as iif
+    shape = iif.motion_launch_shape
+    assert shape(1920, 1080, 16, 608) == 16           # 510 tiles, one chunk
+    assert shape(1920, 1080, 32, 608) == 32           # three chunks: 1530 blocks
+    assert shape(1920, 1080, 16, 608, v2=True) == 32  # motion_v2 plans two chunks
+    assert shape(3840, 2160, 32, 608) == 32           # 2040 tiles
+    assert shape(576, 324, 48, 608) == 16             # 55 tiles x 8 chunks = 440
+    assert shape(64, 48, 1, 608) == 16
+    assert shape(1920, 1080, 16, 500) == 32           # 510 tiles > 500
+    for (w, h, n) in ((1920, 1080, 16), (3840, 2160, 32), (576, 324, 48), (3, 3, 1)):
+        tiles = -(-w // 128) * -(-h // 32)
+        c = iif.motion_plan_chunks(w, h, n, 608)
+        assert (shape(w, h, n, 608) == 16) == (tiles * c <= 608)
+    for bad in ((0, 10, 1, 608), (10, 10, 0, 608), (10, 10, 1, 0), (40000, 10, 1, 608)):
+        with pytest.raises(iif.MotionError):
+            shape(*bad)
 
 
 def test_tile_order(lib):
