@@ -306,8 +306,10 @@ MOTION_API int motion_set_copy_limit(motion_ctx* ctx, size_t bytes);
  * follows "ADR-1226: Size the CUDA AIM CM launch by SM count, not by a fixed
  * rows-per-thread": chunks after the first re-blur one warm-up frame, and
  * the count balances that work against the idle part of the last wave.  This
- * is the plan of the motion and fused kernels; motion_v2 launches weigh a
- * partial last wave less (1080p x 16 frames: two chunks).
+ * is the plan of the motion and fused kernels' uniform launches (a launch
+ * that splits its tail instead, see motion_launch_blocks, runs its full waves
+ * in one chunk); motion_v2 launches weigh a partial last wave less (1080p x
+ * 16 frames: two chunks).
  * *chunks_out (host int) receives the count.  Errors:
  * MOTION_ERR_INVALID_ARGUMENT (w, h < 1, n < 0, resident_ctas < 1, NULL
  * chunks_out).  A launch that continues a sequence in place (the
@@ -346,11 +348,13 @@ MOTION_API int motion_launch_shape(int w, int h, int n, int v2, int resident_cta
  * motion_launch_shape) on a device where `resident_ctas` blocks of that tile
  * run at once (GB300: 608 of 32 rows, 1064 of 16).  The launch is sized by
  * the SM count ("ADR-1226: Size the CUDA AIM CM launch by SM count, not by a
- * fixed rows-per-thread"): the frames run in motion_plan_chunks chunks; a
- * one-chunk launch of more than a wave whose last wave would be at most half
- * full keeps the tiles of its full waves whole and splits the other tiles
- * into chunks (of at least 4 frames but the last, at most 8 per tile), so
- * that the blocks that start last are short.  A chunk that starts after frame
+ * fixed rows-per-thread"): a launch of more than a wave whose last wave
+ * would be at most half full keeps the tiles of its full waves whole (one
+ * chunk of all n frames) and splits the other tiles into chunks (of at least
+ * 4 frames but the last, at most 8 per tile), so that the blocks that start
+ * last are short (the fused 4K 4:2:0 launch of 50 pairs: 1824 whole tiles and
+ * 216 tiles in two chunks of 25); other launches run their frames in
+ * motion_plan_chunks chunks.  A chunk that starts after frame
  * 0 blurs the frame before it as well (no output for it).  *blocks_out (host)
  * receives the block count; for 0 <= block < that count, work_out (host
  * int[4]) receives {tile column, tile row, first frame, end frame} of that

@@ -905,19 +905,11 @@ int motion_launch_blocks(int w, int h, int n, int tile_rows, int resident_ctas, 
         return MOTION_ERR_INVALID_ARGUMENT;
     const int gx = (w + mg::kTileW - 1) / mg::kTileW, gy = (h + tile_rows - 1) / tile_rows;
     const long long tiles = (long long)gx * gy;
-    const int c = mg::plan_frame_chunks(tiles, resident_ctas, n, 8);
-    const int chunk = (n + c - 1) / c;
-    const int gz = (n + chunk - 1) / chunk;
-    int tiles_a = 0, chunk_b = 0;
-    long long blocks = tiles * gz;
-    if (c == 1) {
-        const long long split = mg::plan_split_tail(tiles, resident_ctas, n, &tiles_a, &chunk_b);
-        if (split > 0) blocks = split;
-    }
-    *blocks_out = blocks;
+    const mg::LaunchPlan p = mg::plan_launch(tiles, resident_ctas, n, false, false);
+    *blocks_out = p.blocks;
     if (block < 0) return MOTION_OK;   // the count only
-    if (block >= blocks || !work_out) return MOTION_ERR_INVALID_ARGUMENT;
-    mg::block_work(w, h, gx, gy, gz, n, chunk, tiles_a, chunk_b, (int)block, &work_out[0], &work_out[1],
+    if (block >= p.blocks || !work_out) return MOTION_ERR_INVALID_ARGUMENT;
+    mg::block_work(w, h, gx, gy, p.gz, n, p.chunk, p.tiles_a, p.chunk_b, (int)block, &work_out[0], &work_out[1],
                    &work_out[2], &work_out[3], tile_rows);
     return MOTION_OK;
 }

@@ -163,6 +163,17 @@ long long plan_split_tail(long long tiles, long long slots, int n, int* tiles_a,
 // `slots` CTAs resident on the device at once; 1 <= result <= max_c; v2
 // selects the motion_v2 kernel's constants.
 int plan_frame_chunks(long long tiles, long long slots, int n, int max_c, bool v2 = false);
+// The plan of a TMA launch (host only): chunks of `chunk` frames over gz
+// chunks (tiles_a == 0), or a split tail (tiles_a > 0, see block_work).  The
+// motion and fused kernels take the split tail whenever the one-chunk launch
+// has one (whole tiles keep their frames; only the last wave's tiles pay a
+// warm-up frame); motion_v2 takes it only when plan_frame_chunks picks one
+// chunk; a launch that continues in place (same_plane) always runs one chunk.
+struct LaunchPlan {
+    int chunk, gz, tiles_a, chunk_b;
+    long long blocks;
+};
+LaunchPlan plan_launch(long long tiles, long long slots, int n, bool v2, bool same_plane);
 // Whether a motion-only TMA launch takes tiles of kShortTileH rows (host
 // only): its tiles32 tiles of kTileH rows, in their planned chunks, fit in
 // one wave of slots32 resident CTAs.

@@ -802,6 +802,27 @@ long long plan_split_tail(long long tiles, long long slots, int n, int* tiles_a,
     return (tiles - rest) + rest * chunks;
 }
 
+LaunchPlan plan_launch(long long tiles, long long slots, int n, bool v2, bool same_plane) {
+    LaunchPlan p{n > 0 ? n : 1, 1, 0, 0, tiles};
+    if (same_plane) return p;
+    if (!v2) {
+        const long long b = plan_split_tail(tiles, slots, n, &p.tiles_a, &p.chunk_b);
+        if (b > 0) {
+            p.blocks = b;
+            return p;
+        }
+    }
+    const int c = plan_frame_chunks(tiles, slots, n, 8, v2);
+    p.chunk = (n + c - 1) / c;
+    p.gz = (n + p.chunk - 1) / p.chunk;
+    p.blocks = tiles * p.gz;
+    if (v2 && c == 1) {
+        const long long b = plan_split_tail(tiles, slots, n, &p.tiles_a, &p.chunk_b);
+        if (b > 0) p.blocks = b;
+    }
+    return p;
+}
+
 namespace {
 
 // The driver's tensor-map encoder, looked up once (a function-local static is
@@ -887,15 +908,12 @@ cudaError_t launch_tma_one(const TmaMaps& maps, const TileArgs& a, cudaStream_t 
     // a launch that reads and writes the same resident plane keeps one chunk:
     // the last chunk's store must not overtake the first chunk's read
     const bool same_plane = !V2 && a.has_prev && a.bprev == a.bprev_out;
-    const int best_c = plan_frame_chunks(tiles, spm, a.n, same_plane ? 1 : 8, V2);
-    b.chunk = (a.n + best_c - 1) / best_c;
-    dim3 grid((a.w + TW - 1) / TW, (a.h + TH - 1) / TH, (a.n + b.chunk - 1) / b.chunk);
-    b.tiles_a = 0;
-    b.chunk_b = 0;
-    if (best_c == 1 && !same_plane) {
-        const long long blocks = plan_split_tail(tiles, spm, a.n, &b.tiles_a, &b.chunk_b);
-        if (blocks > 0) grid = dim3((unsigned)blocks, 1, 1);
-    }
+    const LaunchPlan p = plan_launch(tiles, spm, a.n, V2, same_plane);
+    b.chunk = p.chunk;
+    b.tiles_a = p.tiles_a;
+    b.chunk_b = p.chunk_b;
+    const dim3 grid = p.tiles_a > 0 ? dim3((unsigned)p.blocks, 1, 1)
+                                    : dim3((a.w + TW - 1) / TW, (a.h + TH - 1) / TH, p.gz);
     motion_tma_kernel<Pix, FUSED, STAGES, V2, THT><<<grid, SH::NTK, SMEM, s>>>(maps, b);
     return cudaGetLastError();
 }
