@@ -757,8 +757,9 @@ __global__ void __launch_bounds__(ShapeT<THT>::NTK, ShapeT<THT>::MINB)
 // on GB300 with the block order of tile_of_block.  Motion: 1080p x 16 frames
 // is fastest at one chunk (three as fast, two 2 % slower), x 32 at three (4 %
 // over two); 4K x 16 and the 10-bit 4K x 32 at one; the 4K 4:2:0 x 50 pairs at
-// two (2 % over one and three).  motion_v2: 1080p x 16 and x 32 at two (one is
-// 13 % and 19 % slower), 10-bit 4K x 32 at one or two.
+// two (2 % over one and three; a split tail, which plan_launch takes first,
+// beats both by 1.7 %).  motion_v2: 1080p x 16 and x 32 at two (one is 13 % and
+// 19 % slower), 10-bit 4K x 32 at one or two.
 int plan_frame_chunks(long long tiles, long long slots, int n, int max_c, bool v2) {
     if (n <= 1 || tiles <= 0 || slots <= 0) return 1;
     int best_c = 1;
@@ -898,7 +899,7 @@ cudaError_t launch_tma_one(const TmaMaps& maps, const TileArgs& a, cudaStream_t 
     using SH = ShapeT<THT>;
     constexpr int STAGE = FUSED ? G::STAGE_FUSED : G::STAGE_MOTION;
     constexpr int SMEM = STAGES * STAGE + SH::template SV<Pix, FUSED, V2> + 128;
-    // Size the launch by the SM count (ADR-1226): plan_frame_chunks.
+    // Size the launch by the SM count (ADR-1226): plan_launch.
     int spm = 0;
     cudaError_t e = resident_slots<Pix, FUSED, STAGES, V2, THT>(&spm);
     if (e != cudaSuccess) return e;
