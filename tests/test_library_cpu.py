@@ -274,6 +274,13 @@ def test_launch_blocks_cover_every_frame_once(lib):
     assert iif.motion_launch_blocks(3840, 2160, 32, 608, 1824 + 216)[1][2:] == (16, 32)
     with pytest.raises(iif.MotionError):
         iif.motion_launch_blocks(3840, 2160, 32, 608, 1824 + 432)
+    # the fused 4:2:0 launch of 50 pairs takes the split tail ahead of two uniform
+    # chunks (the uniform plan alone would pick two)
+    assert iif.motion_plan_chunks(3840, 2160, 50, 608) == 2
+    assert iif.motion_launch_blocks(3840, 2160, 50, 608)[0] == 1824 + 2 * 216
+    assert iif.motion_launch_blocks(3840, 2160, 50, 608, 1823)[1][2:] == (0, 50)
+    assert iif.motion_launch_blocks(3840, 2160, 50, 608, 1824)[1][2:] == (0, 25)
+    assert iif.motion_launch_blocks(3840, 2160, 50, 608, 1824 + 216)[1][2:] == (25, 50)
     with pytest.raises(iif.MotionError):
         iif.motion_launch_blocks(1920, 1080, 16, 608, tile_rows=24)
     # 1080p x 16 in 128 x 16 tiles: 1020 blocks of all 16 frames, one wave of 1064; the
