@@ -584,8 +584,10 @@ def run_gpu(args):
     sus = sustained_launches(step, stream, min_seconds=args.sustain_seconds, min_launches=200)
     sus["clocks"] = clocks.summary(sus["t0"], sus["t1"])
     secondary = None
+    streams = None
     if ws == 1 and not args.no_secondary:
         secondary = secondary_measurements(dev, stream, planes, n, args.w, args.h, clocks)
+        streams = hbm_stream_ceilings()
     clocks.stop()
 
     # the same metric end to end: pinned host pictures -> device -> results on the host
@@ -661,7 +663,10 @@ def run_gpu(args):
                      "sustained": {k: sus[k] for k in ("launches", "seconds", "median_ms", "mean_ms",
                                                         "p10_ms", "p90_ms", "clocks")},
                      "alu": instruction_co_bound("motion_tma_kernel<uint8_t, fused>", WORKLOAD, kern_ms,
-                                                 (clk or {}).get("sm_mhz"))},
+                                                 (clk or {}).get("sm_mhz")),
+                     # the launch reads 1.25 GB and writes 16 MB: against this box's read-only
+                     # stream rate as well as the copy bandwidth of MEASURED_PEAKS.json
+                     "stream_ceilings": read_only_ceiling(streams, secondary, achieved)},
         "cpu_baseline": cpu,
         "e2e": {"value": ws * n * e2e_steps / e2e_s, "unit": "frames/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
@@ -987,6 +992,42 @@ def run_host_link(args):
     return 0
 
 
+def hbm_stream_ceilings() -> dict | None:
+    """HBM read-only, write-only and copy stream rates measured now on this
+    device (libpipe_rates_gb300.so, hbm_stream_gbs), or None when the probe
+    library cannot be built or a CUDA call failed."""
+    import ctypes
+
+    from integer_image_filter_gb300 import _build
+    try:
+        lib = ctypes.CDLL(_build.build_pipe_rates())
+    except Exception:
+        return None
+    out = {}
+    for kind, name in ((0, "read_only_gbs"), (1, "write_only_gbs"), (2, "copy_gbs")):
+        g = ctypes.c_double()
+        if lib.hbm_stream_gbs(kind, ctypes.byref(g)) != 0:
+            return None
+        out[name] = round(g.value, 1)
+    out["basis"] = ("hbm_stream_gbs (libpipe_rates_gb300.so): 16-byte streaming accesses over 4 GiB "
+                    "read / 4 GiB written / 2 GiB copied (read + write counted), best of 5 launches")
+    return out
+
+
+def read_only_ceiling(streams: dict | None, secondary: dict | None, achieved: float) -> dict | None:
+    """The stream rates of this run with the fused launch's fraction of the
+    fastest read-only stream measured in it: the probe's, or the stand-alone
+    SSE launch's (a read-only stream of the same pairs) when that was faster."""
+    if not streams:
+        return None
+    best, basis = streams["read_only_gbs"], "hbm_stream_gbs read probe"
+    sse = (secondary or {}).get("sse_yuv420_3840x2160_u8_pairs") or {}
+    if sse.get("gb_per_s", 0) > best:
+        best, basis = sse["gb_per_s"], "the stand-alone SSE launch of this run (read-only, same pairs)"
+    return dict(streams, read_only_best_gbs=round(best, 1), read_only_best_basis=basis,
+                frac_of_read_only=achieved / best)
+
+
 def run_pipe_rates(args):
     """The instruction-throughput microbenchmark (libpipe_rates_gb300.so):
     lane-operations per SM clock per SM of each instruction class the motion
@@ -1010,8 +1051,10 @@ def run_pipe_rates(args):
     if rc != 0:
         raise RuntimeError("pipe_rates_measure failed")
     rates = {lib.pipe_rates_name(i).decode(): round(out[i], 2) for i in range(n)}
+    streams = hbm_stream_ceilings()
     print(json.dumps({"metric": "lane-operations per SM clock per SM (shared loads: bytes)",
                       "rates": rates, "sms": torch.cuda.get_device_properties(0).multi_processor_count,
+                      "hbm_streams": streams,
                       "clocks": clocks.summary(),
                       "config": {"workload": "pipe_rates", "threads_per_sm": 1024,
                                  "chains_per_thread": 8}}), flush=True)

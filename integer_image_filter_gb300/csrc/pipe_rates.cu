@@ -1,6 +1,7 @@
 // pipe_rates.cu -- throughput of the instruction classes the motion kernels
-// run, measured on the device they run on (libpipe_rates_gb300.so; not part
-// of the motion library).  Each measurement is a kernel whose loop issues one
+// run, and the HBM read-only, write-only and copy stream rates, measured on
+// the device they run on (libpipe_rates_gb300.so; not part of the motion
+// library).  Each measurement is a kernel whose loop issues one
 // instruction class many times over independent dependency chains, so that
 // the pipe, not the latency of one chain, sets the rate.  Every block reads
 // the SM clock before and after its loop; the rate is the lane-operations of
@@ -162,6 +163,55 @@ int run(K kernel, int ops_per_iter_per_thread, int iters, int blocks_per_sm, dou
     return 0;
 }
 
+// ---- HBM streams: read-only, write-only and copy, 16 bytes per lane access,
+// four accesses in flight per thread, grid-stride over buffers far larger
+// than the L2 (of the variants measured -- eight accesses in flight, one
+// contiguous part per block -- the fastest read stream).
+__device__ __forceinline__ uint4 ld_stream(const uint4* p) {
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+
+__global__ void __launch_bounds__(256) hbm_read_kernel(const uint4* __restrict__ src, size_t n16, Out* out) {
+    const size_t stride = (size_t)gridDim.x * blockDim.x;
+    size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+    uint32_t acc = 0;
+    for (; i + 3 * stride < n16; i += 4 * stride) {
+        const uint4 a = ld_stream(src + i), b = ld_stream(src + i + stride);
+        const uint4 c = ld_stream(src + i + 2 * stride), d = ld_stream(src + i + 3 * stride);
+        acc ^= a.x ^ a.w ^ b.y ^ b.z ^ c.x ^ c.w ^ d.y ^ d.z;
+    }
+    for (; i < n16; i += stride) {
+        const uint4 a = ld_stream(src + i);
+        acc ^= a.x ^ a.w;
+    }
+    if (acc == 0x12345678u) out->sink = acc;
+}
+
+__global__ void __launch_bounds__(256) hbm_write_kernel(uint4* __restrict__ dst, size_t n16, uint32_t v) {
+    const size_t stride = (size_t)gridDim.x * blockDim.x;
+    const uint4 w = make_uint4(v, v + 1, v + 2, v + 3);
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += stride) dst[i] = w;
+}
+
+__global__ void __launch_bounds__(256) hbm_copy_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst,
+                                                       size_t n16) {
+    const size_t stride = (size_t)gridDim.x * blockDim.x;
+    size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+    for (; i + 3 * stride < n16; i += 4 * stride) {
+        const uint4 a = ld_stream(src + i), b = ld_stream(src + i + stride);
+        const uint4 c = ld_stream(src + i + 2 * stride), d = ld_stream(src + i + 3 * stride);
+        dst[i] = a;
+        dst[i + stride] = b;
+        dst[i + 2 * stride] = c;
+        dst[i + 3 * stride] = d;
+    }
+    for (; i < n16; i += stride) dst[i] = ld_stream(src + i);
+}
+
 }  // namespace
 
 // Number of measured classes and their names (static strings).
@@ -198,4 +248,46 @@ extern "C" __attribute__((visibility("default"))) int pipe_rates_measure(double*
     rc |= run(lds_kernel<4>, kUnroll * 2, it, bps, &w);
     out[12] = w * 16.0;
     return rc;
+}
+
+// HBM bandwidth of one stream kind on the current device: 0 read-only (4 GiB
+// read), 1 write-only (4 GiB written), 2 copy (2 GiB read and 2 GiB written;
+// both directions counted).  *gbs receives the best of 5 timed launches after
+// one warm-up, in GB/s (10^9 bytes).  Returns 0, or 1 when a CUDA call failed.
+extern "C" __attribute__((visibility("default"))) int hbm_stream_gbs(int kind, double* gbs) {
+    if (kind < 0 || kind > 2 || !gbs) return 1;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 1;
+    const size_t bytes = kind == 2 ? ((size_t)2 << 30) : ((size_t)4 << 30);
+    const size_t n16 = bytes / 16;
+    uint4 *a = nullptr, *b = nullptr;
+    Out* o = nullptr;
+    cudaEvent_t e0 = nullptr, e1 = nullptr;
+    int rc = 0;
+    if (cudaMalloc(&a, bytes) != cudaSuccess) rc = 1;
+    if (!rc && kind == 2 && cudaMalloc(&b, bytes) != cudaSuccess) rc = 1;
+    if (!rc && cudaMalloc(&o, sizeof(Out)) != cudaSuccess) rc = 1;
+    if (!rc && cudaMemset(a, 1, bytes) != cudaSuccess) rc = 1;
+    if (!rc && (cudaEventCreate(&e0) != cudaSuccess || cudaEventCreate(&e1) != cudaSuccess)) rc = 1;
+    float best = 1e30f;
+    const int grid = sms * 8;
+    for (int rep = 0; rep < 6 && !rc; ++rep) {
+        if (cudaEventRecord(e0) != cudaSuccess) { rc = 1; break; }
+        if (kind == 0) hbm_read_kernel<<<grid, 256>>>(a, n16, o);
+        else if (kind == 1) hbm_write_kernel<<<grid, 256>>>(a, n16, (uint32_t)rep);
+        else hbm_copy_kernel<<<grid, 256>>>(a, b, n16);
+        if (cudaEventRecord(e1) != cudaSuccess || cudaEventSynchronize(e1) != cudaSuccess) { rc = 1; break; }
+        float ms = 0.f;
+        if (cudaEventElapsedTime(&ms, e0, e1) != cudaSuccess) { rc = 1; break; }
+        if (rep > 0 && ms < best) best = ms;
+    }
+    if (e0) cudaEventDestroy(e0);
+    if (e1) cudaEventDestroy(e1);
+    cudaFree(a);
+    cudaFree(b);
+    cudaFree(o);
+    if (rc || best >= 1e29f) return 1;
+    *gbs = (double)(kind == 2 ? 2 * bytes : bytes) / (best * 1e-3) / 1e9;
+    return 0;
 }
