@@ -241,7 +241,6 @@ struct ShapeT {
     static constexpr int SPL = RPW;               // chroma samples per lane and plane
     static constexpr int LPR = 64 / SPL;          // lanes per chroma row
 };
-using Shape = ShapeT<32>;
 
 // V2: motion_v2, the blur of prev - cur (see vsum / vdiff); FUSED is false then.
 // THT: tile rows (32, or 16 for motion-only launches under one wave).
