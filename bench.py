@@ -609,6 +609,16 @@ def run_gpu(args):
         e2e_s = float(t.item())
     h2d = sum(p.numel() * p.element_size() for p in pinned)
     numa = numa_placement(pinned[0])
+    # this box's pinned host->device rate now (a plain copy of the reference luma
+    # onto its own device copy, best of 3): the ceiling of the end-to-end rate
+    link = 0.0
+    for _ in range(3):
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        c0.record(stream)
+        planes[0].copy_(pinned[0], non_blocking=True)
+        c1.record(stream)
+        torch.cuda.synchronize(dev)
+        link = max(link, pinned[0].numel() * pinned[0].element_size() / (c0.elapsed_time(c1) * 1e-3) / 1e9)
     d2h = h_sad.nbytes + h_sse.nbytes
     dev_sad = sad.cpu().numpy().astype(np.uint64)
     dev_sse = sse.cpu().numpy().astype(np.uint64)
@@ -670,7 +680,9 @@ def run_gpu(args):
         "cpu_baseline": cpu,
         "e2e": {"value": ws * n * e2e_steps / e2e_s, "unit": "frames/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "host_link_gbs": h2d * e2e_steps / e2e_s / 1e9, "numa": numa},
+                "host_link_gbs": h2d * e2e_steps / e2e_s / 1e9,
+                "link_h2d_ceiling_gbs": link, "frac_of_link": h2d * e2e_steps / e2e_s / 1e9 / link,
+                "numa": numa},
         "gpu_launches": launches,
         "clocks": clk,
         "secondary": secondary,
