@@ -195,6 +195,35 @@ def test_short_and_full_tiles_agree(iif, oracle, bpc):
         assert np.array_equal(to_u64(out), want_v2), path
 
 
+@pytest.mark.parametrize("bpc", [8, 10])
+def test_short_tiles_with_split_tail(iif, oracle, bpc):
+    """1920x1280 in batches of 16: its 600 tiles of 128 x 32 fit in one wave,
+    so it runs 1200 tiles of 128 x 16, more than the 1064 that are resident at
+    once on GB300: the launch splits its tail (the 16-row plan checked through
+    motion_launch_shape and motion_launch_blocks on this device's SM count).
+    Two calls against the oracle, motion and motion_v2."""
+    import torch
+    w, h, n, batch = 1920, 1280, 32, 16
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert iif.motion_launch_shape(w, h, batch, 4 * sms) == 16
+    tiles16 = (w // 128) * (h // 16)
+    count, _ = iif.motion_launch_blocks(w, h, batch, 7 * sms, tile_rows=16)
+    if tiles16 > 7 * sms and 0 < 2 * (tiles16 % (7 * sms)) <= 7 * sms:
+        assert count > tiles16, "the 16-row launch splits its tail"
+    frames = synth.uniform_frames(91 + bpc, n, w, h, bpc)
+    want = oracle_sad(oracle, frames, bpc)
+    assert np.array_equal(run_batches(iif, frames, bpc, batch), want)
+    d = to_dev(frames)
+    out = dev_zeros(n)
+    with iif.MotionContext(w, h, bpc) as ctx:
+        ctx.set_kernel_path(iif.MOTION_PATH_TMA_16)
+        for s0 in range(0, n, batch):
+            ctx.submit_batch_v2(d[s0:s0 + batch], out[s0:s0 + batch])
+        torch.cuda.synchronize()
+        assert ctx.device_error() == 0
+    assert np.array_equal(to_u64(out), oracle.motion_v2_sequence(frames, bpc))
+
+
 # --------------------------------------------------------------- shapes, layouts
 SIZES = [(w, h) for w in (3, 4, 5, 7, 9) for h in (3, 4, 6, 9)] + [
     (16, 16), (17, 33), (67, 35), (127, 31), (128, 32), (129, 33), (131, 70), (160, 36),
