@@ -408,7 +408,6 @@ __global__ void __launch_bounds__(ShapeT<THT>::NTK, ShapeT<THT>::MINB)
     const int off_dist = G::RAW_BYTES + ((RPW * warp) * TW + 4 * q) * G::S;     // row k: + k TW S
     const int off_chroma = G::RAW_BYTES + G::DIST_BYTES +
                            ((SH::CRW * warp + lane / SH::LPR) * G::CW + SH::SPL * (lane % SH::LPR)) * G::S;
-    bool timed_out = false;
     // lane j holds the warp's sums of frame 32 m + j of the current window
     uint32_t acc_s = 0;
     [[maybe_unused]] Win acc_y = 0, acc_u = 0, acc_v = 0;
@@ -467,7 +466,6 @@ __global__ void __launch_bounds__(ShapeT<THT>::NTK, ShapeT<THT>::MINB)
             const int s = l % STAGES;
             const unsigned parity = (unsigned)(l / STAGES) & 1u;
             const bool ok = mbar_wait_bounded(&full[s], parity, wait_cycles);
-            timed_out |= !ok;
             unsigned char* st = smem + s * STAGE;
             [[maybe_unused]] const Span box{st, (size_t)G::RAW_BYTES};   // the staged luma box
             // the stage of frame l-1 takes frame l+STAGES-1 as soon as every warp
@@ -476,8 +474,8 @@ __global__ void __launch_bounds__(ShapeT<THT>::NTK, ShapeT<THT>::MINB)
                 const int sp = (l - 1) % STAGES;
                 if (mbar_wait_bounded(&empty[sp], (unsigned)((l - 1) / STAGES) & 1u, wait_cycles))
                     issue(l + STAGES - 1);
-                else
-                    timed_out = true;
+                else if (a.err)
+                    atomicOr(a.err, 1);   // never released: the warps waiting for its refill time out too
             }
             // a stage that never landed: this warp records it and leaves (the
             // others then run out of stages and leave too)
