@@ -472,10 +472,10 @@ __global__ void __launch_bounds__(ShapeT<THT>::NTK, ShapeT<THT>::MINB)
             // has released it
             if (tid == 0 && l >= 1 && l + STAGES - 1 < cnt) {
                 const int sp = (l - 1) % STAGES;
+                // (a stage never released is left alone: the warps that wait for
+                // its refill time out and report it)
                 if (mbar_wait_bounded(&empty[sp], (unsigned)((l - 1) / STAGES) & 1u, wait_cycles))
                     issue(l + STAGES - 1);
-                else if (a.err)
-                    atomicOr(a.err, 1);   // never released: the warps waiting for its refill time out too
             }
             // a stage that never landed: this warp records it and leaves (the
             // others then run out of stages and leave too)
