@@ -43,9 +43,12 @@ def _thin(prof_row, wide):
     return np.repeat(prof_row[None, :], 3, axis=0) if wide else np.repeat(prof_row[:, None], 3, axis=1)
 
 
+@pytest.mark.parametrize("path", ["auto", "tma32", "tma16"])
 @pytest.mark.parametrize("bpc", [8, 10])
 @pytest.mark.parametrize("wide", [True, False])
-def test_motion_and_v2_at_the_largest_side(iif, oracle, bpc, wide):
+def test_motion_and_v2_at_the_largest_side(iif, oracle, bpc, wide, path):
+    """Both tile heights (the wide frame chooses 128 x 16 tiles, the tall one
+    128 x 32; each is also forced to the other)."""
     import torch
     w, h = (MAX, 64) if wide else (64, MAX)
     n = 3
@@ -64,6 +67,8 @@ def test_motion_and_v2_at_the_largest_side(iif, oracle, bpc, wide):
     d = to_dev(frames)
     out, out2 = dev_zeros(n), dev_zeros(n)
     with iif.MotionContext(w, h, bpc) as ctx:
+        ctx.set_kernel_path({"auto": iif.MOTION_PATH_AUTO, "tma32": iif.MOTION_PATH_TMA_32,
+                             "tma16": iif.MOTION_PATH_TMA_16}[path])
         ctx.submit_batch(d, out)
         ctx.submit_batch_v2(d, out2)
         torch.cuda.synchronize()

@@ -34,12 +34,17 @@ def _padded(a):
 
 @pytest.mark.parametrize("case", hand_worked_cases(), ids=lambda c: c["name"])
 @pytest.mark.parametrize("padded", [False, True])
-def test_hand_worked_on_gpu(iif, case, padded):
+@pytest.mark.parametrize("rows", [16, 32])
+def test_hand_worked_on_gpu(iif, case, padded, rows):
+    """The hand-worked values on the TMA kernel with 128 x 16 and 128 x 32
+    tiles, from padded rows and from packed 6-sample rows (copied into aligned
+    rows first)."""
     import torch
     fr = impulse_frames(case)
     d = _padded(fr) if padded else to_dev(fr)
     out = torch.zeros(2, dtype=torch.int64, device="cuda")
     with iif.MotionContext(6, 6, 8) as ctx:
+        ctx.set_kernel_path(iif.MOTION_PATH_TMA_16 if rows == 16 else iif.MOTION_PATH_TMA_32)
         ctx.submit_batch(d, out)
         torch.cuda.synchronize()
         assert ctx.device_error() == 0
